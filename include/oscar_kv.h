@@ -1,0 +1,220 @@
+/*
+ * oscar_kv.h -- C ABI of the GB300 (sm_103a) INT2 rotated paged KV cache.
+ *
+ * The method is OSCAR-style INT2 KV caching as described on the axbrief.com page
+ * "Together AI's OSCAR breaks the 2-bit KV cache accuracy barrier":
+ *   - section "attention-statistics rotation + Triton kernels": keys are rotated by
+ *     R_K = U_Q * H_Had * P_br (U_Q = eigenvectors of the query covariance
+ *     C_Q = (1/N) sum_n q_n^T q_n, H_Had the normalised 128-point Hadamard, P_br the
+ *     bit-reversal permutation); the write path clips each token with c_K = 0.96 /
+ *     c_V = 0.92 and quantises it per token to asymmetric INT2 in groups of
+ *     G_K = 64 channels; the read path unpacks, dequantises and inverse-rotates
+ *     inside one fused attention pass with no extra memory traffic;
+ *   - section "attention-statistics rotation + Triton kernels", last paragraph: the
+ *     value rotation R_V is absorbed offline into the projection weights, so values
+ *     are written unrotated;
+ *   - opening paragraph and section "OSCAR release": sink tokens and the recent
+ *     window stay in BF16 (0.24% of a 128K context);
+ * and on the techllm.github.io page "KV cache compression: TurboQuant, OSCAR,
+ * EpiCache", section "OSCAR": a mixed-precision paged cache (recent tokens BF16,
+ * older history INT2).
+ *
+ * Conventions for every entry point:
+ *   - Device pointers are CUDA global-memory addresses on the current device; host
+ *     pointers are plain CPU memory.  Each argument says which it is.
+ *   - The caller allocates and frees ALL device memory (buffer sizes come from the
+ *     *_bytes() queries).  The library allocates only its host-side handle.
+ *   - Calls that take a stream enqueue their GPU work on it and return without
+ *     waiting, unless stated otherwise.  `stream` is a cudaStream_t passed as void*
+ *     (NULL = the legacy default stream).
+ *   - Return value: OSCAR_OK (0) or a negative OSCAR_E* code.  Argument, capacity and
+ *     alignment errors are detected on the host before anything is enqueued, and
+ *     leave the cache unchanged.  OSCAR_ECUDA reports a CUDA launch or copy error;
+ *     oscar_last_cuda_error() gives the CUDA error code.
+ *   - One cache is used from one host thread and one stream at a time.
+ *   - Inputs are assumed finite; NaN or Inf in keys, values or queries gives
+ *     undefined codes and outputs (never out-of-bounds memory access).
+ *   - Head mapping (grouped-query attention): query head hq reads KV head hq / G,
+ *     G = num_q_heads / num_kv_heads.
+ */
+#ifndef OSCAR_KV_H
+#define OSCAR_KV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define OSCAR_OK 0
+#define OSCAR_EINVAL (-1)     /* bad argument or shape */
+#define OSCAR_ENOPAGES (-2)   /* the page pool or a page-table row is full */
+#define OSCAR_EWORKSPACE (-3) /* workspace missing or too small */
+#define OSCAR_ECUDA (-4)      /* a CUDA call failed */
+#define OSCAR_EALIGN (-5)     /* a device pointer is not 16-byte aligned */
+#define OSCAR_ERANGE (-6)     /* a request index or position is out of range */
+
+#define OSCAR_DTYPE_F32 0
+#define OSCAR_DTYPE_BF16 1
+
+/* Fixed geometry of this implementation. */
+#define OSCAR_HEAD_DIM 128
+#define OSCAR_PAGE_TOKENS 64   /* INT2 tokens per page */
+#define OSCAR_GROUP 64         /* channels per quantisation group */
+#define OSCAR_MAX_GQA 16       /* largest num_q_heads / num_kv_heads */
+/* Bytes of one (page, KV head) block: K codes 64x32, K scale/min 64x8,
+ * V codes 128x16 (channel-major), V scale/min 64x8. */
+#define OSCAR_PAGE_HEAD_BYTES 5120
+
+typedef struct {
+    int32_t batch;             /* requests (rows of the page table), >= 1 */
+    int32_t num_kv_heads;      /* >= 1 */
+    int32_t num_q_heads;       /* num_kv_heads * G, G in {1..8, 12, 16} */
+    int32_t head_dim;          /* must be 128 */
+    int32_t page_size;         /* must be 64 */
+    int32_t group_size;        /* must be 64 */
+    int32_t sink;              /* BF16 sink tokens, must be 64 */
+    int32_t window;            /* BF16 recent-window tokens, must be 256 */
+    int32_t max_pages_total;   /* physical INT2 pages in the pool, >= 1 */
+    int32_t max_pages_per_seq; /* INT2 pages one request may hold, >= 1 */
+    float clip_k;              /* key clip factor, 0 < c <= 1 (default 0.96) */
+    float clip_v;              /* value clip factor, 0 < c <= 1 (default 0.92) */
+} oscar_cache_desc;
+
+typedef struct oscar_cache oscar_cache; /* opaque host handle */
+
+/* Fill *d with the defaults (head_dim 128, page 64, group 64, sink 64, window 256,
+ * clip 0.96 / 0.92); the caller then sets batch, heads and the page counts. */
+void oscar_default_desc(oscar_cache_desc *d);
+
+/* Device buffer sizes (bytes) the caller must allocate for a cache described by *d;
+ * 0 if *d is invalid.
+ *   pool:       max_pages_total * num_kv_heads * OSCAR_PAGE_HEAD_BYTES; physical page p,
+ *               KV head h starts at byte (p * num_kv_heads + h) * OSCAR_PAGE_HEAD_BYTES.
+ *   bf16:       batch * num_kv_heads * 2 * (sink + window) * 128 bf16 values, laid out
+ *               [b][h][K|V][slot][128]; slot = pos for pos < sink, else
+ *               sink + (pos - sink) % window.
+ *   page_table: batch * max_pages_per_seq int32 ([b][logical page] -> physical page).
+ *   seq_lens:   batch int32 (tokens held per request). */
+size_t oscar_pool_bytes(const oscar_cache_desc *d);
+size_t oscar_bf16_bytes(const oscar_cache_desc *d);
+size_t oscar_page_table_bytes(const oscar_cache_desc *d);
+size_t oscar_seq_lens_bytes(const oscar_cache_desc *d);
+
+/* Create a host handle over caller-owned device buffers (all 16-byte aligned, sizes as
+ * above).  The handle keeps the pointers but never frees them.  All requests start
+ * empty and the free list hands out physical pages 0, 1, 2, ... until
+ * kv_page_table_init() sets another order.  Nothing is enqueued; the first sync
+ * clears the device page table and lengths.
+ * Errors: OSCAR_EINVAL (bad descriptor or NULL), OSCAR_EALIGN. */
+int oscar_cache_create(const oscar_cache_desc *d, void *pool, void *bf16, int32_t *page_table,
+                       int32_t *seq_lens, oscar_cache **out);
+int oscar_cache_destroy(oscar_cache *c);
+/* Tokens currently held by request b (host mirror), or a negative error. */
+int64_t oscar_cache_length(const oscar_cache *c, int32_t b);
+
+/* ---------------------------------------------------------------- kv_page_table
+ * The page table maps each request's INT2 history (positions sink .. len - window - 1,
+ * 64 per page) onto physical pages of the pool, so a request's pages need not be
+ * contiguous (the pages say OSCAR plugs into paged attention without a custom layout:
+ * axbrief.com OSCAR page, section "OSCAR release"; techllm.github.io page, section
+ * "OSCAR").  The free list and a mirror of the table live on the host: init, reserve
+ * and release touch host memory only and mark rows dirty; kv_page_table_sync (also
+ * called by kv_quant_append and oscar_decode_attention) copies the dirty entries and
+ * lengths to the device buffers with cudaMemcpyAsync on its stream. */
+
+/* Reset every request to length 0 and set the order in which free physical pages are
+ * handed out: page_order (host, max_pages_total distinct ids in [0, max_pages_total))
+ * or NULL for 0, 1, 2, ...  The next sync clears the device table and lengths.
+ * Errors: OSCAR_EINVAL (not a permutation; nothing changes). */
+int kv_page_table_init(oscar_cache *c, const int32_t *page_order);
+/* Make sure request b owns the pages its INT2 history needs once it holds `new_len`
+ * tokens, taking them from the free list.  Errors: OSCAR_ENOPAGES (the pool or the
+ * row is full; nothing is taken), OSCAR_ERANGE. */
+int kv_page_table_reserve(oscar_cache *c, int32_t b, int64_t new_len);
+/* Return request b's pages to the free list and set its length to 0. */
+int kv_page_table_release(oscar_cache *c, int32_t b);
+/* Copy dirty page-table entries and lengths to the device (async on `stream`). */
+int kv_page_table_sync(oscar_cache *c, void *stream);
+/* Host mirror of request b's row: writes up to max_out physical ids to `pages` (host)
+ * and returns how many pages b holds (or a negative error). */
+int kv_page_table_read(const oscar_cache *c, int32_t b, int32_t *pages, int32_t max_out);
+/* Physical pages left on the free list. */
+int32_t kv_page_table_free_pages(const oscar_cache *c);
+
+/* ---------------------------------------------------------------- write path
+ * kv_quant_append: append new_tokens[b] tokens (host array, batch entries, >= 0) to
+ * every request b.  k and v (device, bf16, [sum_b new_tokens[b], num_kv_heads, 128],
+ * requests in order b = 0, 1, ..., tokens in position order) are the new keys (NOT
+ * rotated) and values.  rk (device, fp32, [num_kv_heads][128][128], row-major, row j =
+ * input channel) is R_K of each KV head.
+ * Position p of request b goes to the sink when p < sink, else to the window ring; a
+ * position that falls out of the window (p < len - window) is rotated (keys only:
+ * k~ = k . R_K, fp32, serial fused multiply-add over input channels 0..127), clipped
+ * (lo = c * group min, hi = c * group max), quantised (s = fp16((hi - lo) / 3),
+ * m = fp16(lo), code = clamp(rint((clamp(x, lo, hi) - m) / s), 0, 3), 0 when s = 0)
+ * and stored in its INT2 page.  Tokens leaving the window are quantised from their
+ * BF16 window copy, so appending L tokens at once or one by one stores the same bytes.
+ * Pages are reserved as needed (OSCAR_ENOPAGES leaves the cache unchanged).
+ * Source: axbrief.com OSCAR page, section "attention-statistics rotation + Triton
+ * kernels" (rotation, c_K, c_V, G_K = 64, per-token asymmetric INT2, V unrotated). */
+int kv_quant_append(oscar_cache *c, const void *k, const void *v, const int32_t *new_tokens,
+                    const float *rk, void *stream);
+
+/* ---------------------------------------------------------------- read path
+ * oscar_decode_attention: one decode query per request and query head against every
+ * token the request holds.  q (device, [batch, num_q_heads, 128], OSCAR_DTYPE_F32 or
+ * OSCAR_DTYPE_BF16) is unrotated; rk as for kv_quant_append.  out (device,
+ * [batch, num_q_heads, 128], out_dtype) receives softmax(q K^T / sqrt(128)) V over the
+ * BF16 sink + window tokens (plain q) and the INT2 tokens (q . R_K against the
+ * dequantised rotated keys, which equals inverse-rotating every key because R_K is
+ * orthogonal).  The INT2 pages are unpacked and dequantised on chip; no dequantised
+ * copy reaches global memory.  Requests with length 0 get zeros.
+ * workspace (device, >= oscar_decode_workspace_bytes(c) bytes, 16-byte aligned) holds
+ * the rotated queries and the split-K partial results; it needs no initialisation.
+ * Source: axbrief.com OSCAR page, section "attention-statistics rotation + Triton
+ * kernels" (fused read path). */
+size_t oscar_decode_workspace_bytes(const oscar_cache *c);
+int oscar_decode_attention(oscar_cache *c, const void *q, int32_t q_dtype, const float *rk,
+                           void *out, int32_t out_dtype, void *workspace, size_t workspace_bytes,
+                           void *stream);
+
+/* ---------------------------------------------------------------- calibration
+ * oscar_build_rk: R_K = U_Q * H_Had * P_br for num_kv_heads heads from n query samples
+ * per head.  q (device, fp32, [num_kv_heads][n][128]) are unrotated query samples;
+ * rk (device, fp32, [num_kv_heads][128][128]) receives R_K (row vectors: k~ = k . R_K).
+ * C_Q = (1/n) sum q^T q is accumulated in fp64, U_Q (eigenvalues descending, each
+ * eigenvector signed so its largest-magnitude entry is positive) comes from a parallel
+ * cyclic Jacobi eigen-solver in fp64, H_Had[i][j] = (-1)^popcount(i & j) / sqrt(128),
+ * P_br[i][j] = [j == bitrev7(i)].  workspace >= oscar_build_rk_workspace_bytes(heads).
+ * Source: axbrief.com OSCAR page, section "attention-statistics rotation + Triton
+ * kernels"; techllm.github.io page, section "OSCAR" (Hadamard + bit reversal). */
+size_t oscar_build_rk_workspace_bytes(int32_t num_kv_heads);
+int oscar_build_rk(const float *q, int64_t n, int32_t num_kv_heads, float *rk, void *workspace,
+                   size_t workspace_bytes, void *stream);
+
+/* ---------------------------------------------------------------- readback (synchronous)
+ * Copy n INT2 tokens of request b, KV head h, starting at position pos0 (each position
+ * must lie in the INT2 history) into host buffers, in the per-token logical format:
+ * codes [n][32] bytes (channel 4i+j in bits 2j..2j+1 of byte i) and scale/min
+ * [n][4] fp16 bit patterns (s0, m0, s1, m1), for K and V.  Any host pointer may be
+ * NULL.  Synchronises `stream`. */
+int oscar_read_int2(const oscar_cache *c, int32_t b, int32_t h, int64_t pos0, int64_t n,
+                    uint8_t *k_codes, uint16_t *k_sm, uint8_t *v_codes, uint16_t *v_sm,
+                    void *stream);
+/* Copy n BF16 tokens (sink or window positions, each must be held in BF16) of request b,
+ * KV head h from pos0 into host buffers k, v ([n][128] bf16 bit patterns; NULL allowed). */
+int oscar_read_bf16(const oscar_cache *c, int32_t b, int32_t h, int64_t pos0, int64_t n,
+                    uint16_t *k, uint16_t *v, void *stream);
+
+/* ---------------------------------------------------------------- diagnostics */
+const char *oscar_strerror(int code);
+int oscar_last_cuda_error(void);
+/* Kernel launches issued by this process so far (all entry points). */
+int64_t oscar_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* OSCAR_KV_H */

@@ -1,0 +1,468 @@
+// api.cpp -- host side of the C ABI: argument checks, the cache handle, the host free
+// list of the page table, and the launches.  No device memory is allocated here.
+#include <algorithm>
+#include <atomic>
+#include <cstring>
+#include <vector>
+
+#include "../../include/oscar_kv.h"
+#include "internal.h"
+
+using namespace oscar;
+
+struct oscar_cache {
+    oscar_cache_desc d;
+    uint8_t* pool;
+    uint16_t* bf16;
+    int32_t* pt;
+    int32_t* lens_dev;
+    std::vector<int64_t> len;                 // tokens held per request
+    std::vector<std::vector<int32_t>> rows;   // physical pages held per request
+    std::vector<int32_t> free_list;           // popped from the back
+    std::vector<int32_t> dirty_lo;            // first row entry not yet on the device
+    bool clear_device;                        // the device table / lengths need zeroing
+    bool lens_dirty;
+    int32_t g;
+};
+
+namespace {
+
+std::atomic<int> g_last_cuda{0};
+std::atomic<int64_t> g_launches{0};
+
+int cuda_fail(cudaError_t e) {
+    g_last_cuda = (int)e;
+    return OSCAR_ECUDA;
+}
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+bool desc_ok(const oscar_cache_desc* d) {
+    if (!d) return false;
+    if (d->batch < 1 || d->batch > kMaxBatch) return false;
+    if (d->num_kv_heads < 1 || d->num_q_heads < 1) return false;
+    if (d->num_q_heads % d->num_kv_heads) return false;
+    const int g = d->num_q_heads / d->num_kv_heads;
+    if (g > kMaxG || (g > 8 && g != 12 && g != 16)) return false;
+    if (d->head_dim != kD || d->page_size != kPage || d->group_size != kGroup) return false;
+    if (d->sink != kSink || d->window != kWindow) return false;
+    if (d->max_pages_total < 1 || d->max_pages_per_seq < 1) return false;
+    if (!(d->clip_k > 0.f && d->clip_k <= 1.f && d->clip_v > 0.f && d->clip_v <= 1.f)) return false;
+    return true;
+}
+
+cudaStream_t S(void* s) { return (cudaStream_t)s; }
+
+// Pages the INT2 history of a request needs once it holds `len` tokens.
+int64_t pages_for(int64_t len) {
+    int64_t t = len > kSlots ? len - kSlots : 0;
+    return (t + kPage - 1) / kPage;
+}
+
+int take_pages(oscar_cache* c, int32_t b, int64_t new_len) {
+    int64_t need = pages_for(new_len);
+    int64_t have = (int64_t)c->rows[b].size();
+    if (need <= have) return OSCAR_OK;
+    if (need > c->d.max_pages_per_seq) return OSCAR_ENOPAGES;
+    if (need - have > (int64_t)c->free_list.size()) return OSCAR_ENOPAGES;
+    for (int64_t i = have; i < need; ++i) {
+        c->rows[b].push_back(c->free_list.back());
+        c->free_list.pop_back();
+    }
+    c->dirty_lo[b] = std::min<int32_t>(c->dirty_lo[b], (int32_t)have);
+    return OSCAR_OK;
+}
+
+int sync(oscar_cache* c, cudaStream_t s) {
+    cudaError_t e = cudaSuccess;
+    if (c->clear_device) {
+        e = cudaMemsetAsync(c->pt, 0, oscar_page_table_bytes(&c->d), s);
+        if (e == cudaSuccess) e = cudaMemsetAsync(c->lens_dev, 0, oscar_seq_lens_bytes(&c->d), s);
+        if (e != cudaSuccess) return cuda_fail(e);
+        c->clear_device = false;
+        c->lens_dirty = true;
+    }
+    for (int32_t b = 0; b < c->d.batch; ++b) {
+        const int32_t lo = c->dirty_lo[b];
+        const int32_t hi = (int32_t)c->rows[b].size();
+        if (lo < hi) {
+            e = cudaMemcpyAsync(c->pt + (size_t)b * c->d.max_pages_per_seq + lo, c->rows[b].data() + lo,
+                                sizeof(int32_t) * (hi - lo), cudaMemcpyHostToDevice, s);
+            if (e != cudaSuccess) return cuda_fail(e);
+        }
+        c->dirty_lo[b] = INT32_MAX;
+    }
+    if (c->lens_dirty) {
+        std::vector<int32_t> l(c->len.begin(), c->len.end());
+        e = cudaMemcpyAsync(c->lens_dev, l.data(), sizeof(int32_t) * l.size(), cudaMemcpyHostToDevice, s);
+        if (e != cudaSuccess) return cuda_fail(e);
+        c->lens_dirty = false;
+    }
+    return OSCAR_OK;
+}
+
+}  // namespace
+
+namespace oscar {
+void count_launches(int n) { g_launches += n; }
+}  // namespace oscar
+
+extern "C" {
+
+void oscar_default_desc(oscar_cache_desc* d) {
+    if (!d) return;
+    std::memset(d, 0, sizeof(*d));
+    d->batch = 1;
+    d->num_kv_heads = 1;
+    d->num_q_heads = 1;
+    d->head_dim = kD;
+    d->page_size = kPage;
+    d->group_size = kGroup;
+    d->sink = kSink;
+    d->window = kWindow;
+    d->max_pages_total = 1;
+    d->max_pages_per_seq = 1;
+    d->clip_k = 0.96f;
+    d->clip_v = 0.92f;
+}
+
+size_t oscar_pool_bytes(const oscar_cache_desc* d) {
+    if (!desc_ok(d)) return 0;
+    return (size_t)d->max_pages_total * d->num_kv_heads * kPageHeadBytes;
+}
+size_t oscar_bf16_bytes(const oscar_cache_desc* d) {
+    if (!desc_ok(d)) return 0;
+    return (size_t)d->batch * d->num_kv_heads * 2 * kSlots * kD * sizeof(uint16_t);
+}
+size_t oscar_page_table_bytes(const oscar_cache_desc* d) {
+    if (!desc_ok(d)) return 0;
+    return (size_t)d->batch * d->max_pages_per_seq * sizeof(int32_t);
+}
+size_t oscar_seq_lens_bytes(const oscar_cache_desc* d) {
+    if (!desc_ok(d)) return 0;
+    return (size_t)d->batch * sizeof(int32_t);
+}
+
+int oscar_cache_create(const oscar_cache_desc* d, void* pool, void* bf16, int32_t* page_table,
+                       int32_t* seq_lens, oscar_cache** out) {
+    if (!out) return OSCAR_EINVAL;
+    *out = nullptr;
+    if (!desc_ok(d) || !pool || !bf16 || !page_table || !seq_lens) return OSCAR_EINVAL;
+    if (!aligned16(pool) || !aligned16(bf16) || !aligned16(page_table) || !aligned16(seq_lens))
+        return OSCAR_EALIGN;
+    oscar_cache* c = new oscar_cache();
+    c->d = *d;
+    c->pool = (uint8_t*)pool;
+    c->bf16 = (uint16_t*)bf16;
+    c->pt = page_table;
+    c->lens_dev = seq_lens;
+    c->len.assign(d->batch, 0);
+    c->rows.assign(d->batch, {});
+    c->g = d->num_q_heads / d->num_kv_heads;
+    c->free_list.resize(d->max_pages_total);
+    for (int32_t i = 0; i < d->max_pages_total; ++i) c->free_list[i] = d->max_pages_total - 1 - i;
+    c->dirty_lo.assign(d->batch, INT32_MAX);
+    c->clear_device = true;
+    c->lens_dirty = true;
+    *out = c;
+    return OSCAR_OK;
+}
+
+int oscar_cache_destroy(oscar_cache* c) {
+    delete c;
+    return OSCAR_OK;
+}
+
+int64_t oscar_cache_length(const oscar_cache* c, int32_t b) {
+    if (!c) return OSCAR_EINVAL;
+    if (b < 0 || b >= c->d.batch) return OSCAR_ERANGE;
+    return c->len[b];
+}
+
+// ------------------------------------------------------------------ kv_page_table
+
+int kv_page_table_init(oscar_cache* c, const int32_t* page_order) {
+    if (!c) return OSCAR_EINVAL;
+    const int32_t n = c->d.max_pages_total;
+    std::vector<int32_t> order(n);
+    if (page_order) {
+        std::vector<char> seen(n, 0);
+        for (int32_t i = 0; i < n; ++i) {
+            int32_t p = page_order[i];
+            if (p < 0 || p >= n || seen[p]) return OSCAR_EINVAL;
+            seen[p] = 1;
+            order[i] = p;
+        }
+    } else {
+        for (int32_t i = 0; i < n; ++i) order[i] = i;
+    }
+    c->free_list.assign(order.rbegin(), order.rend());
+    for (auto& r : c->rows) r.clear();
+    std::fill(c->len.begin(), c->len.end(), 0);
+    std::fill(c->dirty_lo.begin(), c->dirty_lo.end(), INT32_MAX);
+    c->clear_device = true;
+    return OSCAR_OK;
+}
+
+int kv_page_table_reserve(oscar_cache* c, int32_t b, int64_t new_len) {
+    if (!c) return OSCAR_EINVAL;
+    if (b < 0 || b >= c->d.batch || new_len < 0) return OSCAR_ERANGE;
+    return take_pages(c, b, new_len);
+}
+
+int kv_page_table_release(oscar_cache* c, int32_t b) {
+    if (!c) return OSCAR_EINVAL;
+    if (b < 0 || b >= c->d.batch) return OSCAR_ERANGE;
+    auto& r = c->rows[b];
+    for (auto it = r.rbegin(); it != r.rend(); ++it) c->free_list.push_back(*it);
+    r.clear();
+    c->dirty_lo[b] = INT32_MAX;
+    c->len[b] = 0;
+    c->lens_dirty = true;
+    return OSCAR_OK;
+}
+
+int kv_page_table_sync(oscar_cache* c, void* stream) {
+    if (!c) return OSCAR_EINVAL;
+    return sync(c, S(stream));
+}
+
+int kv_page_table_read(const oscar_cache* c, int32_t b, int32_t* pages, int32_t max_out) {
+    if (!c) return OSCAR_EINVAL;
+    if (b < 0 || b >= c->d.batch) return OSCAR_ERANGE;
+    const auto& r = c->rows[b];
+    if (pages)
+        for (int32_t i = 0; i < max_out && i < (int32_t)r.size(); ++i) pages[i] = r[i];
+    return (int)r.size();
+}
+
+int32_t kv_page_table_free_pages(const oscar_cache* c) {
+    return c ? (int32_t)c->free_list.size() : OSCAR_EINVAL;
+}
+
+// ------------------------------------------------------------------ write path
+
+int kv_quant_append(oscar_cache* c, const void* k, const void* v, const int32_t* new_tokens,
+                    const float* rk, void* stream) {
+    if (!c || !new_tokens) return OSCAR_EINVAL;
+    const oscar_cache_desc& d = c->d;
+    int64_t rows = 0;
+    int64_t need_pages = 0;
+    for (int32_t b = 0; b < d.batch; ++b) {
+        if (new_tokens[b] < 0) return OSCAR_EINVAL;
+        int64_t l1 = c->len[b] + new_tokens[b];
+        if (l1 > INT32_MAX / 2) return OSCAR_ERANGE;
+        int64_t p = pages_for(l1);
+        if (p > d.max_pages_per_seq) return OSCAR_ENOPAGES;
+        need_pages += std::max<int64_t>(0, p - (int64_t)c->rows[b].size());
+        rows += new_tokens[b];
+    }
+    if (rows == 0) return OSCAR_OK;
+    if (!k || !v || !rk) return OSCAR_EINVAL;
+    if (!aligned16(k) || !aligned16(v) || !aligned16(rk)) return OSCAR_EALIGN;
+    if (need_pages > (int64_t)c->free_list.size()) return OSCAR_ENOPAGES;
+
+    cudaStream_t s = S(stream);
+    for (int32_t b = 0; b < d.batch; ++b) {
+        int rc = take_pages(c, b, c->len[b] + new_tokens[b]);
+        if (rc != OSCAR_OK) return rc;   // cannot happen after the capacity check above
+    }
+    int rc = sync(c, s);
+    if (rc != OSCAR_OK) return rc;
+    AppendParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.batch = d.batch;
+    p.hkv = d.num_kv_heads;
+    p.clip_k = d.clip_k;
+    p.clip_v = d.clip_v;
+    p.k = (const uint16_t*)k;
+    p.v = (const uint16_t*)v;
+    p.rk = rk;
+    p.pool = c->pool;
+    p.bf16 = c->bf16;
+    p.page_table = c->pt;
+    p.seq_lens = c->lens_dev;
+    p.max_pps = d.max_pages_per_seq;
+    int64_t off = 0;
+    int32_t jobs = 0;
+    for (int32_t b = 0; b < d.batch; ++b) {
+        AppendReq& r = p.req[b];
+        r.len0 = (int32_t)c->len[b];
+        r.n_new = new_tokens[b];
+        r.tok_off = off;
+        int32_t l1 = r.len0 + r.n_new;
+        r.e0 = std::max<int32_t>(kSink, r.len0 - kWindow);
+        r.e1 = std::max<int32_t>(kSink, l1 - kWindow);
+        r.job0 = jobs;
+        r.page0 = (r.e0 - kSink) / kPage;
+        if (r.e1 > r.e0) jobs += (r.e1 - 1 - kSink) / kPage - r.page0 + 1;
+        off += new_tokens[b];
+    }
+    p.n_jobs = jobs;
+    cudaError_t e = launch_append(p, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    for (int32_t b = 0; b < d.batch; ++b) c->len[b] += new_tokens[b];
+    return OSCAR_OK;
+}
+
+// ------------------------------------------------------------------ read path
+
+static const int kMaxSplits = 128;   // INT2 splits + 1 BF16 split per (request, KV head)
+
+static int pick_pps(const oscar_cache* c) {
+    int64_t total = 0;
+    int64_t longest = 0;
+    for (int32_t b = 0; b < c->d.batch; ++b) {
+        total += pages_for(c->len[b]);
+        longest = std::max<int64_t>(longest, pages_for(c->len[b]));
+    }
+    total *= c->d.num_kv_heads;
+    // about 8 split CTAs per SM of a 152-SM part, at least 4 pages (256 tokens) each
+    int64_t pps = std::max<int64_t>(4, (total + 152 * 8 - 1) / (152 * 8));
+    pps = std::max<int64_t>(pps, (longest + kMaxSplits - 2) / (kMaxSplits - 1));
+    return (int)pps;
+}
+
+size_t oscar_decode_workspace_bytes(const oscar_cache* c) {
+    if (!c) return 0;
+    size_t qrot = (size_t)c->d.batch * c->d.num_q_heads * kD * sizeof(float);
+    size_t part = (size_t)c->d.batch * c->d.num_kv_heads * kMaxSplits * c->g * (2 + kD) * sizeof(float);
+    return qrot + part;
+}
+
+int oscar_decode_attention(oscar_cache* c, const void* q, int32_t q_dtype, const float* rk,
+                           void* out, int32_t out_dtype, void* workspace, size_t workspace_bytes,
+                           void* stream) {
+    if (!c || !q || !rk || !out) return OSCAR_EINVAL;
+    if ((q_dtype != OSCAR_DTYPE_F32 && q_dtype != OSCAR_DTYPE_BF16) ||
+        (out_dtype != OSCAR_DTYPE_F32 && out_dtype != OSCAR_DTYPE_BF16))
+        return OSCAR_EINVAL;
+    if (!workspace || workspace_bytes < oscar_decode_workspace_bytes(c)) return OSCAR_EWORKSPACE;
+    if (!aligned16(q) || !aligned16(rk) || !aligned16(out) || !aligned16(workspace)) return OSCAR_EALIGN;
+    int rc = sync(c, S(stream));
+    if (rc != OSCAR_OK) return rc;
+    DecodeParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.batch = c->d.batch;
+    p.hkv = c->d.num_kv_heads;
+    p.g = c->g;
+    p.pps = pick_pps(c);
+    p.max_splits = kMaxSplits;
+    p.q = q;
+    p.q_dtype = q_dtype;
+    p.rk = rk;
+    p.out = out;
+    p.out_dtype = out_dtype;
+    p.pool = c->pool;
+    p.bf16 = c->bf16;
+    p.page_table = c->pt;
+    p.max_pps = c->d.max_pages_per_seq;
+    p.qrot = (float*)workspace;
+    p.partial = p.qrot + (size_t)c->d.batch * c->d.num_q_heads * kD;
+    for (int32_t b = 0; b < c->d.batch; ++b) p.len[b] = (int32_t)c->len[b];
+    cudaError_t e = launch_decode(p, S(stream));
+    return e == cudaSuccess ? OSCAR_OK : cuda_fail(e);
+}
+
+// ------------------------------------------------------------------ calibration
+
+size_t oscar_build_rk_workspace_bytes(int32_t num_kv_heads) {
+    return num_kv_heads > 0 ? build_rk_ws_bytes(num_kv_heads) : 0;
+}
+
+int oscar_build_rk(const float* q, int64_t n, int32_t num_kv_heads, float* rk, void* workspace,
+                   size_t workspace_bytes, void* stream) {
+    if (!q || !rk || n < 1 || num_kv_heads < 1) return OSCAR_EINVAL;
+    if (!workspace || workspace_bytes < build_rk_ws_bytes(num_kv_heads)) return OSCAR_EWORKSPACE;
+    if (!aligned16(q) || !aligned16(rk) || !aligned16(workspace)) return OSCAR_EALIGN;
+    cudaError_t e = launch_build_rk(q, n, num_kv_heads, rk, workspace, S(stream));
+    return e == cudaSuccess ? OSCAR_OK : cuda_fail(e);
+}
+
+// ------------------------------------------------------------------ readback
+
+int oscar_read_int2(const oscar_cache* c, int32_t b, int32_t h, int64_t pos0, int64_t n,
+                    uint8_t* k_codes, uint16_t* k_sm, uint8_t* v_codes, uint16_t* v_sm,
+                    void* stream) {
+    if (!c) return OSCAR_EINVAL;
+    if (b < 0 || b >= c->d.batch || h < 0 || h >= c->d.num_kv_heads || n < 0) return OSCAR_ERANGE;
+    int64_t l = c->len[b];
+    if (n == 0) return OSCAR_OK;
+    if (pos0 < kSink || pos0 + n > l - kWindow) return OSCAR_ERANGE;
+    std::vector<uint8_t> blk(kPageHeadBytes);
+    int64_t cur_page = -1;
+    for (int64_t i = 0; i < n; ++i) {
+        int64_t pos = pos0 + i;
+        int64_t pg = (pos - kSink) / kPage;
+        int t = (int)((pos - kSink) % kPage);
+        if (pg != cur_page) {
+            int32_t phys = c->rows[b][pg];
+            const uint8_t* src = c->pool + ((size_t)phys * c->d.num_kv_heads + h) * kPageHeadBytes;
+            cudaError_t e = cudaMemcpyAsync(blk.data(), src, kPageHeadBytes, cudaMemcpyDeviceToHost,
+                                            S(stream));
+            if (e == cudaSuccess) e = cudaStreamSynchronize(S(stream));
+            if (e != cudaSuccess) return cuda_fail(e);
+            cur_page = pg;
+        }
+        if (k_codes) std::memcpy(k_codes + i * 32, blk.data() + kKCodes + t * 32, 32);
+        if (k_sm) std::memcpy(k_sm + i * 4, blk.data() + kKSm + t * 8, 8);
+        if (v_sm) std::memcpy(v_sm + i * 4, blk.data() + kVSm + t * 8, 8);
+        if (v_codes) {
+            uint8_t* dst = v_codes + i * 32;
+            std::memset(dst, 0, 32);
+            for (int ch = 0; ch < kD; ++ch) {
+                int code = (blk[kVCodes + ch * 16 + t / 4] >> (2 * (t % 4))) & 3;
+                dst[ch / 4] |= (uint8_t)(code << (2 * (ch % 4)));
+            }
+        }
+    }
+    return OSCAR_OK;
+}
+
+int oscar_read_bf16(const oscar_cache* c, int32_t b, int32_t h, int64_t pos0, int64_t n,
+                    uint16_t* k, uint16_t* v, void* stream) {
+    if (!c) return OSCAR_EINVAL;
+    if (b < 0 || b >= c->d.batch || h < 0 || h >= c->d.num_kv_heads || n < 0 || pos0 < 0)
+        return OSCAR_ERANGE;
+    int64_t l = c->len[b];
+    for (int64_t pos = pos0; pos < pos0 + n; ++pos) {
+        bool sink = pos < std::min<int64_t>(l, kSink);
+        bool win = pos >= std::max<int64_t>(kSink, l - kWindow) && pos < l;
+        if (!sink && !win) return OSCAR_ERANGE;
+    }
+    size_t base = ((size_t)b * c->d.num_kv_heads + h) * 2 * kSlots * kD;
+    for (int64_t i = 0; i < n; ++i) {
+        int slot = bf16_slot(pos0 + i);
+        for (int kv = 0; kv < 2; ++kv) {
+            uint16_t* dst = kv == 0 ? k : v;
+            if (!dst) continue;
+            const uint16_t* src = c->bf16 + base + ((size_t)kv * kSlots + slot) * kD;
+            cudaError_t e = cudaMemcpyAsync(dst + i * kD, src, kD * sizeof(uint16_t),
+                                            cudaMemcpyDeviceToHost, S(stream));
+            if (e != cudaSuccess) return cuda_fail(e);
+        }
+    }
+    cudaError_t e = cudaStreamSynchronize(S(stream));
+    return e == cudaSuccess ? OSCAR_OK : cuda_fail(e);
+}
+
+// ------------------------------------------------------------------ diagnostics
+
+const char* oscar_strerror(int code) {
+    switch (code) {
+        case OSCAR_OK: return "ok";
+        case OSCAR_EINVAL: return "invalid argument";
+        case OSCAR_ENOPAGES: return "out of INT2 pages";
+        case OSCAR_EWORKSPACE: return "workspace missing or too small";
+        case OSCAR_ECUDA: return "CUDA error";
+        case OSCAR_EALIGN: return "device pointer not 16-byte aligned";
+        case OSCAR_ERANGE: return "index or position out of range";
+        default: return "unknown error";
+    }
+}
+
+int oscar_last_cuda_error(void) { return g_last_cuda; }
+
+int64_t oscar_launch_count(void) { return g_launches; }
+
+}  // extern "C"

@@ -1,0 +1,230 @@
+// append.cu -- write path of the INT2 rotated paged KV cache (sm_103a).
+//
+// kv_quant_append runs two kernels on the caller's stream:
+//   1. quant_pages: one CTA per (touched INT2 page, KV head).  Every position that
+//      leaves the BF16 window in this call (or goes straight to INT2 in a long
+//      append) is rotated (keys only), clipped, quantised to asymmetric INT2 in two
+//      64-channel groups and packed into its page (axbrief.com OSCAR page, section
+//      "attention-statistics rotation + Triton kernels": k . R_K, c_K = 0.96,
+//      c_V = 0.92, G_K = 64, per-token asymmetric INT2; values unrotated because R_V
+//      is folded into W_V / W_O offline).
+//   2. insert_bf16: copies the new tokens that stay in BF16 into the sink / window
+//      slots and publishes the new lengths (axbrief.com OSCAR page, section "OSCAR
+//      release": BF16 sink + recent window).
+// Stream order makes kernel 1 read the window before kernel 2 overwrites it.
+//
+// Bit-exact contract (shared with nothing but the written specification): the key
+// rotation is the serial chain acc = fma(x_j, R[j][c], acc), j = 0..127, acc0 = +0;
+// clip products, the range subtraction and both divisions are single IEEE fp32
+// operations (explicit _rn intrinsics, so the compiler cannot contract them);
+// fp16 conversions round to nearest even; codes use rint (ties to even).
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "internal.h"
+
+namespace oscar {
+namespace {
+
+constexpr int kTok = 8;   // tokens rotated together per thread (independent FMA chains)
+
+__device__ __forceinline__ float bf16_bits_to_f32(uint16_t b) {
+    return __uint_as_float(((uint32_t)b) << 16);
+}
+
+__device__ __forceinline__ int find_request(const AppendParams& p, int job) {
+    int b = 0;
+    for (int i = 1; i < p.batch; ++i)
+        if (p.req[i].e1 > p.req[i].e0 && p.req[i].job0 <= job) b = i;
+    return b;
+}
+
+// Source row (bf16[128]) of position `pos` of request b, KV head h, tensor kv (0 = K, 1 = V).
+__device__ __forceinline__ const uint16_t* token_src(const AppendParams& p, int b, int h, int kv,
+                                                     int pos) {
+    const AppendReq& r = p.req[b];
+    if (pos < r.len0) {   // still in the BF16 window (it leaves it in this call)
+        size_t base = (((size_t)b * p.hkv + h) * 2 + kv) * kSlots + bf16_slot(pos);
+        return p.bf16 + base * kD;
+    }
+    const uint16_t* t = kv == 0 ? p.k : p.v;
+    return t + ((size_t)(r.tok_off + (pos - r.len0)) * p.hkv + h) * kD;
+}
+
+struct GroupStat {
+    float mn, mx;
+};
+
+// Min and max over the 64 channels of each group (threads 0..63 and 64..127).
+__device__ __forceinline__ GroupStat group_minmax(float y, float* red) {
+    float mn = y, mx = y;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    }
+    const int w = threadIdx.x >> 5;
+    if ((threadIdx.x & 31) == 0) {
+        red[2 * w] = mn;
+        red[2 * w + 1] = mx;
+    }
+    __syncthreads();
+    const int w0 = w & ~1;
+    GroupStat g;
+    g.mn = fminf(red[2 * w0], red[2 * w0 + 2]);
+    g.mx = fmaxf(red[2 * w0 + 1], red[2 * w0 + 3]);
+    __syncthreads();
+    return g;
+}
+
+struct Quant {
+    int code;
+    uint16_t s16, m16;
+};
+
+__device__ __forceinline__ Quant quantise(float y, GroupStat g, float clip) {
+    const float lo = __fmul_rn(clip, g.mn);
+    const float hi = __fmul_rn(clip, g.mx);
+    const float s_exact = __fdiv_rn(__fsub_rn(hi, lo), 3.0f);
+    Quant q;
+    q.s16 = __half_as_ushort(__float2half_rn(s_exact));
+    q.m16 = __half_as_ushort(__float2half_rn(lo));
+    const float s = __half2float(__ushort_as_half(q.s16));
+    const float m = __half2float(__ushort_as_half(q.m16));
+    const float xc = fminf(fmaxf(y, lo), hi);
+    int code = 0;
+    if (s != 0.0f) {
+        const float t = rintf(__fdiv_rn(__fsub_rn(xc, m), s));
+        code = t < 0.0f ? 0 : (t > 3.0f ? 3 : (int)t);
+    }
+    q.code = code;
+    return q;
+}
+
+__global__ void __launch_bounds__(128) quant_pages(const __grid_constant__ AppendParams p) {
+    extern __shared__ __align__(16) float smem[];
+    float* R = smem;                   // [128][128]
+    float* xs = R + kD * kD;           // [kTok][128]
+    float* red = xs + kTok * kD;       // [8]
+
+    const int job = blockIdx.x;
+    const int h = blockIdx.y;
+    const int c = threadIdx.x;
+    const int lane = c & 31;
+    const int b = find_request(p, job);
+    const AppendReq& r = p.req[b];
+    const int pg = r.page0 + (job - r.job0);
+    const int pbeg = max(r.e0, kSink + pg * kPage);
+    const int pend = min(r.e1, kSink + (pg + 1) * kPage);
+    const int phys = p.page_table[(size_t)b * p.max_pps + pg];
+    uint8_t* blk = p.pool + ((size_t)phys * p.hkv + h) * kPageHeadBytes;
+
+    {   // stage R_K of this head
+        const float4* src = reinterpret_cast<const float4*>(p.rk + (size_t)h * kD * kD);
+        float4* dst = reinterpret_cast<float4*>(R);
+        for (int i = c; i < kD * kD / 4; i += 128) dst[i] = src[i];
+    }
+    // this channel's row of V codes (16 bytes = 64 tokens), updated in registers
+    uint32_t vw[4];
+    {
+        const uint4 cur = *reinterpret_cast<const uint4*>(blk + kVCodes + c * 16);
+        vw[0] = cur.x; vw[1] = cur.y; vw[2] = cur.z; vw[3] = cur.w;
+    }
+
+    for (int p0 = pbeg; p0 < pend; p0 += kTok) {
+        const int n = min(kTok, pend - p0);
+        __syncthreads();
+        for (int t = 0; t < n; ++t) xs[t * kD + c] = bf16_bits_to_f32(token_src(p, b, h, 0, p0 + t)[c]);
+        __syncthreads();
+        // keys: k~_c = sum_j x_j R[j][c], serial fused multiply-add in ascending j
+        float acc[kTok];
+#pragma unroll
+        for (int t = 0; t < kTok; ++t) acc[t] = 0.0f;
+#pragma unroll 4
+        for (int j = 0; j < kD; ++j) {
+            const float rj = R[j * kD + c];
+#pragma unroll
+            for (int t = 0; t < kTok; ++t) acc[t] = __fmaf_rn(xs[t * kD + j], rj, acc[t]);
+        }
+        for (int t = 0; t < n; ++t) {
+            const int slot = (p0 + t - kSink) % kPage;
+            // ---- K: token-major codes
+            {
+                const float y = acc[t];
+                const GroupStat g = group_minmax(y, red);
+                const Quant q = quantise(y, g, p.clip_k);
+                uint32_t word = (uint32_t)q.code << (2 * (lane & 15));
+#pragma unroll
+                for (int o = 1; o < 16; o <<= 1) word |= __shfl_xor_sync(0xffffffffu, word, o);
+                if ((lane & 15) == 0)
+                    *reinterpret_cast<uint32_t*>(blk + kKCodes + slot * 32 + (c >> 4) * 4) = word;
+                if ((c & 63) == 0)
+                    *reinterpret_cast<uint32_t*>(blk + kKSm + slot * 8 + (c >> 6) * 4) =
+                        (uint32_t)q.s16 | ((uint32_t)q.m16 << 16);
+            }
+            // ---- V: unrotated, channel-major codes
+            {
+                const float y = bf16_bits_to_f32(token_src(p, b, h, 1, p0 + t)[c]);
+                const GroupStat g = group_minmax(y, red);
+                const Quant q = quantise(y, g, p.clip_v);
+                const int wi = slot >> 4;
+                const int sh = 2 * (slot & 15);
+                const uint32_t m = ~(3u << sh);
+                const uint32_t v = (uint32_t)q.code << sh;
+                if (wi == 0) vw[0] = (vw[0] & m) | v;
+                else if (wi == 1) vw[1] = (vw[1] & m) | v;
+                else if (wi == 2) vw[2] = (vw[2] & m) | v;
+                else vw[3] = (vw[3] & m) | v;
+                if ((c & 63) == 0)
+                    *reinterpret_cast<uint32_t*>(blk + kVSm + slot * 8 + (c >> 6) * 4) =
+                        (uint32_t)q.s16 | ((uint32_t)q.m16 << 16);
+            }
+        }
+    }
+    *reinterpret_cast<uint4*>(blk + kVCodes + c * 16) = make_uint4(vw[0], vw[1], vw[2], vw[3]);
+}
+
+// New tokens that stay in BF16 (sink, or the final window) -> their slots.
+__global__ void __launch_bounds__(128) insert_bf16(const __grid_constant__ AppendParams p) {
+    const int b = blockIdx.x;
+    const int h = blockIdx.y;
+    const AppendReq& r = p.req[b];
+    const int l1 = r.len0 + r.n_new;
+    const int wstart = max(kSink, l1 - kWindow);
+    for (int kv = 0; kv < 2; ++kv) {
+        const uint16_t* src_t = kv == 0 ? p.k : p.v;
+        uint16_t* dst_base = p.bf16 + ((((size_t)b * p.hkv + h) * 2 + kv) * kSlots) * kD;
+        // sink positions [len0, min(l1, sink)), then the final window [max(len0, wstart), l1)
+        const int ranges[2][2] = {{r.len0, min(l1, kSink)}, {max(r.len0, wstart), l1}};
+        for (int rg = 0; rg < 2; ++rg)
+            for (int pos = ranges[rg][0]; pos < ranges[rg][1]; ++pos) {
+                const uint16_t* src = src_t + ((size_t)(r.tok_off + (pos - r.len0)) * p.hkv + h) * kD;
+                dst_base[(size_t)bf16_slot(pos) * kD + threadIdx.x] = src[threadIdx.x];
+            }
+    }
+    if (h == 0 && threadIdx.x == 0) p.seq_lens[b] = l1;
+}
+
+}  // namespace
+
+cudaError_t launch_append(const AppendParams& p, cudaStream_t s) {
+    const size_t smem = (size_t)(kD * kD + kTok * kD + 8) * sizeof(float);
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(quant_pages, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)smem);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    int n = 0;
+    if (p.n_jobs > 0) {
+        quant_pages<<<dim3(p.n_jobs, p.hkv), 128, smem, s>>>(p);
+        ++n;
+    }
+    insert_bf16<<<dim3(p.batch, p.hkv), 128, 0, s>>>(p);
+    ++n;
+    count_launches(n);
+    return cudaGetLastError();
+}
+
+}  // namespace oscar

@@ -1,0 +1,316 @@
+// decode.cu -- read path of the INT2 rotated paged KV cache (sm_103a): paged GQA decode
+// attention over INT2 pages + BF16 sink / window tokens, split over the context with a
+// log-sum-exp combine.
+//
+// The pages' read path (axbrief.com OSCAR page, section "attention-statistics rotation +
+// Triton kernels") unpacks, dequantises and inverse-rotates the keys inside one fused
+// attention pass.  Here the rotation is applied once to the query (q~ = q . R_K), which
+// equals inverse-rotating every key because R_K is orthogonal; keys and values are
+// dequantised in registers (x^ = m + code * s, folded into the dot products) and never
+// written back.
+//
+// Kernels:
+//   rotate_q      q~ = q . R_K for every (request, query head), fp32.
+//   split_simt    one CTA per (split, KV head, request): online softmax over its INT2
+//                 pages (or, for the last split of a request, over the BF16 tokens) for
+//                 the G query heads of the KV head; writes (max, sum, unnormalised out).
+//   combine       out = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s per (request, head).
+// All softmax arithmetic is in base 2 (logits pre-scaled by log2(e) / sqrt(128)).
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "internal.h"
+
+namespace oscar {
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+__device__ __forceinline__ float bf16f(uint16_t b) { return __uint_as_float(((uint32_t)b) << 16); }
+__device__ __forceinline__ float h2f(uint16_t b) { return __half2float(__ushort_as_half(b)); }
+
+__device__ __forceinline__ float load_q(const DecodeParams& p, size_t idx) {
+    return p.q_dtype == 0 ? reinterpret_cast<const float*>(p.q)[idx]
+                          : bf16f(reinterpret_cast<const uint16_t*>(p.q)[idx]);
+}
+
+// q~[b][hq][c] = sum_j q[b][hq][j] R_{hq / G}[j][c]
+__global__ void __launch_bounds__(128) rotate_q(const __grid_constant__ DecodeParams p) {
+    __shared__ float qs[kMaxG][kD];
+    const int b = blockIdx.y;
+    const int h = blockIdx.x;
+    const int c = threadIdx.x;
+    const size_t qbase = ((size_t)b * p.hkv * p.g + (size_t)h * p.g) * kD;
+    for (int i = 0; i < p.g; ++i) qs[i][c] = load_q(p, qbase + (size_t)i * kD + c);
+    __syncthreads();
+    float acc[kMaxG];
+#pragma unroll
+    for (int i = 0; i < kMaxG; ++i) acc[i] = 0.f;
+    const float* R = p.rk + (size_t)h * kD * kD;
+    for (int j = 0; j < kD; ++j) {
+        const float r = R[j * kD + c];
+#pragma unroll
+        for (int i = 0; i < kMaxG; ++i)
+            if (i < p.g) acc[i] = fmaf(qs[i][j], r, acc[i]);
+    }
+    for (int i = 0; i < p.g; ++i) p.qrot[qbase + (size_t)i * kD + c] = acc[i];
+}
+
+template <int G>
+struct WarpState {
+    float m[G], l[G], o[G][4];
+};
+
+template <int G>
+__device__ __forceinline__ void softmax_update(WarpState<G>& st, const float (&lg)[4][G],
+                                               const float (&vv)[4][4]) {
+#pragma unroll
+    for (int hh = 0; hh < G; ++hh) {
+        float mx = st.m[hh];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) mx = fmaxf(mx, lg[i][hh]);
+        const float sc = exp2f(st.m[hh] - mx);   // 0 when m was -inf
+        float pi[4];
+        float ps = 0.f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            pi[i] = exp2f(lg[i][hh] - mx);
+            ps += pi[i];
+        }
+        st.l[hh] = st.l[hh] * sc + ps;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            float a = st.o[hh][j] * sc;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) a = fmaf(pi[i], vv[i][j], a);
+            st.o[hh][j] = a;
+        }
+        st.m[hh] = mx;
+    }
+}
+
+template <int G>
+__global__ void __launch_bounds__(128) split_simt(const __grid_constant__ DecodeParams p) {
+    __shared__ float sm_m[4][G], sm_l[4][G];
+    __shared__ float sm_o[4][G][kD];
+    const int b = blockIdx.z;
+    const int h = blockIdx.y;
+    const int s = blockIdx.x;
+    const int len = p.len[b];
+    if (len == 0) return;
+    const int nsp = int2_splits(len, p.pps);
+    if (s > nsp) return;
+    const int w = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const bool bf16_split = (s == nsp);
+    const float qscale = kLog2e * rsqrtf((float)kD);
+
+    // this lane's 4 channels of every query head (rotated for INT2 tokens, plain for BF16)
+    float qr[G][4];
+    float qsum[G];   // sum of this lane's 4 rotated channels (for the m * sum(q) term)
+    const size_t qbase = ((size_t)b * p.hkv * p.g + (size_t)h * p.g) * kD;
+#pragma unroll
+    for (int hh = 0; hh < G; ++hh) {
+        qsum[hh] = 0.f;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const size_t idx = qbase + (size_t)hh * kD + 4 * lane + j;
+            qr[hh][j] = (bf16_split ? load_q(p, idx) : p.qrot[idx]) * qscale;
+            qsum[hh] += qr[hh][j];
+        }
+    }
+    WarpState<G> st;
+#pragma unroll
+    for (int hh = 0; hh < G; ++hh) {
+        st.m[hh] = -INFINITY;
+        st.l[hh] = 0.f;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) st.o[hh][j] = 0.f;
+    }
+
+    if (!bf16_split) {
+        const int n_tok = int2_tokens(len);
+        const int pg_end = min((s + 1) * p.pps, int2_pages(len));
+        const int grp = lane >> 4;   // this lane's 4 channels sit in group lane / 16
+        for (int pg = s * p.pps + w; pg < pg_end; pg += 4) {
+            const int phys = p.page_table[(size_t)b * p.max_pps + pg];
+            const uint8_t* blk = p.pool + ((size_t)phys * p.hkv + h) * kPageHeadBytes;
+            const int nt = min(kPage, n_tok - pg * kPage);
+            for (int t4 = 0; t4 < nt; t4 += 4) {
+                float lg[4][G];
+                float vv[4][4];
+                // V: byte (channel 4*lane + j, tokens t4 .. t4+3)
+                uint32_t vb[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) vb[j] = blk[kVCodes + (4 * lane + j) * 16 + (t4 >> 2)];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int t = t4 + i;
+                    const uint32_t kb = blk[kKCodes + t * 32 + lane];
+                    const uint32_t ksm = *reinterpret_cast<const uint32_t*>(blk + kKSm + t * 8 + grp * 4);
+                    const uint32_t vsm = *reinterpret_cast<const uint32_t*>(blk + kVSm + t * 8 + grp * 4);
+                    const float ks = h2f(ksm & 0xffff), km = h2f(ksm >> 16);
+                    const float vs = h2f(vsm & 0xffff), vm = h2f(vsm >> 16);
+#pragma unroll
+                    for (int hh = 0; hh < G; ++hh) {
+                        float d = 0.f;
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) d = fmaf(qr[hh][j], (float)((kb >> (2 * j)) & 3), d);
+                        lg[i][hh] = fmaf(ks, d, km * qsum[hh]);
+                    }
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) vv[i][j] = fmaf((float)((vb[j] >> (2 * i)) & 3), vs, vm);
+                }
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+#pragma unroll
+                    for (int hh = 0; hh < G; ++hh) {
+                        float x = lg[i][hh];
+#pragma unroll
+                        for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+                        lg[i][hh] = (t4 + i < nt) ? x : -INFINITY;
+                    }
+                softmax_update<G>(st, lg, vv);
+            }
+        }
+    } else {
+        // BF16 tokens: sink slots [0, n_sink) and window slots [sink, sink + n_win)
+        const int n_sink = min(len, kSink);
+        const int n_win = min(kWindow, max(0, len - kSink));
+        const int n_all = n_sink + n_win;
+        const uint16_t* kb = p.bf16 + (((size_t)b * p.hkv + h) * 2 + 0) * kSlots * kD;
+        const uint16_t* vb = p.bf16 + (((size_t)b * p.hkv + h) * 2 + 1) * kSlots * kD;
+        for (int t4 = 4 * w; t4 < n_all; t4 += 16) {
+            float lg[4][G];
+            float vv[4][4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int t = min(t4 + i, n_all - 1);
+                const int slot = t < n_sink ? t : kSink + (t - n_sink);
+                const uint2 kr = *reinterpret_cast<const uint2*>(kb + (size_t)slot * kD + 4 * lane);
+                const uint2 vr = *reinterpret_cast<const uint2*>(vb + (size_t)slot * kD + 4 * lane);
+                const float kf[4] = {bf16f(kr.x & 0xffff), bf16f(kr.x >> 16), bf16f(kr.y & 0xffff),
+                                     bf16f(kr.y >> 16)};
+                vv[i][0] = bf16f(vr.x & 0xffff);
+                vv[i][1] = bf16f(vr.x >> 16);
+                vv[i][2] = bf16f(vr.y & 0xffff);
+                vv[i][3] = bf16f(vr.y >> 16);
+#pragma unroll
+                for (int hh = 0; hh < G; ++hh) {
+                    float d = 0.f;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) d = fmaf(qr[hh][j], kf[j], d);
+                    lg[i][hh] = d;
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int hh = 0; hh < G; ++hh) {
+                    float x = lg[i][hh];
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+                    lg[i][hh] = (t4 + i < n_all) ? x : -INFINITY;
+                }
+            softmax_update<G>(st, lg, vv);
+        }
+    }
+
+    // merge the 4 warps and write this split's partial result
+    if (lane == 0) {
+#pragma unroll
+        for (int hh = 0; hh < G; ++hh) {
+            sm_m[w][hh] = st.m[hh];
+            sm_l[w][hh] = st.l[hh];
+        }
+    }
+#pragma unroll
+    for (int hh = 0; hh < G; ++hh)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) sm_o[w][hh][4 * lane + j] = st.o[hh][j];
+    __syncthreads();
+    const int c = threadIdx.x;
+    float* part = p.partial + (((size_t)b * p.hkv + h) * p.max_splits + s) * p.g * (2 + kD);
+    for (int hh = 0; hh < G; ++hh) {
+        float M = -INFINITY;
+#pragma unroll
+        for (int ww = 0; ww < 4; ++ww) M = fmaxf(M, sm_m[ww][hh]);
+        float L = 0.f, O = 0.f;
+#pragma unroll
+        for (int ww = 0; ww < 4; ++ww) {
+            const float f = sm_m[ww][hh] == -INFINITY ? 0.f : exp2f(sm_m[ww][hh] - M);
+            L = fmaf(f, sm_l[ww][hh], L);
+            O = fmaf(f, sm_o[ww][hh][c], O);
+        }
+        float* ph = part + (size_t)hh * (2 + kD);
+        if (c == 0) {
+            ph[0] = M;
+            ph[1] = L;
+        }
+        ph[2 + c] = O;
+    }
+}
+
+__global__ void __launch_bounds__(128) combine(const __grid_constant__ DecodeParams p) {
+    const int b = blockIdx.y;
+    const int hq = blockIdx.x;
+    const int h = hq / p.g;
+    const int hh = hq % p.g;
+    const int c = threadIdx.x;
+    const int len = p.len[b];
+    const size_t oidx = ((size_t)b * p.hkv * p.g + hq) * kD + c;
+    float res = 0.f;
+    if (len > 0) {
+        const int ns = int2_splits(len, p.pps) + 1;
+        const float* part = p.partial + ((size_t)b * p.hkv + h) * p.max_splits * p.g * (2 + kD);
+        float M = -INFINITY;
+        for (int s = 0; s < ns; ++s) M = fmaxf(M, part[((size_t)s * p.g + hh) * (2 + kD)]);
+        float L = 0.f, O = 0.f;
+        for (int s = 0; s < ns; ++s) {
+            const float* ph = part + ((size_t)s * p.g + hh) * (2 + kD);
+            const float f = ph[0] == -INFINITY ? 0.f : exp2f(ph[0] - M);
+            L = fmaf(f, ph[1], L);
+            O = fmaf(f, ph[2 + c], O);
+        }
+        res = O / L;
+    }
+    if (p.out_dtype == 0)
+        reinterpret_cast<float*>(p.out)[oidx] = res;
+    else
+        reinterpret_cast<__nv_bfloat16*>(p.out)[oidx] = __float2bfloat16_rn(res);
+}
+
+template <int G>
+cudaError_t launch_split(const DecodeParams& p, int max_ns, cudaStream_t s) {
+    split_simt<G><<<dim3(max_ns, p.hkv, p.batch), 128, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_decode(const DecodeParams& p, cudaStream_t s) {
+    int max_ns = 1;
+    for (int b = 0; b < p.batch; ++b) max_ns = max(max_ns, int2_splits(p.len[b], p.pps) + 1);
+    rotate_q<<<dim3(p.hkv, p.batch), 128, 0, s>>>(p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    switch (p.g) {
+        case 1: e = launch_split<1>(p, max_ns, s); break;
+        case 2: e = launch_split<2>(p, max_ns, s); break;
+        case 3: e = launch_split<3>(p, max_ns, s); break;
+        case 4: e = launch_split<4>(p, max_ns, s); break;
+        case 5: e = launch_split<5>(p, max_ns, s); break;
+        case 6: e = launch_split<6>(p, max_ns, s); break;
+        case 7: e = launch_split<7>(p, max_ns, s); break;
+        case 8: e = launch_split<8>(p, max_ns, s); break;
+        case 12: e = launch_split<12>(p, max_ns, s); break;
+        case 16: e = launch_split<16>(p, max_ns, s); break;
+        default: return cudaErrorInvalidValue;
+    }
+    if (e != cudaSuccess) return e;
+    combine<<<dim3(p.hkv * p.g, p.batch), 128, 0, s>>>(p);
+    count_launches(3);
+    return cudaGetLastError();
+}
+
+}  // namespace oscar

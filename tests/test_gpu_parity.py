@@ -1,0 +1,166 @@
+"""GPU parity: the CUDA write path is bit-exact against the CPU oracle (codes and fp16
+scale/min of every INT2 token, BF16 sink/window bytes), and decode attention is within
+relative L2 1e-3 and max-abs 2e-3 of the oracle's fp64 attention on the same cache.
+Everything is called through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+import int2_rotated_paged_gb300 as K
+from gpu_util import (append_initial, check_bf16_bytes, check_int2_bytes, decode_query, make_cache,
+                      oracle_caches, oracle_rk, rel_l2)
+
+pytestmark = pytest.mark.gpu
+
+REL_L2 = 1e-3
+MAX_ABS = 2e-3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from int2_rotated_paged_gb300 import build
+    build.build()
+    oracle.build()
+    assert torch.cuda.is_available()
+
+
+def _attend(cache, q, rk_dev, out_dtype=torch.float32):
+    out = torch.empty(q.shape, dtype=out_dtype, device="cuda")
+    cache.attend(q, rk_dev, out)
+    torch.cuda.synchronize()
+    return out.float().cpu().numpy()
+
+
+def _check_attention(out, q, ocs, cfg):
+    g = cfg.group
+    worst = 0.0
+    for (b, h), oc in ocs.items():
+        ref, _ = oc.attend(q[b, h * g:(h + 1) * g].cpu().numpy())
+        got = out[b, h * g:(h + 1) * g]
+        r = rel_l2(got, ref)
+        m = float(np.abs(got - ref).max())
+        worst = max(worst, r)
+        assert r <= REL_L2 and m <= MAX_ABS, f"(b={b}, h={h}): rel-L2 {r:.3e}, max-abs {m:.3e}"
+    return worst
+
+
+def _run(cfg, lens, pairs=None, steps=2, chunks=None, table=None, check_bytes=True, out_dtype=torch.float32):
+    rk = oracle_rk(cfg.seed, cfg.num_kv_heads, 1024)
+    rk_dev = torch.tensor(rk, device="cuda")
+    cache = make_cache(cfg, max(lens) + steps, table)
+    append_initial(cache, cfg, lens, rk_dev, chunks)
+    pairs = pairs or [(b, h) for b in range(cfg.batch) for h in range(cfg.num_kv_heads)]
+    ocs = oracle_caches(cfg, pairs, lens, rk)
+    cur = list(lens)
+    for step in range(steps):
+        if check_bytes:
+            for (b, h), oc in ocs.items():
+                check_int2_bytes(cache, oc, b, h)
+                check_bf16_bytes(cache, oc, b, h)
+        q = decode_query(cfg, step)
+        out = _attend(cache, q, rk_dev, out_dtype)
+        if out_dtype == torch.float32:
+            _check_attention(out, q, ocs, cfg)
+        else:
+            g = cfg.group
+            for (b, h), oc in ocs.items():
+                ref, _ = oc.attend(q[b, h * g:(h + 1) * g].cpu().numpy())
+                refb = torch.tensor(ref).to(torch.bfloat16).float().numpy()
+                got = out[b, h * g:(h + 1) * g]
+                ulp = np.abs(refb) * 2.0 ** -7
+                assert (np.abs(got - refb) <= ulp + 1e-30).mean() >= 0.999
+        # one decode token per request, then the next step attends over it too
+        n = [1] * cfg.batch
+        k, v = synth.kv_block(cfg.seed, n, cur, cfg.num_kv_heads, device="cuda")
+        cache.append(k, v, n, rk_dev)
+        for (b, h), oc in ocs.items():
+            oc.append(synth.bf16_bits(k[b, h][None]), synth.bf16_bits(v[b, h][None]))
+        cur = [c + 1 for c in cur]
+    return cache, ocs
+
+
+def test_tiny_config_bulk_then_decode():
+    cfg = synth.config("tiny")
+    _run(cfg, cfg.ctx, steps=cfg.decode_steps)
+
+
+def test_incremental_append_matches_bulk():
+    cfg = synth.scaled(synth.config("qwen3_4b"), [700, 333, 321, 1024], batch=4)
+    # chunked appends of odd sizes must store exactly what one bulk append stores
+    _run(cfg, cfg.ctx, steps=1, chunks=[1, 7, 64, 100, 3, 300, 256])
+
+
+@pytest.mark.parametrize("lens", [[0, 1, 63, 64], [65, 319, 320, 321], [383, 384, 385, 448],
+                                  [320 + 64 * 5 - 1, 320 + 64 * 5, 320 + 64 * 5 + 1, 2]])
+def test_lengths_at_region_and_page_edges(lens):
+    cfg = synth.scaled(synth.config("qwen3_4b"), lens, batch=4)
+    _run(cfg, lens, steps=3)
+
+
+@pytest.mark.parametrize("hq,hkv", [(2, 2), (8, 2), (16, 2), (24, 2), (32, 2), (12, 2), (14, 2)])
+def test_gqa_group_sizes(hq, hkv):
+    base = synth.config("qwen3_4b")
+    cfg = synth.LayerConfig("gqa", 2, hq, hkv, [1500, 900], 2, "permuted", "bf16", 4242)
+    _run(cfg, cfg.ctx, steps=2)
+
+
+def test_qwen3_4b_shape_sampled_heads():
+    cfg = synth.config("qwen3_4b")
+    pairs = [(0, 0), (3, 5), (7, 7)]
+    _run(cfg, cfg.ctx, pairs=pairs, steps=2)
+
+
+def test_bf16_output_and_bf16_query():
+    cfg = synth.scaled(synth.config("qwen3_8b"), [2000, 700], batch=2)
+    _run(cfg, cfg.ctx, steps=1, out_dtype=torch.bfloat16)
+
+
+def test_page_order_does_not_change_output():
+    cfg = synth.scaled(synth.config("qwen3_4b"), [3000, 1400, 2500], batch=3)
+    rk = oracle_rk(cfg.seed, cfg.num_kv_heads, 1024)
+    rk_dev = torch.tensor(rk, device="cuda")
+    outs = []
+    for table in ("contiguous", "permuted"):
+        cache = make_cache(cfg, max(cfg.ctx), table)
+        append_initial(cache, cfg, cfg.ctx, rk_dev)
+        q = decode_query(cfg, 0)
+        outs.append(_attend(cache, q, rk_dev))
+    assert np.array_equal(outs[0], outs[1])
+
+
+def test_release_and_reuse_pages():
+    cfg = synth.scaled(synth.config("qwen3_4b"), [900, 900], batch=2)
+    rk = oracle_rk(cfg.seed, cfg.num_kv_heads, 1024)
+    rk_dev = torch.tensor(rk, device="cuda")
+    cache = make_cache(cfg, 1000)
+    append_initial(cache, cfg, [900, 900], rk_dev)
+    K.kv_page_table_release(cache.handle, 0)
+    assert cache.length(0) == 0
+    q = decode_query(cfg, 0)
+    out = _attend(cache, q, rk_dev)
+    assert np.all(out[0] == 0)                     # an empty request attends to nothing
+    # refill request 0 with other tokens: pages come back from the free list
+    k, v = synth.kv_block(cfg.seed + 1, [800, 0], [0, 0], cfg.num_kv_heads, device="cuda")
+    cache.append(k, v, [800, 0], rk_dev)
+    oc = oracle.OracleCache(rk[1])
+    oc.append(synth.bf16_bits(k[:, 1]), synth.bf16_bits(v[:, 1]))
+    check_int2_bytes(cache, oc, 0, 1)
+    out = _attend(cache, q, rk_dev)
+    ref, _ = oc.attend(q[0, cfg.group:2 * cfg.group].cpu().numpy())
+    assert rel_l2(out[0, cfg.group:2 * cfg.group], ref) <= REL_L2
+
+
+def test_build_rk_on_gpu_matches_oracle():
+    hkv, n = 4, 4096
+    q = torch.stack([synth.calibration_queries(77, h, n) for h in range(hkv)]).cuda().contiguous()
+    rk = torch.empty(hkv, 128, 128, device="cuda")
+    ws = torch.empty(K.oscar_build_rk_workspace_bytes(hkv), dtype=torch.uint8, device="cuda")
+    K.oscar_build_rk(q, n, hkv, rk, ws)
+    torch.cuda.synchronize()
+    got = rk.cpu().numpy().astype(np.float64)
+    for h in range(hkv):
+        ref32, ref64, _ = oracle.build_rk(q[h].cpu().numpy())
+        assert np.abs(got[h] - ref64).max() < 1e-6
+        assert np.abs(got[h] @ got[h].T - np.eye(128)).max() < 1e-6
