@@ -49,6 +49,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-pairs", type=int, default=3, help="(request, KV head) pairs the CPU oracle times")
+    ap.add_argument("--path", default="tensor", choices=["tensor", "simt"],
+                    help="decode kernel: tcgen05 tensor cores (default) or the SIMT baseline")
     return ap.parse_args()
 
 
@@ -199,6 +201,7 @@ def run_ours(args, cfg, rank, world, dist):
     from int2_rotated_paged_gb300 import build as kbuild
 
     kbuild.build()
+    K.oscar_set_decode_path(K.PATH_TENSOR if args.path == "tensor" else K.PATH_SIMT)
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
     stream = torch.cuda.current_stream()
@@ -276,6 +279,7 @@ def run_ours(args, cfg, rank, world, dist):
     t1.record(stream)
     torch.cuda.synchronize()
     clk = clocks.stop()
+    cache.status()          # raises if a bounded in-kernel wait gave up
     if dist is not None:
         dist.barrier()
     launches = K.oscar_launch_count() - launches0
@@ -346,7 +350,8 @@ def run_ours(args, cfg, rank, world, dist):
                                f"(append 1 token + split-K GQA decode), {cfg.table} pages",
                    "batch_per_gpu": B, "context": lens0[0], "l2": "inputs larger than L2 (about 2.1 GB per step vs 129 MB)"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "peak_kind": peak_kind, "kernel": "oscar_decode_attention (rotate_q + split + combine)",
+                     "peak_kind": peak_kind, "kernel": f"oscar_decode_attention, {args.path} path (rotate_q + bf16 split + "
+                               f"{'decode_tc' if args.path == 'tensor' else 'split_simt'} + combine)",
                      "traffic": profiled_traffic("decode.cu"), "bytes_per_call": dec_bytes,
                      "ms_per_call": dec_t * 1e3},
         "append": {"prefill_tokens_per_s": tok_append / t_append, "prefill_tokens": tok_append,

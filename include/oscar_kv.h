@@ -54,6 +54,7 @@ extern "C" {
 #define OSCAR_ECUDA (-4)      /* a CUDA call failed */
 #define OSCAR_EALIGN (-5)     /* a device pointer is not 16-byte aligned */
 #define OSCAR_ERANGE (-6)     /* a request index or position is out of range */
+#define OSCAR_ETIMEOUT (-7)   /* a bounded wait inside a kernel gave up (see oscar_decode_status) */
 
 #define OSCAR_DTYPE_F32 0
 #define OSCAR_DTYPE_BF16 1
@@ -179,6 +180,20 @@ size_t oscar_decode_workspace_bytes(const oscar_cache *c);
 int oscar_decode_attention(oscar_cache *c, const void *q, int32_t q_dtype, const float *rk,
                            void *out, int32_t out_dtype, void *workspace, size_t workspace_bytes,
                            void *stream);
+
+/* Which decode kernel oscar_decode_attention runs (process-wide; default tensor cores):
+ * OSCAR_PATH_TENSOR: persistent warp-specialised kernel, tcgen05 MMAs with the dequantised
+ *                    pages in tensor memory; OSCAR_PATH_SIMT: one CTA per split, CUDA-core
+ *                    dot products (kept as the baseline the tensor-core path is measured
+ *                    against).  Both give the same result within the parity tolerance. */
+#define OSCAR_PATH_TENSOR 0
+#define OSCAR_PATH_SIMT 1
+int oscar_set_decode_path(int32_t path);
+/* Synchronise `stream` and report whether the last decode call that used `workspace`
+ * completed normally (OSCAR_OK) or one of its bounded in-kernel waits gave up
+ * (OSCAR_ETIMEOUT; its output is then undefined). */
+int oscar_decode_status(const void *workspace, size_t workspace_bytes, const oscar_cache *c,
+                        void *stream);
 
 /* ---------------------------------------------------------------- calibration
  * oscar_build_rk: R_K = U_Q * H_Had * P_br for num_kv_heads heads from n query samples

@@ -35,7 +35,11 @@ EXPORTS = [
     "kv_page_table_free_pages", "kv_quant_append", "oscar_decode_workspace_bytes",
     "oscar_decode_attention", "oscar_build_rk_workspace_bytes", "oscar_build_rk", "oscar_read_int2",
     "oscar_read_bf16", "oscar_strerror", "oscar_last_cuda_error", "oscar_launch_count",
+    "oscar_set_decode_path", "oscar_decode_status",
 ]
+OSCAR_ETIMEOUT = -7
+PATH_TENSOR = 0
+PATH_SIMT = 1
 
 
 class OscarError(RuntimeError):
@@ -91,6 +95,8 @@ def lib() -> ctypes.CDLL:
         "oscar_strerror": (ctypes.c_char_p, [ctypes.c_int]),
         "oscar_last_cuda_error": (ctypes.c_int, []),
         "oscar_launch_count": (I64, []),
+        "oscar_set_decode_path": (ctypes.c_int, [I32]),
+        "oscar_decode_status": (ctypes.c_int, [P, SZ, P, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -224,6 +230,15 @@ def oscar_cache_length(cache, b: int) -> int:
     return _check("oscar_cache_length", lib().oscar_cache_length(cache, b))
 
 
+def oscar_set_decode_path(path: int):
+    _check("oscar_set_decode_path", lib().oscar_set_decode_path(path))
+
+
+def oscar_decode_status(cache, workspace, stream=None):
+    nbytes = workspace.numel() * workspace.element_size()
+    _check("oscar_decode_status", lib().oscar_decode_status(_ptr(workspace), nbytes, cache, _stream(stream)))
+
+
 def oscar_launch_count() -> int:
     return int(lib().oscar_launch_count())
 
@@ -269,6 +284,10 @@ class Cache:
         qd = DTYPE_BF16 if str(q.dtype) == "torch.bfloat16" else DTYPE_F32
         od = DTYPE_BF16 if str(out.dtype) == "torch.bfloat16" else DTYPE_F32
         oscar_decode_attention(self.handle, q, qd, rk, out, od, self.workspace, stream)
+
+    def status(self, stream=None):
+        """Raise if the last decode on this cache's workspace hit a bounded in-kernel wait."""
+        oscar_decode_status(self.handle, self.workspace, stream)
 
     def length(self, b: int) -> int:
         return oscar_cache_length(self.handle, b)

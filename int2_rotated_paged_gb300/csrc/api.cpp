@@ -307,7 +307,8 @@ int kv_quant_append(oscar_cache* c, const void* k, const void* v, const int32_t*
 
 // ------------------------------------------------------------------ read path
 
-static const int kMaxSplits = 128;   // INT2 splits + 1 BF16 split per (request, KV head)
+static const int kMaxSplits = 64;   // SIMT path: INT2 splits + 1 BF16 split per (request, KV head)
+static std::atomic<int> g_decode_path{0};
 
 static int pick_pps(const oscar_cache* c) {
     int64_t total = 0;
@@ -323,11 +324,56 @@ static int pick_pps(const oscar_cache* c) {
     return (int)pps;
 }
 
+static int sm_count() {
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    if (!cached[dev]) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        cached[dev] = n;
+    }
+    return cached[dev];
+}
+
+struct WsLayout {
+    size_t qrot, simt, tc, bf16, err, total;
+};
+
+static WsLayout ws_layout(const oscar_cache* c) {
+    const size_t per = (size_t)c->g * (2 + kD) * sizeof(float);
+    const size_t bh = (size_t)c->d.batch * c->d.num_kv_heads;
+    WsLayout w;
+    w.qrot = 0;
+    w.simt = w.qrot + (size_t)c->d.batch * c->d.num_q_heads * kD * sizeof(float);
+    w.tc = w.simt + bh * kMaxSplits * per;
+    w.bf16 = w.tc + (bh + kMaxCtas) * per;
+    w.err = w.bf16 + bh * per;
+    w.total = w.err + 16;
+    return w;
+}
+
 size_t oscar_decode_workspace_bytes(const oscar_cache* c) {
     if (!c) return 0;
-    size_t qrot = (size_t)c->d.batch * c->d.num_q_heads * kD * sizeof(float);
-    size_t part = (size_t)c->d.batch * c->d.num_kv_heads * kMaxSplits * c->g * (2 + kD) * sizeof(float);
-    return qrot + part;
+    return ws_layout(c).total;
+}
+
+int oscar_set_decode_path(int32_t path) {
+    if (path != OSCAR_PATH_TENSOR && path != OSCAR_PATH_SIMT) return OSCAR_EINVAL;
+    g_decode_path = path;
+    return OSCAR_OK;
+}
+
+int oscar_decode_status(const void* workspace, size_t workspace_bytes, const oscar_cache* c, void* stream) {
+    if (!c || !workspace) return OSCAR_EINVAL;
+    const WsLayout w = ws_layout(c);
+    if (workspace_bytes < w.total) return OSCAR_EWORKSPACE;
+    int32_t err = 0;
+    cudaError_t e = cudaMemcpyAsync(&err, (const uint8_t*)workspace + w.err, sizeof(err), cudaMemcpyDeviceToHost,
+                                    S(stream));
+    if (e == cudaSuccess) e = cudaStreamSynchronize(S(stream));
+    if (e != cudaSuccess) return cuda_fail(e);
+    return err ? OSCAR_ETIMEOUT : OSCAR_OK;
 }
 
 int oscar_decode_attention(oscar_cache* c, const void* q, int32_t q_dtype, const float* rk,
@@ -357,9 +403,28 @@ int oscar_decode_attention(oscar_cache* c, const void* q, int32_t q_dtype, const
     p.bf16 = c->bf16;
     p.page_table = c->pt;
     p.max_pps = c->d.max_pages_per_seq;
-    p.qrot = (float*)workspace;
-    p.partial = p.qrot + (size_t)c->d.batch * c->d.num_q_heads * kD;
-    for (int32_t b = 0; b < c->d.batch; ++b) p.len[b] = (int32_t)c->len[b];
+    const WsLayout w = ws_layout(c);
+    uint8_t* ws = (uint8_t*)workspace;
+    p.qrot = (float*)(ws + w.qrot);
+    p.partial = (float*)(ws + w.simt);
+    p.part_tc = (float*)(ws + w.tc);
+    p.part_bf16 = (float*)(ws + w.bf16);
+    p.err = (int32_t*)(ws + w.err);
+    p.path = g_decode_path;
+    int64_t tiles = 0;
+    for (int32_t b = 0; b < c->d.batch; ++b) {
+        p.len[b] = (int32_t)c->len[b];
+        p.tile_off[b] = (int32_t)tiles;
+        tiles += (int64_t)int2_tiles(p.len[b]) * c->d.num_kv_heads;
+    }
+    p.tile_off[c->d.batch] = (int32_t)tiles;
+    if (tiles > INT32_MAX / 2) return OSCAR_ERANGE;
+    p.total_tiles = (int32_t)tiles;
+    if (p.path == 0 && tiles > 0) {
+        const int sms = sm_count();
+        if (sms <= 0) return cuda_fail(cudaGetLastError());
+        p.n_cta = (int32_t)std::min<int64_t>(std::min(sms, kMaxCtas), tiles);
+    }
     cudaError_t e = launch_decode(p, S(stream));
     return e == cudaSuccess ? OSCAR_OK : cuda_fail(e);
 }
@@ -457,6 +522,7 @@ const char* oscar_strerror(int code) {
         case OSCAR_ECUDA: return "CUDA error";
         case OSCAR_EALIGN: return "device pointer not 16-byte aligned";
         case OSCAR_ERANGE: return "index or position out of range";
+        case OSCAR_ETIMEOUT: return "a kernel wait timed out";
         default: return "unknown error";
     }
 }

@@ -40,6 +40,7 @@ __global__ void __launch_bounds__(128) rotate_q(const __grid_constant__ DecodePa
     const int b = blockIdx.y;
     const int h = blockIdx.x;
     const int c = threadIdx.x;
+    if (b == 0 && h == 0 && c == 0 && p.err) *p.err = 0;
     const size_t qbase = ((size_t)b * p.hkv * p.g + (size_t)h * p.g) * kD;
     for (int i = 0; i < p.g; ++i) qs[i][c] = load_q(p, qbase + (size_t)i * kD + c);
     __syncthreads();
@@ -95,10 +96,11 @@ __global__ void __launch_bounds__(128) split_simt(const __grid_constant__ Decode
     __shared__ float sm_o[4][G][kD];
     const int b = blockIdx.z;
     const int h = blockIdx.y;
-    const int s = blockIdx.x;
     const int len = p.len[b];
     if (len == 0) return;
     const int nsp = int2_splits(len, p.pps);
+    // tensor-core path: this kernel only handles the BF16 split (one CTA per request and head)
+    const int s = p.path == 0 ? nsp : (int)blockIdx.x;
     if (s > nsp) return;
     const int w = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -158,8 +160,12 @@ __global__ void __launch_bounds__(128) split_simt(const __grid_constant__ Decode
                         for (int j = 0; j < 4; ++j) d = fmaf(qr[hh][j], (float)((kb >> (2 * j)) & 3), d);
                         lg[i][hh] = fmaf(ks, d, km * qsum[hh]);
                     }
+                    // slots past the request's last token hold stale bytes (possibly NaN
+                    // scales): their values must be exact zeros, not 0 * garbage
+                    const bool live = t < nt;
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) vv[i][j] = fmaf((float)((vb[j] >> (2 * i)) & 3), vs, vm);
+                    for (int j = 0; j < 4; ++j)
+                        vv[i][j] = live ? fmaf((float)((vb[j] >> (2 * i)) & 3), vs, vm) : 0.f;
                 }
 #pragma unroll
                 for (int i = 0; i < 4; ++i)
@@ -230,7 +236,8 @@ __global__ void __launch_bounds__(128) split_simt(const __grid_constant__ Decode
         for (int j = 0; j < 4; ++j) sm_o[w][hh][4 * lane + j] = st.o[hh][j];
     __syncthreads();
     const int c = threadIdx.x;
-    float* part = p.partial + (((size_t)b * p.hkv + h) * p.max_splits + s) * p.g * (2 + kD);
+    float* part = p.path == 0 ? p.part_bf16 + ((size_t)b * p.hkv + h) * p.g * (2 + kD)
+                              : p.partial + (((size_t)b * p.hkv + h) * p.max_splits + s) * p.g * (2 + kD);
     for (int hh = 0; hh < G; ++hh) {
         float M = -INFINITY;
 #pragma unroll
@@ -251,6 +258,22 @@ __global__ void __launch_bounds__(128) split_simt(const __grid_constant__ Decode
     }
 }
 
+// CTA of the tensor-core kernel that owns tile T (CTA c owns [c T_all / C, (c + 1) T_all / C)).
+__device__ __forceinline__ int cta_of(const DecodeParams& p, int T) {
+    return (int)((((long long)T + 1) * p.n_cta - 1) / p.total_tiles);
+}
+
+__device__ __forceinline__ void merge(const float* ph, int c, float& M, float& L, float& O) {
+    const float m = ph[0];
+    if (m == -INFINITY) return;
+    const float nm = fmaxf(M, m);
+    const float fa = M == -INFINITY ? 0.f : exp2f(M - nm);
+    const float fb = exp2f(m - nm);
+    L = L * fa + ph[1] * fb;
+    O = O * fa + ph[2 + c] * fb;
+    M = nm;
+}
+
 __global__ void __launch_bounds__(128) combine(const __grid_constant__ DecodeParams p) {
     const int b = blockIdx.y;
     const int hq = blockIdx.x;
@@ -261,16 +284,21 @@ __global__ void __launch_bounds__(128) combine(const __grid_constant__ DecodePar
     const size_t oidx = ((size_t)b * p.hkv * p.g + hq) * kD + c;
     float res = 0.f;
     if (len > 0) {
-        const int ns = int2_splits(len, p.pps) + 1;
-        const float* part = p.partial + ((size_t)b * p.hkv + h) * p.max_splits * p.g * (2 + kD);
-        float M = -INFINITY;
-        for (int s = 0; s < ns; ++s) M = fmaxf(M, part[((size_t)s * p.g + hh) * (2 + kD)]);
-        float L = 0.f, O = 0.f;
-        for (int s = 0; s < ns; ++s) {
-            const float* ph = part + ((size_t)s * p.g + hh) * (2 + kD);
-            const float f = ph[0] == -INFINITY ? 0.f : exp2f(ph[0] - M);
-            L = fmaf(f, ph[1], L);
-            O = fmaf(f, ph[2 + c], O);
+        float M = -INFINITY, L = 0.f, O = 0.f;
+        if (p.path == 0) {
+            const int u = b * p.hkv + h;
+            merge(p.part_bf16 + ((size_t)u * p.g + hh) * (2 + kD), c, M, L, O);
+            const int tiles = int2_tiles(len);
+            if (tiles > 0) {
+                const int tf = p.tile_off[b] + h * tiles;
+                const int c0 = cta_of(p, tf), c1 = cta_of(p, tf + tiles - 1);
+                for (int k = c0; k <= c1; ++k)
+                    merge(p.part_tc + (((size_t)u + k) * p.g + hh) * (2 + kD), c, M, L, O);
+            }
+        } else {
+            const int ns = int2_splits(len, p.pps) + 1;
+            const float* part = p.partial + ((size_t)b * p.hkv + h) * p.max_splits * p.g * (2 + kD);
+            for (int s = 0; s < ns; ++s) merge(part + ((size_t)s * p.g + hh) * (2 + kD), c, M, L, O);
         }
         res = O / L;
     }
@@ -290,7 +318,8 @@ cudaError_t launch_split(const DecodeParams& p, int max_ns, cudaStream_t s) {
 
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t s) {
     int max_ns = 1;
-    for (int b = 0; b < p.batch; ++b) max_ns = max(max_ns, int2_splits(p.len[b], p.pps) + 1);
+    if (p.path != 0)
+        for (int b = 0; b < p.batch; ++b) max_ns = max(max_ns, int2_splits(p.len[b], p.pps) + 1);
     rotate_q<<<dim3(p.hkv, p.batch), 128, 0, s>>>(p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
@@ -308,6 +337,10 @@ cudaError_t launch_decode(const DecodeParams& p, cudaStream_t s) {
         default: return cudaErrorInvalidValue;
     }
     if (e != cudaSuccess) return e;
+    if (p.path == 0) {
+        e = launch_decode_tc(p, s);
+        if (e != cudaSuccess) return e;
+    }
     combine<<<dim3(p.hkv * p.g, p.batch), 128, 0, s>>>(p);
     count_launches(3);
     return cudaGetLastError();

@@ -64,8 +64,16 @@ struct DecodeParams {
     const int32_t* page_table;
     int32_t max_pps;
     float* qrot;           // [batch][hkv*g][128]
-    float* partial;        // [batch][hkv][max_splits][g][2 + 128]
+    float* partial;        // SIMT path: [batch][hkv][max_splits][g][2 + 128]
     int32_t len[kMaxBatch];
+    // tensor-core path
+    int32_t path;          // 0 = tensor cores, 1 = SIMT
+    int32_t n_cta;         // persistent CTAs
+    int32_t total_tiles;   // 128-token INT2 tiles over all (request, KV head)
+    float* part_tc;        // [batch * hkv + n_cta][g][2 + 128], segment id = (b * hkv + h) + cta
+    float* part_bf16;      // [batch * hkv][g][2 + 128]
+    int32_t* err;          // nonzero after a bounded wait gave up
+    int32_t tile_off[kMaxBatch + 1];   // sum over earlier requests of tiles * hkv
 };
 
 // Split-K partition of one request: INT2 splits of `pps` pages plus one BF16 split.
@@ -79,9 +87,16 @@ __host__ __device__ inline int int2_splits(int len, int pps) {
     return (int2_pages(len) + pps - 1) / pps;
 }
 
+constexpr int kTileTok = 128;          // tokens per tensor-core tile (two pages)
+constexpr int kMaxCtas = 1024;
+__host__ __device__ inline int int2_tiles(int len) {
+    return (int2_tokens(len) + kTileTok - 1) / kTileTok;
+}
+
 // Launchers (each returns the cudaError_t of its launch).
 cudaError_t launch_append(const AppendParams& p, cudaStream_t s);
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t s);
+cudaError_t launch_decode_tc(const DecodeParams& p, cudaStream_t s);
 cudaError_t launch_build_rk(const float* q, int64_t n, int hkv, float* rk, void* ws, cudaStream_t s);
 size_t build_rk_ws_bytes(int hkv);
 

@@ -26,9 +26,18 @@ def _built():
     assert torch.cuda.is_available()
 
 
+@pytest.fixture(params=["tensor", "simt"], autouse=True)
+def decode_path(request):
+    """Every test runs against both decode kernels: tcgen05 tensor cores and the SIMT baseline."""
+    K.oscar_set_decode_path(K.PATH_TENSOR if request.param == "tensor" else K.PATH_SIMT)
+    yield request.param
+    K.oscar_set_decode_path(K.PATH_TENSOR)
+
+
 def _attend(cache, q, rk_dev, out_dtype=torch.float32):
     out = torch.empty(q.shape, dtype=out_dtype, device="cuda")
     cache.attend(q, rk_dev, out)
+    cache.status()          # raises if a bounded in-kernel wait gave up
     torch.cuda.synchronize()
     return out.float().cpu().numpy()
 
