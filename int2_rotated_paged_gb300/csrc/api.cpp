@@ -347,7 +347,7 @@ static WsLayout ws_layout(const oscar_cache* c) {
     w.qrot = 0;
     w.simt = w.qrot + (size_t)c->d.batch * c->d.num_q_heads * kD * sizeof(float);
     w.tc = w.simt + bh * kMaxSplits * per;
-    w.bf16 = w.tc + (bh + kMaxCtas) * per;
+    w.bf16 = w.tc + (bh + kMaxCtas) * 2 * per;   // two token groups per (segment, CTA)
     w.err = w.bf16 + bh * per;
     w.total = w.err + 16;
     return w;

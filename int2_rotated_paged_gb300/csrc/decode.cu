@@ -290,10 +290,19 @@ __global__ void __launch_bounds__(128) combine(const __grid_constant__ DecodePar
             merge(p.part_bf16 + ((size_t)u * p.g + hh) * (2 + kD), c, M, L, O);
             const int tiles = int2_tiles(len);
             if (tiles > 0) {
+                // segment of (b, h) inside CTA k: tiles [lo, hi); its token groups 0 and 1
+                // took the tiles of even and odd local index, each writing its own partial
                 const int tf = p.tile_off[b] + h * tiles;
                 const int c0 = cta_of(p, tf), c1 = cta_of(p, tf + tiles - 1);
-                for (int k = c0; k <= c1; ++k)
-                    merge(p.part_tc + (((size_t)u + k) * p.g + hh) * (2 + kD), c, M, L, O);
+                for (int k = c0; k <= c1; ++k) {
+                    const int start = (int)(((long long)k * p.total_tiles) / p.n_cta);
+                    const int end = (int)(((long long)(k + 1) * p.total_tiles) / p.n_cta);
+                    const int lo = max(start, tf), hi = min(end, tf + tiles);
+                    for (int w = 0; w < 2; ++w) {
+                        if (hi - lo < 2 && ((lo - start) & 1) != w) continue;   // group w took no tile
+                        merge(p.part_tc + ((((size_t)u + k) * 2 + w) * p.g + hh) * (2 + kD), c, M, L, O);
+                    }
+                }
             }
         } else {
             const int ns = int2_splits(len, p.pps) + 1;

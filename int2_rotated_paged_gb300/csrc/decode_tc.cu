@@ -8,26 +8,29 @@
 //
 // One persistent CTA per SM walks a contiguous range of 128-token tiles (two INT2 pages) of
 // the flattened (request, KV head, tile) list, so every SM streams the same number of bytes
-// whatever the request lengths.  Roles (10 warps):
-//   warp 8      producer: bulk-async copies of each tile's two 5120-byte page blocks into a
-//               10-stage shared-memory ring (page-table entries fetched one batch ahead);
-//   warps 0-3   dequant: thread = TMEM lane.  Keys: thread = token, its 128 2-bit codes become
-//               64 fp16x2 words (1 + code/4) stored to TMEM; values (channel-major pages):
-//               thread = channel, its 128 tokens' codes likewise;
-//   warp 9      MMA: S = A_K x Q^T (M = 128 tokens, N = 2G padded: q split in fp16 hi + lo,
-//               one accumulator per 64-channel group) and O += A_V x P'^T (M = 128 channels,
-//               K = tokens, N = 2G: p * s_V per head and group), tcgen05.mma kind::f16 with A
-//               read from TMEM and B from shared memory, fp32 accumulators in TMEM;
-//   warps 4-7   softmax: thread = token.  logit = sum_g 4 s_g S_g + (m_g - 4 s_g) sum_g(q~),
-//               online softmax with a lazily raised reference (rescale O only when a logit
-//               exceeds the reference by 2^8), P' stores for the PV MMA, and the per-segment
-//               flush out = sum_t p m_V + 4 (O - sum_t P') of each (request, KV head) run.
-// A segment's result (reference max, sum, unnormalised output) goes to the split-K partial
-// buffer; combine (decode.cu) merges segments and the BF16 sink / window part.
+// whatever the request lengths.  Sixteen warps in four warpgroups:
+//   WG0, WG1  token groups (thread = token = TMEM lane), alternating tiles: unpack the tile's
+//             2-bit key codes to fp16 (1 + code/4) into their own TMEM A buffer, then run
+//             the online softmax of that tile on their own score and output accumulators:
+//             logit = sum_g 4 s_g S_g + (m_g - 4 s_g) sum_{c in g} q~_c, a reference max that
+//             is raised only when a logit passes it by 2^8 (then O is rescaled once),
+//             P' = p * s_V per head and group stored as the B operand of the PV product;
+//   WG2       value group (thread = channel = TMEM lane): unpacks the tile's channel-major
+//             value codes into a 3-deep ring of TMEM A buffers;
+//   WG3       warp 12 producer (bulk-async copies of each tile's two 5120-byte page blocks into
+//             a 10-stage shared-memory ring, page-table entries fetched a batch ahead),
+//             warp 13 issues S = A_K x Q^T (M 128 tokens, N 16, q split into fp16 hi and lo
+//             halves that two MMAs add into one accumulator per 64-channel group), warp 14
+//             issues O += A_V x P'^T (M 128 channels, K tokens, N = 2G padded), all
+//             tcgen05.mma kind::f16 with A read from TMEM, fp32 accumulators in TMEM.
+// Each token group writes its own (reference max, sum, unnormalised output) per segment (a
+// run of tiles of one request and KV head); combine (decode.cu) merges them with the BF16
+// sink / window part.
 //
-// Every wait on an mbarrier is bounded (about two seconds of clock cycles); on timeout the
-// kernel records an error word, stops issuing work, drains its own copies and MMAs, frees
-// its tensor memory and returns.
+// Every mbarrier wait is bounded (about two seconds of clock cycles); on timeout the kernel
+// records an error word, stops waiting, drains its own copies and MMAs, frees its tensor
+// memory and returns.  Warp-uniform roles never leave their loops early, so named barriers
+// and .sync.aligned instructions always see every thread.
 #include <cuda_fp16.h>
 
 #include "internal.h"
@@ -38,60 +41,88 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kWarps = 10;
-constexpr int kThreads = kWarps * 32;
+constexpr int kThreads = 512;
 constexpr int kStages = 10;
+constexpr int kNV = 3;                                   // value A-buffer ring depth
 constexpr int kStageBytes = 2 * kPageHeadBytes;
 constexpr float kTau = 8.0f;
 constexpr float kQScale = 1.4426950408889634f * 0.08838834764831845f;   // log2(e) / sqrt(128)
 constexpr long long kWaitCycles = 4000000000ll;
 
-constexpr uint32_t kColAK = 0, kColAV = 128, kColS = 256, kColO = 384, kTmemCols = 512;
-constexpr uint32_t kQLbo = 128, kQSbo = 2048;          // Q operand core-matrix strides (K, N)
-constexpr uint32_t kPLbo = 144, kPSbo = 16 * 144;      // P' operand: padded K stride
+// TMEM columns
+constexpr uint32_t kColAK = 0;      // 2 x 64  (token group w)
+constexpr uint32_t kColAV = 128;    // 3 x 64
+constexpr uint32_t kColS = 320;     // 2 x 32  (group 0: 16 columns, group 1: 16 columns)
+constexpr uint32_t kColO = 384;     // 2 x 32
+constexpr uint32_t kTmemCols = 512;
 
+// shared memory
+constexpr uint32_t kQLbo = 128, kQSbo = 2048;    // Q: K-major, 16 rows x 128 k per half
+constexpr uint32_t kQHalf = 4096;                 // hi half, then lo half
+constexpr uint32_t kQBuf = 2 * kQHalf;            // one buffer per segment parity
+constexpr uint32_t kPLbo = 128, kPSbo = 2048;     // P': MN-major (N contiguous), K-group stride 128
+constexpr uint32_t kPBuf = 4 * kPSbo;             // up to 32 rows
 constexpr int kOffQ = kStages * kStageBytes;
-constexpr int kQBytes = 4 * kQSbo;
-constexpr int kOffP = kOffQ + kQBytes;
-constexpr int kPBytes = 4 * kPSbo;
-constexpr int kOffMisc = kOffP + 2 * kPBytes;
+constexpr int kOffP = kOffQ + 2 * kQBuf;
+constexpr int kOffMisc = kOffP + 2 * kPBuf;
 
 struct Misc {
     uint64_t full[kStages], empty[kStages];
-    uint64_t akf[2], ake[2], avf[2], ave[2], sf[2], se[2], pf[2], pe[2];
-    uint64_t qf, qe, of, oe, drain;
+    uint64_t akf[2], sf[2], pf[2], pe[2], of[2], oe[2];
+    uint64_t avf[kNV], ave[kNV];
+    uint64_t qf[2], qe[2];
+    uint64_t drain_q, drain_p;
     uint32_t tmem;
     int abort_flag;
-    float redm[4][kMaxG];
-    float red5[4][kMaxG * 5];
-    float qred[4][kMaxG];
+    float qsum[2][kMaxG][2];
+    float redm[2][4][kMaxG];
+    float red5[2][4][kMaxG * 5];
+    float qred[2][4][kMaxG];
 };
 constexpr int kSmemBytes = kOffMisc + (int)sizeof(Misc);
 
-struct Tile {
-    int b, h, j, tiles;
+// Walks the CTA's tiles in order: request b, KV head h, tile j of (b, h), and the local
+// indices of the first and last tile of the current segment.
+struct TileIt {
+    int i, b, h, j, tiles, seg, sfirst, slast, n;
+
+    __device__ __forceinline__ void init(const DecodeParams& p, int T0, int n_) {
+        n = n_;
+        i = 0;
+        int lo = 0, hi = p.batch;
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (p.tile_off[mid] <= T0) lo = mid;
+            else hi = mid;
+        }
+        b = lo;
+        tiles = int2_tiles(p.len[b]);
+        const int rem = T0 - p.tile_off[b];
+        h = rem / tiles;
+        j = rem - h * tiles;
+        seg = 0;
+        sfirst = 0;
+        slast = min(n - 1, tiles - 1 - j);
+    }
+    __device__ __forceinline__ void next(const DecodeParams& p) {
+        ++i;
+        if (++j == tiles) {
+            j = 0;
+            if (++h == p.hkv) {
+                h = 0;
+                do {
+                    ++b;
+                } while (b < p.batch - 1 && int2_tiles(p.len[b]) == 0);
+                tiles = int2_tiles(p.len[b < p.batch ? b : p.batch - 1]);
+            }
+            ++seg;
+            sfirst = i;
+            slast = min(n - 1, i + tiles - 1);
+        }
+    }
 };
 
-__device__ __forceinline__ Tile tile_at(const DecodeParams& p, int T) {
-    int lo = 0, hi = p.batch;
-    while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (p.tile_off[mid] <= T) lo = mid;
-        else hi = mid;
-    }
-    Tile t;
-    t.b = lo;
-    t.tiles = int2_tiles(p.len[lo]);
-    const int rem = T - p.tile_off[lo];
-    t.h = rem / t.tiles;
-    t.j = rem - t.h * t.tiles;
-    return t;
-}
-
-// Bounded wait: false (and the CTA abort flag set, the error word written) on timeout.  Once the
-// CTA has aborted, waits return false at once unless `drain` is set (the tail waits for copies and
-// MMAs in flight, which must land before the CTA may exit; those stay bounded by the timeout).
-__device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, Misc* m, int* err, bool drain = false) {
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, Misc* m, int* err, bool drain = false) {
     if (mbar_try(bar, parity)) return true;
     const long long t0 = clock64();
     while (true) {
@@ -105,7 +136,7 @@ __device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, Misc* m, in
     }
 }
 
-// fp16x2 (1 + code_a / 4, 1 + code_b / 4) of the two codes at bits 2r and 2r + 16 of w.
+// fp16x2 (1 + code_a / 4, 1 + code_b / 4) of the two codes at bits 2R and 2R + 16 of w.
 template <int R>
 __device__ __forceinline__ uint32_t half_pair(uint32_t w) {
     uint32_t x;
@@ -115,8 +146,8 @@ __device__ __forceinline__ uint32_t half_pair(uint32_t w) {
     return (x & 0x03000300u) | 0x3C003C00u;
 }
 
-template <int I>
-__device__ __forceinline__ void unpack_word(uint32_t w, uint32_t (&v)[64]) {
+template <int I, int N>
+__device__ __forceinline__ void unpack_word(uint32_t w, uint32_t (&v)[N]) {
     v[8 * I + 0] = half_pair<0>(w);
     v[8 * I + 1] = half_pair<1>(w);
     v[8 * I + 2] = half_pair<2>(w);
@@ -127,19 +158,25 @@ __device__ __forceinline__ void unpack_word(uint32_t w, uint32_t (&v)[64]) {
     v[8 * I + 7] = half_pair<7>(w);
 }
 
-__device__ __forceinline__ void unpack128(uint4 a, uint4 b, uint32_t (&v)[64]) {
+// 64 codes (16 bytes) -> 32 fp16x2 words
+__device__ __forceinline__ void unpack64(uint4 a, uint32_t (&v)[32]) {
     unpack_word<0>(a.x, v);
     unpack_word<1>(a.y, v);
     unpack_word<2>(a.z, v);
     unpack_word<3>(a.w, v);
-    unpack_word<4>(b.x, v);
-    unpack_word<5>(b.y, v);
-    unpack_word<6>(b.z, v);
-    unpack_word<7>(b.w, v);
 }
 
-// Position in the MMA's K order of element u of a 16-element block: the unpack pairs
-// elements (r, r + 8) of each 16-code word into TMEM column r, i.e. K positions 2r, 2r + 1.
+// 128 codes -> two 32-column TMEM stores (keeps only 32 words live at a time)
+__device__ __forceinline__ void unpack_store128(uint4 a, uint4 b, uint32_t taddr) {
+    uint32_t v[32];
+    unpack64(a, v);
+    tmem_st32(taddr, v);
+    unpack64(b, v);
+    tmem_st32(taddr + 32, v);
+}
+
+// K position of element x of the unpacked order: codes (r, r + 8) of each 16-code word share
+// TMEM column r, i.e. K positions 2r and 2r + 1 of that 16-element block.
 __device__ __forceinline__ int kpos(int x) { return (x & ~15) + 2 * (x & 7) + ((x >> 3) & 1); }
 
 __device__ __forceinline__ float warp_sum(float x) {
@@ -153,23 +190,22 @@ __device__ __forceinline__ float warp_max(float x) {
     return x;
 }
 
-template <int NP>
-__device__ __forceinline__ void ld_cols(uint32_t taddr, uint32_t (&v)[NP]) {
-    if constexpr (NP == 16) tmem_ld16(taddr, v);
-    else if constexpr (NP == 32) tmem_ld32(taddr, v);
-    else tmem_ld64(taddr, v);
+template <int NPV>
+__device__ __forceinline__ void ld_o(uint32_t taddr, uint32_t (&v)[NPV]) {
+    if constexpr (NPV == 16) tmem_ld16(taddr, v);
+    else tmem_ld32(taddr, v);
 }
-template <int NP>
-__device__ __forceinline__ void st_cols(uint32_t taddr, const uint32_t (&v)[NP]) {
-    if constexpr (NP == 16) tmem_st16(taddr, v);
-    else if constexpr (NP == 32) tmem_st32(taddr, v);
-    else tmem_st64(taddr, v);
+template <int NPV>
+__device__ __forceinline__ void st_o(uint32_t taddr, const uint32_t (&v)[NPV]) {
+    if constexpr (NPV == 16) tmem_st16(taddr, v);
+    else tmem_st32(taddr, v);
 }
 
 template <int G>
 __global__ void __launch_bounds__(kThreads, 1) decode_tc(const __grid_constant__ DecodeParams p) {
-    constexpr int NP = ((2 * G + 15) / 16) * 16;   // MMA N (both products)
-    constexpr uint32_t kIdesc = idesc_f16(128, NP);
+    constexpr int NPV = ((2 * G + 15) / 16) * 16;                  // N of the PV product
+    constexpr uint32_t kIdescQK = idesc_f16(128, 16);
+    constexpr uint32_t kIdescPV = idesc_f16(128, NPV) | (1u << 16);   // B (P') is MN-major
     extern __shared__ __align__(1024) uint8_t smem[];
     Misc* m = reinterpret_cast<Misc*>(smem + kOffMisc);
     const int tid = threadIdx.x;
@@ -179,7 +215,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc(const __grid_constant__
     const int T1 = (int)(((long long)(blockIdx.x + 1) * p.total_tiles) / p.n_cta);
     const int n = T1 - T0;
 
-    // ---- set-up: barriers, TMEM, zeroed operand buffers
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(smem_u32(&m->full[s]), 1);
@@ -187,238 +222,249 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc(const __grid_constant__
         }
         for (int x = 0; x < 2; ++x) {
             mbar_init(smem_u32(&m->akf[x]), 128);
-            mbar_init(smem_u32(&m->ake[x]), 1);
-            mbar_init(smem_u32(&m->avf[x]), 128);
-            mbar_init(smem_u32(&m->ave[x]), 1);
             mbar_init(smem_u32(&m->sf[x]), 1);
-            mbar_init(smem_u32(&m->se[x]), 128);
             mbar_init(smem_u32(&m->pf[x]), 128);
             mbar_init(smem_u32(&m->pe[x]), 1);
+            mbar_init(smem_u32(&m->of[x]), 1);
+            mbar_init(smem_u32(&m->oe[x]), 128);
+            mbar_init(smem_u32(&m->qf[x]), 128);
+            mbar_init(smem_u32(&m->qe[x]), 1);
         }
-        mbar_init(smem_u32(&m->qf), 128);
-        mbar_init(smem_u32(&m->qe), 1);
-        mbar_init(smem_u32(&m->of), 1);
-        mbar_init(smem_u32(&m->oe), 128);
-        mbar_init(smem_u32(&m->drain), 1);
+        for (int x = 0; x < kNV; ++x) {
+            mbar_init(smem_u32(&m->avf[x]), 128);
+            mbar_init(smem_u32(&m->ave[x]), 1);
+        }
+        mbar_init(smem_u32(&m->drain_q), 1);
+        mbar_init(smem_u32(&m->drain_p), 1);
         m->abort_flag = 0;
         fence_mbar_init();
     }
-    for (int i = tid; i < (kQBytes + 2 * kPBytes) / 16; i += kThreads)
+    for (int i = tid; i < (2 * kQBuf + 2 * kPBuf) / 16; i += kThreads)
         reinterpret_cast<uint4*>(smem + kOffQ)[i] = make_uint4(0, 0, 0, 0);
-    if (warp == 9) tmem_alloc(smem_u32(&m->tmem), kTmemCols);
+    if (warp == 13) tmem_alloc(smem_u32(&m->tmem), kTmemCols);
     fence_proxy_async();
     tc_before();
     __syncthreads();
     tc_after();
     const uint32_t tm = m->tmem;
 
-    if (warp == 8) {
-        // ================================================================ producer
-        constexpr int kBatch = 16;
-        auto fetch = [&](int bi) -> int32_t {
-            const int i = bi * kBatch + (lane >> 1);
-            if (i >= n) return 0;
-            const Tile t = tile_at(p, T0 + i);
-            const int pg = 2 * t.j + (lane & 1);
-            if (pg >= int2_pages(p.len[t.b])) return 0;
-            return p.page_table[(size_t)t.b * p.max_pps + pg];
-        };
-        const int nb = (n + kBatch - 1) / kBatch;
-        int32_t cur = nb > 0 ? fetch(0) : 0;
-        bool ok = true;
-        int issued = 0;
-        for (int bi = 0; bi < nb && ok; ++bi) {
-            const int32_t nxt = (bi + 1 < nb) ? fetch(bi + 1) : 0;
-            for (int k = 0; k < kBatch; ++k) {
-                const int i = bi * kBatch + k;
-                if (i >= n) break;
-                const int32_t ph0 = __shfl_sync(0xffffffffu, cur, 2 * k);
-                const int32_t ph1 = __shfl_sync(0xffffffffu, cur, 2 * k + 1);
-                if (lane == 0) {
-                    const int s = i % kStages;
-                    const int use = i / kStages;
-                    if (use > 0 && !wait_bar(smem_u32(&m->empty[s]), (use - 1) & 1, m, p.err)) ok = false;
-                    if (ok) {
-                        const Tile t = tile_at(p, T0 + i);
-                        const bool two = 2 * t.j + 1 < int2_pages(p.len[t.b]);
-                        const uint32_t bar = smem_u32(&m->full[s]);
-                        const uint32_t dst = smem_u32(smem + s * kStageBytes);
-                        mbar_expect_tx(bar, two ? 2 * kPageHeadBytes : kPageHeadBytes);
-                        bulk_g2s(dst, p.pool + ((size_t)ph0 * p.hkv + t.h) * kPageHeadBytes, kPageHeadBytes, bar);
-                        if (two)
-                            bulk_g2s(dst + kPageHeadBytes, p.pool + ((size_t)ph1 * p.hkv + t.h) * kPageHeadBytes,
-                                     kPageHeadBytes, bar);
-                        issued = i + 1;
+    if (warp >= 12) {
+        regs_dec<56>();
+        if (warp == 12) {
+            // ============================================================ producer
+            constexpr int kBatch = 16;
+            TileIt it;      // tile described by lane (2k, 2k + 1) of the batch being fetched
+            it.init(p, T0, n);
+            TileIt is = it; // tile being issued
+            auto fetch = [&](TileIt& f, int count) -> int32_t {
+                // lanes 2k and 2k + 1 fetch the two page ids of the k-th tile of the batch
+                int32_t v = 0;
+                for (int k = 0; k < count; ++k) {
+                    if (lane >> 1 == k) {
+                        const int pg = 2 * f.j + (lane & 1);
+                        if (pg < int2_pages(p.len[f.b])) v = p.page_table[(size_t)f.b * p.max_pps + pg];
                     }
+                    f.next(p);
                 }
-                ok = __shfl_sync(0xffffffffu, ok, 0);
-                if (!ok) break;
-            }
-            cur = nxt;
-        }
-        // every issued copy must have landed before the CTA may exit
-        if (lane == 0) {
-            for (int i = max(0, issued - kStages); i < issued; ++i)
-                wait_bar(smem_u32(&m->full[i % kStages]), (i / kStages) & 1, m, p.err, true);
-        }
-    } else if (warp == 9) {
-        // ================================================================ MMA issuer
-        if (lane == 0) {
-            const uint32_t qaddr = smem_u32(smem + kOffQ);
-            int seg = 0;        // segment of the QK tile
-            int pseg = 0;       // segment of the PV tile
+                return v;
+            };
+            int32_t cur = fetch(it, min(kBatch, n));
             bool ok = true;
-            for (int i = 0; i <= n && ok; ++i) {
-                if (i < n) {
-                    const Tile t = tile_at(p, T0 + i);
-                    if (i > 0 && t.j == 0) ++seg;
-                    const int a = i & 1, use = i >> 1;
-                    if (t.j == 0 || i == 0) ok = ok && wait_bar(smem_u32(&m->qf), seg & 1, m, p.err);
-                    ok = ok && wait_bar(smem_u32(&m->akf[a]), use & 1, m, p.err);
-                    if (use > 0) ok = ok && wait_bar(smem_u32(&m->se[a]), (use - 1) & 1, m, p.err);
+            int issued = 0;
+            for (int base = 0; base < n && ok; base += kBatch) {
+                const int cnt = min(kBatch, n - base);
+                const int nxt_cnt = min(kBatch, n - base - cnt);
+                const int32_t nxt = nxt_cnt > 0 ? fetch(it, nxt_cnt) : 0;
+                for (int k = 0; k < cnt; ++k) {
+                    const int i = base + k;
+                    const int32_t ph0 = __shfl_sync(0xffffffffu, cur, 2 * k);
+                    const int32_t ph1 = __shfl_sync(0xffffffffu, cur, 2 * k + 1);
+                    if (lane == 0) {
+                        const int s = i % kStages;
+                        const int use = i / kStages;
+                        if (use > 0 && !wait_bar(smem_u32(&m->empty[s]), (use - 1) & 1, m, p.err)) ok = false;
+                        if (ok) {
+                            const bool two = 2 * is.j + 1 < int2_pages(p.len[is.b]);
+                            const uint32_t bar = smem_u32(&m->full[s]);
+                            const uint32_t dst = smem_u32(smem + s * kStageBytes);
+                            mbar_expect_tx(bar, two ? 2 * kPageHeadBytes : kPageHeadBytes);
+                            bulk_g2s(dst, p.pool + ((size_t)ph0 * p.hkv + is.h) * kPageHeadBytes, kPageHeadBytes, bar);
+                            if (two)
+                                bulk_g2s(dst + kPageHeadBytes, p.pool + ((size_t)ph1 * p.hkv + is.h) * kPageHeadBytes,
+                                         kPageHeadBytes, bar);
+                            issued = i + 1;
+                        }
+                    }
+                    is.next(p);
+                    ok = __shfl_sync(0xffffffffu, ok, 0);
                     if (!ok) break;
-                    tc_after();
-                    const uint32_t d0 = tm + kColS + 64 * a;
-#pragma unroll
-                    for (int ks = 0; ks < 8; ++ks)
-                        umma_ts(d0 + (ks < 4 ? 0 : NP), tm + kColAK + 64 * a + 8 * ks,
-                                sdesc(qaddr + ks * 2 * kQLbo, kQLbo, kQSbo), kIdesc, (ks & 3) != 0);
-                    umma_commit(smem_u32(&m->sf[a]));
-                    umma_commit(smem_u32(&m->ake[a]));
-                    if (t.j == t.tiles - 1 || i == n - 1) umma_commit(smem_u32(&m->qe));
                 }
-                if (i >= 1) {
-                    const int i2 = i - 1;
-                    const Tile t = tile_at(p, T0 + i2);
-                    const bool first = (t.j == 0) || i2 == 0;
-                    if (i2 > 0 && t.j == 0) ++pseg;
-                    const int a = i2 & 1, use = i2 >> 1;
-                    ok = ok && wait_bar(smem_u32(&m->avf[a]), use & 1, m, p.err);
-                    ok = ok && wait_bar(smem_u32(&m->pf[a]), use & 1, m, p.err);
-                    if (first && pseg > 0) ok = ok && wait_bar(smem_u32(&m->oe), (pseg - 1) & 1, m, p.err);
-                    if (!ok) break;
-                    tc_after();
-                    const uint32_t paddr = smem_u32(smem + kOffP + a * kPBytes);
-#pragma unroll
-                    for (int ks = 0; ks < 8; ++ks)
-                        umma_ts(tm + kColO, tm + kColAV + 64 * a + 8 * ks,
-                                sdesc(paddr + ks * 2 * kPLbo, kPLbo, kPSbo), kIdesc, !(first && ks == 0));
-                    umma_commit(smem_u32(&m->ave[a]));
-                    umma_commit(smem_u32(&m->pe[a]));
-                    if (t.j == t.tiles - 1 || i2 == n - 1) umma_commit(smem_u32(&m->of));
-                }
-            }
-            // all issued MMAs must finish before the tensor memory is released
-            umma_commit(smem_u32(&m->drain));
-            wait_bar(smem_u32(&m->drain), 0, m, p.err, true);
-        }
-        __syncwarp();
-    } else if (warp < 4) {
-        // ================================================================ dequant (thread = TMEM lane)
-        const int r = tid;
-        const uint32_t lanebase = (uint32_t)(32 * warp) << 16;
-        for (int i = 0; i < n; ++i) {
-            const int s = i % kStages;
-            wait_bar(smem_u32(&m->full[s]), (i / kStages) & 1, m, p.err);
-            const uint8_t* st = smem + s * kStageBytes;
-            const int a = i & 1, use = i >> 1;
-            uint32_t v[64];
-            {   // keys: token r, 32 bytes of codes
-                const uint4* src = reinterpret_cast<const uint4*>(st + (r >> 6) * kPageHeadBytes + kKCodes + (r & 63) * 32);
-                const uint4 x0 = src[0], x1 = src[1];
-                unpack128(x0, x1, v);
-            }
-            if (use > 0) wait_bar(smem_u32(&m->ake[a]), (use - 1) & 1, m, p.err);
-            tc_after();
-            tmem_st64(tm + lanebase + kColAK + 64 * a, v);
-            tmem_wait_st();
-            tc_before();
-            mbar_arrive(smem_u32(&m->akf[a]));
-            {   // values: channel r, 16 bytes (64 tokens) from each page
-                const uint4 x0 = *reinterpret_cast<const uint4*>(st + kVCodes + r * 16);
-                const uint4 x1 = *reinterpret_cast<const uint4*>(st + kPageHeadBytes + kVCodes + r * 16);
-                unpack128(x0, x1, v);
-            }
-            if (use > 0) wait_bar(smem_u32(&m->ave[a]), (use - 1) & 1, m, p.err);
-            tc_after();
-            tmem_st64(tm + lanebase + kColAV + 64 * a, v);
-            tmem_wait_st();
-            tc_before();
-            mbar_arrive(smem_u32(&m->avf[a]));
-            mbar_arrive(smem_u32(&m->empty[s]));
-        }
-    } else {
-        // ================================================================ softmax (thread = token / channel lane)
-        const int w4 = warp - 4;
-        const int r = tid - 128;
-        const uint32_t lanebase = (uint32_t)(32 * w4) << 16;
-        const int kq = kpos(r);
-        float mref[G], l[G], sp[G][2], mv[G][2], qs[G][2];
-        auto reset = [&]() {
-#pragma unroll
-            for (int hh = 0; hh < G; ++hh) {
-                mref[hh] = -INFINITY;
-                l[hh] = 0.f;
-                sp[hh][0] = sp[hh][1] = mv[hh][0] = mv[hh][1] = 0.f;
-            }
-        };
-        // Q operand of the segment that starts at local tile i (channel r of every head)
-        auto write_q = [&](const Tile& t) {
-            const float* qr = p.qrot + ((size_t)t.b * p.hkv * G + (size_t)t.h * G) * kD;
-            uint8_t* Q = smem + kOffQ;
-            const int kc = kq >> 3, kin = kq & 7;
-            float part[G];
-#pragma unroll
-            for (int hh = 0; hh < G; ++hh) {
-                const float q = qr[hh * kD + r] * kQScale;
-                const __half hi = __float2half_rn(q);
-                const __half lo = __float2half_rn(q - __half2float(hi));
-                const int n0 = 2 * hh, n1 = 2 * hh + 1;
-                *reinterpret_cast<__half*>(Q + (n0 >> 3) * kQSbo + kc * kQLbo + (n0 & 7) * 16 + kin * 2) = hi;
-                *reinterpret_cast<__half*>(Q + (n1 >> 3) * kQSbo + kc * kQLbo + (n1 & 7) * 16 + kin * 2) = lo;
-                part[hh] = warp_sum(__half2float(hi) + __half2float(lo));
+                cur = nxt;
             }
             if (lane == 0)
+                for (int i = max(0, issued - kStages); i < issued; ++i)
+                    wait_bar(smem_u32(&m->full[i % kStages]), (i / kStages) & 1, m, p.err, true);
+        } else if (warp == 13) {
+            // ============================================================ QK issuer
+            if (lane == 0) {
+                TileIt it;
+                it.init(p, T0, n);
+                const uint32_t qbase = smem_u32(smem + kOffQ);
+                for (int i = 0; i < n; ++i) {
+                    const int w = i & 1;
+                    if (i == it.sfirst && !wait_bar(smem_u32(&m->qf[it.seg & 1]), (it.seg >> 1) & 1, m, p.err)) break;
+                    if (!wait_bar(smem_u32(&m->akf[w]), (i >> 1) & 1, m, p.err)) break;
+                    tc_after();
+                    const uint32_t qa = qbase + (it.seg & 1) * kQBuf;
 #pragma unroll
-                for (int hh = 0; hh < G; ++hh) m->qred[w4][hh] = part[hh];
-            bar_sync(2, 128);
-#pragma unroll
-            for (int hh = 0; hh < G; ++hh) {
-                qs[hh][0] = m->qred[0][hh] + m->qred[1][hh];
-                qs[hh][1] = m->qred[2][hh] + m->qred[3][hh];
+                    for (int ks = 0; ks < 8; ++ks) {
+                        const uint32_t d = tm + kColS + 32 * w + 16 * (ks >> 2);
+                        const uint32_t a = tm + kColAK + 64 * w + 8 * ks;
+                        umma_ts(d, a, sdesc(qa + ks * 2 * kQLbo, kQLbo, kQSbo), kIdescQK, (ks & 3) != 0);
+                        umma_ts(d, a, sdesc(qa + kQHalf + ks * 2 * kQLbo, kQLbo, kQSbo), kIdescQK, 1);
+                    }
+                    umma_commit(smem_u32(&m->sf[w]));
+                    if (i == it.slast) umma_commit(smem_u32(&m->qe[it.seg & 1]));
+                    it.next(p);
+                }
+                umma_commit(smem_u32(&m->drain_q));
+                wait_bar(smem_u32(&m->drain_q), 0, m, p.err, true);
             }
-            bar_sync(2, 128);
-            fence_proxy_async();
-            mbar_arrive(smem_u32(&m->qf));
-        };
-        reset();
-        if (n > 0) write_q(tile_at(p, T0));
-        int seg = 0;
-        // Warp-uniform roles never leave the loop early: after an abort every wait returns at
-        // once and all 128 threads still meet at the same named barriers.
+            __syncwarp();
+        } else if (warp == 14) {
+            // ============================================================ PV issuer
+            if (lane == 0) {
+                TileIt it;
+                it.init(p, T0, n);
+                int started[2] = {0, 0};
+                const uint32_t pbase = smem_u32(smem + kOffP);
+                for (int i = 0; i < n; ++i) {
+                    const int w = i & 1, x = i % kNV;
+                    const bool first = i - it.sfirst <= 1;
+                    const bool last = it.slast - i <= 1;
+                    if (!wait_bar(smem_u32(&m->avf[x]), (i / kNV) & 1, m, p.err)) break;
+                    if (!wait_bar(smem_u32(&m->pf[w]), (i >> 1) & 1, m, p.err)) break;
+                    if (first && started[w] > 0 &&
+                        !wait_bar(smem_u32(&m->oe[w]), (started[w] - 1) & 1, m, p.err))
+                        break;
+                    if (first) ++started[w];
+                    tc_after();
+                    const uint32_t pa = pbase + w * kPBuf;
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks)
+                        umma_ts(tm + kColO + 32 * w, tm + kColAV + 64 * x + 8 * ks,
+                                sdesc(pa + ks * 2 * kPLbo, kPLbo, kPSbo), kIdescPV, !(first && ks == 0));
+                    umma_commit(smem_u32(&m->ave[x]));
+                    umma_commit(smem_u32(&m->pe[w]));
+                    if (last) umma_commit(smem_u32(&m->of[w]));
+                    it.next(p);
+                }
+                umma_commit(smem_u32(&m->drain_p));
+                wait_bar(smem_u32(&m->drain_p), 0, m, p.err, true);
+            }
+            __syncwarp();
+        }
+        regs_inc<128>();
+    } else if (warp >= 8) {
+        // ================================================================ value group
+        regs_dec<88>();
+        const int r = tid - 256;
+        const uint32_t lanebase = (uint32_t)(32 * (warp - 8)) << 16;
         for (int i = 0; i < n; ++i) {
-            const Tile t = tile_at(p, T0 + i);
-            const bool first = (t.j == 0) || i == 0;
-            const int s = i % kStages;
-            const int a = i & 1, use = i >> 1;
-            // ---- scores of this tile (TMEM -> registers)
-            wait_bar(smem_u32(&m->sf[a]), use & 1, m, p.err);
+            const int s = i % kStages, x = i % kNV, use = i / kNV;
+            wait_bar(smem_u32(&m->full[s]), (i / kStages) & 1, m, p.err);
+            const uint8_t* st = smem + s * kStageBytes;
+            const uint4 x0 = *reinterpret_cast<const uint4*>(st + kVCodes + r * 16);
+            const uint4 x1 = *reinterpret_cast<const uint4*>(st + kPageHeadBytes + kVCodes + r * 16);
+            mbar_arrive(smem_u32(&m->empty[s]));
+            if (use > 0) wait_bar(smem_u32(&m->ave[x]), (use - 1) & 1, m, p.err);
             tc_after();
-            uint32_t sv[2 * NP];
-            if constexpr (NP == 16) {
-                tmem_ld32(tm + lanebase + kColS + 64 * a, sv);
-            } else {
-                tmem_ld64(tm + lanebase + kColS + 64 * a, sv);
-            }
-            tmem_wait_ld();
+            unpack_store128(x0, x1, tm + lanebase + kColAV + 64 * x);
+            tmem_wait_st();
             tc_before();
-            mbar_arrive(smem_u32(&m->se[a]));
+            mbar_arrive(smem_u32(&m->avf[x]));
+        }
+        regs_inc<128>();
+    } else {
+        // ================================================================ token groups
+        regs_inc<184>();
+        const int w = warp >> 2;             // token group
+        const int wk = warp & 3;             // warp within the group
+        const int r = tid - 128 * w;         // token of the tile = TMEM lane
+        const uint32_t lanebase = (uint32_t)(32 * wk) << 16;
+        const int bar_vote = 1 + 2 * w, bar_sync_id = 2 + 2 * w;
+        const int kq = kpos(r);
+        const uint32_t pdst = smem_u32(smem + kOffP + w * kPBuf) + (kq >> 3) * kPLbo + (kq & 7) * 16;
+        constexpr bool kQsRegs = G <= 12;       // G = 16 reads the per-group q sums from shared memory
+        float mref[G], l[G], sp[G][2], mv[G][2], qs[kQsRegs ? G : 1][2];
+        int flushes = 0;
+        TileIt it;
+        it.init(p, T0, n);
+        if (w == 1 && n > 1) it.next(p);
+        for (int i = w; i < n; i += 2) {
+            const int s = i % kStages;
+            const int k = i >> 1;                           // this group's tile count so far
+            const bool first = i - it.sfirst <= 1;
+            const bool last = it.slast - i <= 1;
+            const int qpar = it.seg & 1;
+            if (i == it.sfirst) {
+                // ---- this group opens the segment: Q operand (hi / lo fp16) and per-group sums
+                if (it.seg >= 2) wait_bar(smem_u32(&m->qe[qpar]), ((it.seg - 2) >> 1) & 1, m, p.err);
+                const float* qr = p.qrot + ((size_t)it.b * p.hkv * G + (size_t)it.h * G) * kD;
+                uint8_t* Q = smem + kOffQ + qpar * kQBuf;
+                const int kc = kq >> 3, kin = kq & 7;
+                float part[G];
+#pragma unroll
+                for (int hh = 0; hh < G; ++hh) {
+                    const float q = qr[hh * kD + r] * kQScale;
+                    const __half hi = __float2half_rn(q);
+                    const __half lo = __float2half_rn(q - __half2float(hi));
+                    const int off = (hh >> 3) * kQSbo + kc * kQLbo + (hh & 7) * 16 + kin * 2;
+                    *reinterpret_cast<__half*>(Q + off) = hi;
+                    *reinterpret_cast<__half*>(Q + kQHalf + off) = lo;
+                    part[hh] = warp_sum(__half2float(hi) + __half2float(lo));
+                }
+                if (lane == 0)
+#pragma unroll
+                    for (int hh = 0; hh < G; ++hh) m->qred[w][wk][hh] = part[hh];
+                bar_sync(bar_sync_id, 128);
+                if (r < G) {
+                    m->qsum[qpar][r][0] = m->qred[w][0][r] + m->qred[w][1][r];
+                    m->qsum[qpar][r][1] = m->qred[w][2][r] + m->qred[w][3][r];
+                }
+                fence_proxy_async();
+                mbar_arrive(smem_u32(&m->qf[qpar]));
+            }
+            if (first) {
+                if (i != it.sfirst) wait_bar(smem_u32(&m->qf[qpar]), (it.seg >> 1) & 1, m, p.err);
+                else bar_sync(bar_sync_id, 128);
+#pragma unroll
+                for (int hh = 0; hh < G; ++hh) {
+                    if constexpr (kQsRegs) {
+                        qs[hh][0] = m->qsum[qpar][hh][0];
+                        qs[hh][1] = m->qsum[qpar][hh][1];
+                    }
+                    mref[hh] = -INFINITY;
+                    l[hh] = 0.f;
+                    sp[hh][0] = sp[hh][1] = mv[hh][0] = mv[hh][1] = 0.f;
+                }
+            }
+            // ---- keys of token r -> TMEM A operand
             wait_bar(smem_u32(&m->full[s]), (i / kStages) & 1, m, p.err);
             const uint8_t* st = smem + s * kStageBytes + (r >> 6) * kPageHeadBytes;
+            {
+                const uint4* src = reinterpret_cast<const uint4*>(st + kKCodes + (r & 63) * 32);
+                const uint4 x0 = src[0], x1 = src[1];
+                tc_after();
+                unpack_store128(x0, x1, tm + lanebase + kColAK + 64 * w);
+                tmem_wait_st();
+                tc_before();
+                mbar_arrive(smem_u32(&m->akf[w]));
+            }
             const uint2 ksm = *reinterpret_cast<const uint2*>(st + kKSm + (r & 63) * 8);
             const uint2 vsm = *reinterpret_cast<const uint2*>(st + kVSm + (r & 63) * 8);
             mbar_arrive(smem_u32(&m->empty[s]));
-            const bool live = t.j * kTileTok + r < int2_tokens(p.len[t.b]);
+            const bool live = it.j * kTileTok + r < int2_tokens(p.len[it.b]);
             const float ks0 = __half2float(__ushort_as_half(ksm.x & 0xffff));
             const float km0 = __half2float(__ushort_as_half(ksm.x >> 16));
             const float ks1 = __half2float(__ushort_as_half(ksm.y & 0xffff));
@@ -429,47 +475,61 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc(const __grid_constant__
             const float vm1 = live ? __half2float(__ushort_as_half(vsm.y >> 16)) : 0.f;
             const float a0 = 4.f * ks0, a1 = 4.f * ks1;
             const float c0 = km0 - a0, c1 = km1 - a1;
+            // ---- scores
+            wait_bar(smem_u32(&m->sf[w]), k & 1, m, p.err);
+            tc_after();
+            uint32_t sv[32];
+            tmem_ld32(tm + lanebase + kColS + 32 * w, sv);
+            tmem_wait_ld();
             float lg[G];
             bool ex = false;
 #pragma unroll
             for (int hh = 0; hh < G; ++hh) {
-                const float t0 = __uint_as_float(sv[2 * hh]) + __uint_as_float(sv[2 * hh + 1]);
-                const float t1 = __uint_as_float(sv[NP + 2 * hh]) + __uint_as_float(sv[NP + 2 * hh + 1]);
-                float x = fmaf(a0, t0, fmaf(a1, t1, fmaf(c0, qs[hh][0], c1 * qs[hh][1])));
+                float q0, q1;
+                if constexpr (kQsRegs) {
+                    q0 = qs[hh][0];
+                    q1 = qs[hh][1];
+                } else {
+                    q0 = m->qsum[qpar][hh][0];
+                    q1 = m->qsum[qpar][hh][1];
+                }
+                float x = fmaf(a0, __uint_as_float(sv[hh]),
+                               fmaf(a1, __uint_as_float(sv[16 + hh]), fmaf(c0, q0, c1 * q1)));
                 x = live ? x : -INFINITY;
                 lg[hh] = x;
                 ex |= x > mref[hh] + kTau;
             }
             // ---- raise the reference max when a logit passes it by more than 2^8 (rare)
-            if (bar_or(1, 128, ex)) {
+            if (bar_or(bar_vote, 128, ex)) {
 #pragma unroll
                 for (int hh = 0; hh < G; ++hh) {
                     const float tmx = warp_max(lg[hh]);
-                    if (lane == 0) m->redm[w4][hh] = tmx;
+                    if (lane == 0) m->redm[w][wk][hh] = tmx;
                 }
-                bar_sync(2, 128);
+                bar_sync(bar_sync_id, 128);
                 float f[G];
                 bool changed = false;
 #pragma unroll
                 for (int hh = 0; hh < G; ++hh) {
-                    const float tmx = fmaxf(fmaxf(m->redm[0][hh], m->redm[1][hh]), fmaxf(m->redm[2][hh], m->redm[3][hh]));
+                    const float tmx = fmaxf(fmaxf(m->redm[w][0][hh], m->redm[w][1][hh]),
+                                            fmaxf(m->redm[w][2][hh], m->redm[w][3][hh]));
                     const float old = mref[hh];
                     const float nw = (tmx > old + kTau) ? tmx : old;
                     f[hh] = (old == -INFINITY) ? 0.f : exp2f(old - nw);
                     changed |= nw != old;
                     mref[hh] = nw;
                 }
-                bar_sync(2, 128);
+                bar_sync(bar_sync_id, 128);
                 if (changed && !first) {
-                    // O holds earlier tiles of this segment: rescale it once PV(i - 1) is done
-                    wait_bar(smem_u32(&m->pe[(i - 1) & 1]), ((i - 1) >> 1) & 1, m, p.err);
+                    // O holds this group's earlier tiles: rescale once its last PV is done
+                    wait_bar(smem_u32(&m->pe[w]), (k - 1) & 1, m, p.err);
                     tc_after();
-                    uint32_t o[NP];
-                    ld_cols<NP>(tm + lanebase + kColO, o);
+                    uint32_t o[NPV];
+                    ld_o<NPV>(tm + lanebase + kColO + 32 * w, o);
                     tmem_wait_ld();
 #pragma unroll
                     for (int c = 0; c < 2 * G; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * f[c >> 1]);
-                    st_cols<NP>(tm + lanebase + kColO, o);
+                    st_o<NPV>(tm + lanebase + kColO + 32 * w, o);
                     tmem_wait_st();
                     tc_before();
 #pragma unroll
@@ -482,9 +542,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc(const __grid_constant__
                     }
                 }
             }
-            // ---- probabilities, P' = p * s_V (fp16) for the PV MMA
-            if (use > 0) wait_bar(smem_u32(&m->pe[a]), (use - 1) & 1, m, p.err);
-            uint8_t* P = smem + kOffP + a * kPBytes + (kq >> 3) * kPLbo + (kq & 7) * 2;
+            // ---- probabilities, P' = p * s_V (fp16, N contiguous) for the PV product
+            uint32_t pp[NPV / 2];
+#pragma unroll
+            for (int c = 0; c < NPV / 2; ++c) pp[c] = 0u;
 #pragma unroll
             for (int hh = 0; hh < G; ++hh) {
                 const float pr = live ? exp2f(lg[hh] - mref[hh]) : 0.f;
@@ -494,26 +555,26 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc(const __grid_constant__
                 sp[hh][1] += __high2float(h2);
                 mv[hh][0] = fmaf(pr, vm0, mv[hh][0]);
                 mv[hh][1] = fmaf(pr, vm1, mv[hh][1]);
-                const int n0 = 2 * hh, n1 = 2 * hh + 1;
-                *reinterpret_cast<__half*>(P + (n0 >> 3) * kPSbo + (n0 & 7) * 16) = __low2half(h2);
-                *reinterpret_cast<__half*>(P + (n1 >> 3) * kPSbo + (n1 & 7) * 16) = __high2half(h2);
+                pp[hh] = *reinterpret_cast<const uint32_t*>(&h2);
             }
+            if (k > 0) wait_bar(smem_u32(&m->pe[w]), (k - 1) & 1, m, p.err);
+#pragma unroll
+            for (int c = 0; c < NPV / 8; ++c)
+                st_shared_v4(pdst + c * kPSbo, pp[4 * c], pp[4 * c + 1], pp[4 * c + 2], pp[4 * c + 3]);
             fence_proxy_async();
-            mbar_arrive(smem_u32(&m->pf[a]));
+            tc_before();
+            mbar_arrive(smem_u32(&m->pf[w]));
 
-            // ---- end of a (request, KV head) segment: write its partial result
-            if (t.j == t.tiles - 1 || i == n - 1) {
-                if (i + 1 < n) {
-                    wait_bar(smem_u32(&m->qe), seg & 1, m, p.err);
-                    write_q(tile_at(p, T0 + i + 1));
-                }
-                wait_bar(smem_u32(&m->of), seg & 1, m, p.err);
+            // ---- this group's last tile of the segment: write its partial result
+            if (last) {
+                wait_bar(smem_u32(&m->of[w]), flushes & 1, m, p.err);
+                ++flushes;
                 tc_after();
-                uint32_t o[NP];
-                ld_cols<NP>(tm + lanebase + kColO, o);
+                uint32_t o[NPV];
+                ld_o<NPV>(tm + lanebase + kColO + 32 * w, o);
                 tmem_wait_ld();
                 tc_before();
-                mbar_arrive(smem_u32(&m->oe));
+                mbar_arrive(smem_u32(&m->oe[w]));
 #pragma unroll
                 for (int hh = 0; hh < G; ++hh) {
                     const float v0 = warp_sum(l[hh]);
@@ -522,49 +583,55 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc(const __grid_constant__
                     const float v3 = warp_sum(mv[hh][0]);
                     const float v4 = warp_sum(mv[hh][1]);
                     if (lane == 0) {
-                        m->red5[w4][5 * hh + 0] = v0;
-                        m->red5[w4][5 * hh + 1] = v1;
-                        m->red5[w4][5 * hh + 2] = v2;
-                        m->red5[w4][5 * hh + 3] = v3;
-                        m->red5[w4][5 * hh + 4] = v4;
+                        m->red5[w][wk][5 * hh + 0] = v0;
+                        m->red5[w][wk][5 * hh + 1] = v1;
+                        m->red5[w][wk][5 * hh + 2] = v2;
+                        m->red5[w][wk][5 * hh + 3] = v3;
+                        m->red5[w][wk][5 * hh + 4] = v4;
                     }
                 }
-                bar_sync(2, 128);
+                bar_sync(bar_sync_id, 128);
                 const int gc = r >> 6;
-                float* part = p.part_tc + ((size_t)(t.b * p.hkv + t.h) + blockIdx.x) * G * (2 + kD);
+                float* part = p.part_tc + (((size_t)(it.b * p.hkv + it.h) + blockIdx.x) * 2 + w) * G * (2 + kD);
 #pragma unroll
                 for (int hh = 0; hh < G; ++hh) {
                     float tot[5];
 #pragma unroll
                     for (int q = 0; q < 5; ++q)
-                        tot[q] = m->red5[0][5 * hh + q] + m->red5[1][5 * hh + q] + m->red5[2][5 * hh + q] +
-                                 m->red5[3][5 * hh + q];
+                        tot[q] = m->red5[w][0][5 * hh + q] + m->red5[w][1][5 * hh + q] + m->red5[w][2][5 * hh + q] +
+                                 m->red5[w][3][5 * hh + q];
                     const float spg = gc ? tot[2] : tot[1];
                     const float mvg = gc ? tot[4] : tot[3];
-                    const float out = fmaf(4.f, __uint_as_float(o[2 * hh + gc]) - spg, mvg);
-                    part[hh * (2 + kD) + 2 + r] = out;
+                    part[hh * (2 + kD) + 2 + r] = fmaf(4.f, __uint_as_float(o[2 * hh + gc]) - spg, mvg);
                     if (r == 0) {
                         part[hh * (2 + kD) + 0] = mref[hh];
                         part[hh * (2 + kD) + 1] = tot[0];
                     }
                 }
-                bar_sync(2, 128);
-                reset();
-                ++seg;
+                bar_sync(bar_sync_id, 128);
             }
+            it.next(p);
+            if (i + 1 < n) it.next(p);
         }
+        regs_dec<128>();
     }
 
     // ---- tear-down: every role is past its last wait; free the tensor memory
     tc_before();
     __syncthreads();
     tc_after();
-    if (warp == 9) tmem_dealloc(tm, kTmemCols);
+    if (warp == 13) tmem_dealloc(tm, kTmemCols);
 }
 
 template <int G>
 cudaError_t launch_g(const DecodeParams& p, cudaStream_t s) {
-    cudaError_t e = cudaFuncSetAttribute(decode_tc<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    // The warpgroups' setmaxnreg targets (184 + 184 + 88 + 56) add up to 4 x 128: the launch
+    // must reserve exactly 128 registers per thread or the increase could never be granted.
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, decode_tc<G>);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs != 128) return cudaErrorInvalidConfiguration;
+    e = cudaFuncSetAttribute(decode_tc<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
     decode_tc<G><<<p.n_cta, kThreads, kSmemBytes, s>>>(p);
     return cudaGetLastError();

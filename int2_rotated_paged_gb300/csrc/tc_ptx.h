@@ -172,3 +172,21 @@ __device__ __forceinline__ bool bar_or(int id, int n, bool pred) {
 
 }  // namespace ptx
 }  // namespace oscar
+
+namespace oscar {
+namespace ptx {
+// Register-file rebalancing between warpgroups (all threads of the warpgroup execute it).
+template <int N>
+__device__ __forceinline__ void regs_inc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void regs_dec() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+                 : "memory");
+}
+}  // namespace ptx
+}  // namespace oscar
