@@ -248,6 +248,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc(const __grid_constant__
     tc_after();
     const uint32_t tm = m->tmem;
 
+    // Register split: the token groups take 184 per thread, the value group keeps 88 and the
+    // producer / MMA group 56 (184 + 184 + 88 + 56 = 4 x 128, the launch's reservation).  The
+    // only increase is the token groups' one below, so it is always granted from what the other
+    // groups release; nothing gives registers back before exit.
     if (warp >= 12) {
         regs_dec<56>();
         if (warp == 12) {
@@ -364,7 +368,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc(const __grid_constant__
             }
             __syncwarp();
         }
-        regs_inc<128>();
     } else if (warp >= 8) {
         // ================================================================ value group
         regs_dec<88>();
@@ -384,7 +387,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc(const __grid_constant__
             tc_before();
             mbar_arrive(smem_u32(&m->avf[x]));
         }
-        regs_inc<128>();
     } else {
         // ================================================================ token groups
         regs_inc<184>();
@@ -613,7 +615,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc(const __grid_constant__
             it.next(p);
             if (i + 1 < n) it.next(p);
         }
-        regs_dec<128>();
     }
 
     // ---- tear-down: every role is past its last wait; free the tensor memory
