@@ -77,11 +77,11 @@ def _run(cfg, lens, pairs=None, steps=2, chunks=None, table=None, check_bytes=Tr
             for (b, h), oc in ocs.items():
                 ref, _ = oc.attend(q[b, h * g:(h + 1) * g].cpu().numpy())
                 got = out[b, h * g:(h + 1) * g]
-                # bf16 output = fp32-mode result rounded once more to 8 mantissa bits: its error
-                # budget is the fp32-mode bar plus half a bf16 ulp (relative 2^-9) per element
+                # bf16 output = fp32-mode result rounded once more to 8 significant bits: its
+                # error budget is the fp32-mode bar plus the bf16 unit roundoff 2^-8 per element
                 r = rel_l2(got, ref)
-                assert r <= REL_L2 + 2.0 ** -9, f"(b={b}, h={h}): rel-L2 {r:.3e}"
-                assert (np.abs(got - ref) <= MAX_ABS + 2.0 ** -9 * np.abs(ref)).all()
+                assert r <= REL_L2 + 2.0 ** -8, f"(b={b}, h={h}): rel-L2 {r:.3e}"
+                assert (np.abs(got - ref) <= MAX_ABS + 2.0 ** -8 * np.abs(ref)).all()
         # one decode token per request, then the next step attends over it too
         n = [1] * cfg.batch
         k, v = synth.kv_block(cfg.seed, n, cur, cfg.num_kv_heads, device="cuda")
