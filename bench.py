@@ -49,6 +49,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-pairs", type=int, default=3, help="(request, KV head) pairs the CPU oracle times")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="requests per GPU (0 = the workload's batch); smaller values are for profiling")
     ap.add_argument("--path", default="tensor", choices=["tensor", "simt"],
                     help="decode kernel: tcgen05 tensor cores (default) or the SIMT baseline")
     return ap.parse_args()
@@ -368,6 +370,8 @@ def main():
     args = parse()
     import synth
     cfg = synth.config(args.config)
+    if args.batch:
+        cfg = synth.scaled(cfg, cfg.ctx, batch=args.batch)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     dist = None

@@ -47,7 +47,6 @@ constexpr int kNV = 3;                                   // value A-buffer ring 
 constexpr int kStageBytes = 2 * kPageHeadBytes;
 constexpr float kTau = 8.0f;
 constexpr float kQScale = 1.4426950408889634f * 0.08838834764831845f;   // log2(e) / sqrt(128)
-constexpr long long kWaitCycles = 4000000000ll;
 
 // TMEM columns
 constexpr uint32_t kColAK = 0;      // 2 x 64  (token group w)
@@ -60,7 +59,9 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kQLbo = 128, kQSbo = 2048;    // Q: K-major, 16 rows x 128 k per half
 constexpr uint32_t kQHalf = 4096;                 // hi half, then lo half
 constexpr uint32_t kQBuf = 2 * kQHalf;            // one buffer per segment parity
-constexpr uint32_t kPLbo = 128, kPSbo = 2048;     // P': MN-major (N contiguous), K-group stride 128
+// P': MN-major (N contiguous).  The K-group stride is padded from 128 to 144 bytes so that the
+// eight tokens of a quarter-warp (even or odd K rows of two groups) hit distinct banks.
+constexpr uint32_t kPLbo = 144, kPSbo = 16 * 144;
 constexpr uint32_t kPBuf = 4 * kPSbo;             // up to 32 rows
 constexpr int kOffQ = kStages * kStageBytes;
 constexpr int kOffP = kOffQ + 2 * kQBuf;
@@ -122,18 +123,21 @@ struct TileIt {
     }
 };
 
+// Bounded wait: the thread sleeps in try_wait (up to 1 ms per attempt, woken when the phase
+// completes), at most kWaitTries attempts.  False (abort flag set, error word written) on
+// timeout; once the CTA has aborted, waits return false at once unless `drain` is set (tail
+// waits for copies and MMAs in flight, which must land before the CTA may exit).
+constexpr uint32_t kSleepNs = 1000000;
+constexpr int kWaitTries = 2000;
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, Misc* m, int* err, bool drain = false) {
-    if (mbar_try(bar, parity)) return true;
-    const long long t0 = clock64();
-    while (true) {
-        if (mbar_try(bar, parity)) return true;
+    if (mbar_try_sleep(bar, parity, kSleepNs)) return true;
+    for (int t = 1; t < kWaitTries; ++t) {
         if (!drain && *(volatile int*)&m->abort_flag) return false;
-        if (clock64() - t0 > kWaitCycles) {
-            *(volatile int*)&m->abort_flag = 1;
-            atomicOr(err, 1);
-            return false;
-        }
+        if (mbar_try_sleep(bar, parity, kSleepNs)) return true;
     }
+    *(volatile int*)&m->abort_flag = 1;
+    atomicOr(err, 1);
+    return false;
 }
 
 // fp16x2 (1 + code_a / 4, 1 + code_b / 4) of the two codes at bits 2R and 2R + 16 of w.
@@ -455,8 +459,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc(const __grid_constant__
             wait_bar(smem_u32(&m->full[s]), (i / kStages) & 1, m, p.err);
             const uint8_t* st = smem + s * kStageBytes + (r >> 6) * kPageHeadBytes;
             {
-                const uint4* src = reinterpret_cast<const uint4*>(st + kKCodes + (r & 63) * 32);
-                const uint4 x0 = src[0], x1 = src[1];
+                // 32 bytes per token: lanes with (r >> 2) odd read the upper half first, so each
+                // quarter-warp's 16-byte loads cover all 32 banks
+                const uint8_t* src = st + kKCodes + (r & 63) * 32;
+                const int sw = (r >> 2) & 1;
+                const uint4 y0 = *reinterpret_cast<const uint4*>(src + 16 * sw);
+                const uint4 y1 = *reinterpret_cast<const uint4*>(src + 16 * (sw ^ 1));
+                const uint4 x0 = sw ? y1 : y0, x1 = sw ? y0 : y1;
                 tc_after();
                 unpack_store128(x0, x1, tm + lanebase + kColAK + 64 * w);
                 tmem_wait_st();
