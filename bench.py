@@ -51,8 +51,8 @@ def parse():
     ap.add_argument("--cpu-pairs", type=int, default=3, help="(request, KV head) pairs the CPU oracle times")
     ap.add_argument("--batch", type=int, default=0,
                     help="requests per GPU (0 = the workload's batch); smaller values are for profiling")
-    ap.add_argument("--path", default="tensor", choices=["tensor", "simt"],
-                    help="decode kernel: tcgen05 tensor cores (default) or the SIMT baseline")
+    ap.add_argument("--path", default="mma", choices=["mma", "tensor", "simt"],
+                    help="decode kernel: warp-level MMA (default), tcgen05, or the SIMT baseline")
     return ap.parse_args()
 
 
@@ -203,7 +203,7 @@ def run_ours(args, cfg, rank, world, dist):
     from int2_rotated_paged_gb300 import build as kbuild
 
     kbuild.build()
-    K.oscar_set_decode_path(K.PATH_TENSOR if args.path == "tensor" else K.PATH_SIMT)
+    K.oscar_set_decode_path({"mma": K.PATH_WARP_MMA, "tensor": K.PATH_TENSOR, "simt": K.PATH_SIMT}[args.path])
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
     stream = torch.cuda.current_stream()
@@ -353,7 +353,7 @@ def run_ours(args, cfg, rank, world, dist):
                    "batch_per_gpu": B, "context": lens0[0], "l2": "inputs larger than L2 (about 2.1 GB per step vs 129 MB)"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_kind": peak_kind, "kernel": f"oscar_decode_attention, {args.path} path (rotate_q + bf16 split + "
-                               f"{'decode_tc' if args.path == 'tensor' else 'split_simt'} + combine)",
+                               f"{dict(mma='decode_mma', tensor='decode_tc', simt='split_simt')[args.path]} + combine)",
                      "traffic": profiled_traffic("decode.cu"), "bytes_per_call": dec_bytes,
                      "ms_per_call": dec_t * 1e3},
         "append": {"prefill_tokens_per_s": tok_append / t_append, "prefill_tokens": tok_append,

@@ -188,6 +188,7 @@ int oscar_decode_attention(oscar_cache *c, const void *q, int32_t q_dtype, const
  *                    against).  Both give the same result within the parity tolerance. */
 #define OSCAR_PATH_TENSOR 0
 #define OSCAR_PATH_SIMT 1
+#define OSCAR_PATH_WARP_MMA 2
 int oscar_set_decode_path(int32_t path);
 /* Synchronise `stream` and report whether the last decode call that used `workspace`
  * completed normally (OSCAR_OK) or one of its bounded in-kernel waits gave up

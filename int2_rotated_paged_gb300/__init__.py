@@ -40,6 +40,7 @@ EXPORTS = [
 OSCAR_ETIMEOUT = -7
 PATH_TENSOR = 0
 PATH_SIMT = 1
+PATH_WARP_MMA = 2
 
 
 class OscarError(RuntimeError):

@@ -359,7 +359,7 @@ size_t oscar_decode_workspace_bytes(const oscar_cache* c) {
 }
 
 int oscar_set_decode_path(int32_t path) {
-    if (path != OSCAR_PATH_TENSOR && path != OSCAR_PATH_SIMT) return OSCAR_EINVAL;
+    if (path != OSCAR_PATH_TENSOR && path != OSCAR_PATH_SIMT && path != OSCAR_PATH_WARP_MMA) return OSCAR_EINVAL;
     g_decode_path = path;
     return OSCAR_OK;
 }
@@ -418,6 +418,21 @@ int oscar_decode_attention(oscar_cache* c, const void* q, int32_t q_dtype, const
         tiles += (int64_t)int2_tiles(p.len[b]) * c->d.num_kv_heads;
     }
     p.tile_off[c->d.batch] = (int32_t)tiles;
+    int64_t pages = 0;
+    for (int32_t b = 0; b < c->d.batch; ++b) {
+        p.page_off[b] = (int32_t)pages;
+        pages += (int64_t)int2_pages(p.len[b]) * c->d.num_kv_heads;
+    }
+    p.page_off[c->d.batch] = (int32_t)pages;
+    if (pages > INT32_MAX / 4) return OSCAR_ERANGE;
+    p.total_pages = (int32_t)pages;
+    if (p.path == 2 && pages > 0) {
+        const int sms = sm_count();
+        if (sms <= 0) return cuda_fail(cudaGetLastError());
+        const int per = mma_warps_per_cta();
+        const int64_t ctas = std::min<int64_t>(std::min(sms, 2 * kMaxCtas / per), (pages + per - 1) / per);
+        p.n_warps = (int32_t)(ctas * per);
+    }
     if (tiles > INT32_MAX / 2) return OSCAR_ERANGE;
     p.total_tiles = (int32_t)tiles;
     if (p.path == 0 && tiles > 0) {

@@ -100,7 +100,7 @@ __global__ void __launch_bounds__(128) split_simt(const __grid_constant__ Decode
     if (len == 0) return;
     const int nsp = int2_splits(len, p.pps);
     // tensor-core path: this kernel only handles the BF16 split (one CTA per request and head)
-    const int s = p.path == 0 ? nsp : (int)blockIdx.x;
+    const int s = p.path != 1 ? nsp : (int)blockIdx.x;
     if (s > nsp) return;
     const int w = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -236,7 +236,7 @@ __global__ void __launch_bounds__(128) split_simt(const __grid_constant__ Decode
         for (int j = 0; j < 4; ++j) sm_o[w][hh][4 * lane + j] = st.o[hh][j];
     __syncthreads();
     const int c = threadIdx.x;
-    float* part = p.path == 0 ? p.part_bf16 + ((size_t)b * p.hkv + h) * p.g * (2 + kD)
+    float* part = p.path != 1 ? p.part_bf16 + ((size_t)b * p.hkv + h) * p.g * (2 + kD)
                               : p.partial + (((size_t)b * p.hkv + h) * p.max_splits + s) * p.g * (2 + kD);
     for (int hh = 0; hh < G; ++hh) {
         float M = -INFINITY;
@@ -304,6 +304,23 @@ __global__ void __launch_bounds__(128) combine(const __grid_constant__ DecodePar
                     }
                 }
             }
+        } else if (p.path == 2) {
+            const int u = b * p.hkv + h;
+            merge(p.part_bf16 + ((size_t)u * p.g + hh) * (2 + kD), c, M, L, O);
+            const int pages = int2_pages(len);
+            if (pages > 0) {
+                // warps w0 .. w1 own the pages of (b, h); each wrote one partial at u + w
+                const int pf = p.page_off[b] + h * pages;
+                const int w0 = (int)((((long long)pf + 1) * p.n_warps - 1) / p.total_pages);
+                const int w1 = (int)((((long long)pf + pages) * p.n_warps - 1) / p.total_pages);
+                for (int w = w0; w <= w1; ++w) {
+                    // warps whose page range is empty (more warps than pages) wrote nothing
+                    const long long lo = ((long long)w * p.total_pages) / p.n_warps;
+                    const long long hi = ((long long)(w + 1) * p.total_pages) / p.n_warps;
+                    if (lo == hi) continue;
+                    merge(p.part_tc + (((size_t)u + w) * p.g + hh) * (2 + kD), c, M, L, O);
+                }
+            }
         } else {
             const int ns = int2_splits(len, p.pps) + 1;
             const float* part = p.partial + ((size_t)b * p.hkv + h) * p.max_splits * p.g * (2 + kD);
@@ -348,6 +365,9 @@ cudaError_t launch_decode(const DecodeParams& p, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     if (p.path == 0) {
         e = launch_decode_tc(p, s);
+        if (e != cudaSuccess) return e;
+    } else if (p.path == 2) {
+        e = launch_decode_mma(p, s);
         if (e != cudaSuccess) return e;
     }
     combine<<<dim3(p.hkv * p.g, p.batch), 128, 0, s>>>(p);

@@ -1,0 +1,434 @@
+// decode_mma.cu -- fused paged GQA decode attention over INT2 pages, warp-level tensor-core MMAs.
+//
+// The read path of the axbrief.com OSCAR page, section "attention-statistics rotation +
+// Triton kernels": keys and values are unpacked and dequantised on chip inside the attention
+// pass, with nothing dequantised written back; the key rotation is applied to the query
+// (q~ = q . R_K from rotate_q), which equals inverse-rotating every key (R_K orthogonal).
+//
+// Every warp works alone on a contiguous range of 64-token INT2 pages of the flattened
+// (request, KV head, page) list, so all warps stream the same number of bytes whatever the
+// request lengths.  A warp keeps its own four-page ring of shared-memory stages filled by
+// bulk-async copies (page-table entries fetched 32 pages ahead), and per 32-token chunk:
+//   scores   S = Q~ K^T on mma.sync.m16n8k16 (fp16 in, fp32 accumulate): A = the query,
+//            rows = head (fp16 high part) and head + 8 (fp16 low part, the rounding residue),
+//            so S_hi + S_lo carries ~22 bits of q~; B = 2-bit key codes placed in registers as
+//            fp16 subnormals code * 2^-24 (a shift and a mask per pair of codes, exact);
+//            one accumulator per 64-channel group because each group has its own scale:
+//            logit = 2^24 s_g S_g + m_g sum_{c in g} q~_c (all in log2 units);
+//   softmax  online, per head, with a lazily raised reference max (output rescaled only when a
+//            logit passes the reference by 2^8);
+//   output   O += P' V on the same MMA: A = P' = p * s_V (fp16) taken straight from the score
+//            accumulators' register layout, B = the value codes (channel-major pages) as fp16
+//            subnormals; the m_V term sum_t p m_V is accumulated on the CUDA cores.
+// The token order inside a page is permuted consistently between the score fragments (the
+// B columns), the probability fragments (the A columns) and the value fragments so that every
+// fragment comes from the thread's own registers.  At the end of each (request, KV head) run
+// the warp writes (reference max, sum, unnormalised output) to the split-K partial buffer.
+//
+// mbarrier waits are bounded; on timeout the kernel records an error word and the warp stops.
+#include <cuda_fp16.h>
+
+#include "internal.h"
+#include "tc_ptx.h"
+
+namespace oscar {
+namespace {
+
+using namespace ptx;
+
+constexpr int kWarpsPerCta = 8;
+constexpr int kThreadsMma = kWarpsPerCta * 32;
+constexpr int kStagesPerWarp = 4;
+constexpr float kTauM = 8.0f;
+constexpr float kQScaleM = 1.4426950408889634f * 0.08838834764831845f;   // log2(e) / sqrt(128)
+constexpr float kTwo24 = 16777216.0f;
+
+struct MmaSmem {
+    uint8_t stage[kWarpsPerCta][kStagesPerWarp][kPageHeadBytes];
+    uint64_t full[kWarpsPerCta][kStagesPerWarp];
+    float tsc[kWarpsPerCta][32][8];     // per-token scales of the current chunk
+};
+
+// (request, KV head, page) walk over the flattened page list
+struct PageIt {
+    int b, h, j, pages;
+    __device__ __forceinline__ void init(const DecodeParams& p, int P) {
+        int lo = 0, hi = p.batch;
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (p.page_off[mid] <= P) lo = mid;
+            else hi = mid;
+        }
+        b = lo;
+        pages = int2_pages(p.len[b]);
+        const int rem = P - p.page_off[b];
+        h = rem / pages;
+        j = rem - h * pages;
+    }
+    __device__ __forceinline__ bool next(const DecodeParams& p) {   // true when a new segment starts
+        if (++j < pages) return false;
+        j = 0;
+        if (++h == p.hkv) {
+            h = 0;
+            do {
+                ++b;
+            } while (b < p.batch - 1 && int2_pages(p.len[b]) == 0);
+            if (b >= p.batch) b = p.batch - 1;
+            pages = int2_pages(p.len[b]);
+        }
+        return true;
+    }
+};
+
+__device__ __forceinline__ bool wait_full(uint32_t bar, uint32_t parity, int* err) {
+    if (mbar_try(bar, parity)) return true;
+    for (int t = 0; t < 2000; ++t)
+        if (mbar_try_sleep(bar, parity, 1000000)) return true;
+    atomicOr(err, 1);
+    return false;
+}
+
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// codes at bits 2r and 2r + 16 of w as two fp16 subnormals code * 2^-24
+__device__ __forceinline__ uint32_t code_pair(uint32_t w, int r) { return (w >> (2 * r)) & 0x00030003u; }
+
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
+    const __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// token (0..31 of a 32-token chunk) behind score column col of n-tile nt (0..3)
+__device__ __forceinline__ int ptok(int nt, int col) {
+    return 16 * (nt >> 1) + 4 * (nt & 1) + (col >> 1) + 8 * (col & 1);
+}
+
+template <int G>
+__global__ void __launch_bounds__(kThreadsMma, 1) decode_mma(const __grid_constant__ DecodeParams p) {
+    constexpr int MT = (G + 7) / 8;              // heads per thread (rows g and g + 8 of each m-tile)
+    constexpr int NT = MT == 1 ? 4 : 2;          // score n-tiles per chunk (8 tokens each)
+    constexpr int CT = 8 * NT;                   // tokens per chunk
+    constexpr int KK = NT / 2;                   // PV k-steps per chunk
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    MmaSmem* sm = reinterpret_cast<MmaSmem*>(smem_raw);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int g = lane >> 2, tig = lane & 3;
+    const int gw = blockIdx.x * kWarpsPerCta + warp;
+    const int P0 = (int)(((long long)gw * p.total_pages) / p.n_warps);
+    const int P1 = (int)(((long long)(gw + 1) * p.total_pages) / p.n_warps);
+    const int n = P1 - P0;
+    if (lane == 0) {
+        for (int s = 0; s < kStagesPerWarp; ++s) mbar_init(smem_u32(&sm->full[warp][s]), 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+    if (n <= 0) return;
+
+    // ---- page-table prefetch: lane l holds the physical page of page (base + l)
+    auto fetch_pt = [&](int base) -> int32_t {
+        const int P = P0 + base + lane;
+        if (base + lane >= n) return 0;
+        PageIt t;
+        t.init(p, P);
+        return p.page_table[(size_t)t.b * p.max_pps + t.j];
+    };
+    int pt_base = 0;
+    int32_t pt_cur = fetch_pt(0);
+    int32_t pt_nxt = fetch_pt(32);
+    PageIt is;          // page being issued (lane 0 uses it)
+    is.init(p, P0);
+    int issued = 0;
+    auto issue = [&]() {   // lane 0: copy page `issued` into its stage
+        const int q = issued;
+        const int32_t phys = __shfl_sync(0xffffffffu, (q - pt_base) < 32 ? pt_cur : pt_nxt, (q - pt_base) & 31);
+        if (lane == 0) {
+            const int s = q % kStagesPerWarp;
+            const uint32_t bar = smem_u32(&sm->full[warp][s]);
+            mbar_expect_tx(bar, kPageHeadBytes);
+            bulk_g2s(smem_u32(sm->stage[warp][s]), p.pool + ((size_t)phys * p.hkv + is.h) * kPageHeadBytes,
+                     kPageHeadBytes, bar);
+        }
+        is.next(p);
+        ++issued;
+    };
+    for (int k = 0; k < kStagesPerWarp && k < n; ++k) issue();
+
+    // ---- per-segment state
+    uint32_t qa[MT][8][4];          // query fragments (hi rows g, lo rows g + 8) per head slot and k-step
+    float qs[MT][2];                // sum over each channel group of (q_hi + q_lo)
+    float mref[MT], lsum[MT], mv[MT][2];
+    float o[16][4];                 // output accumulators: channel tile ntc, rows g / g + 8
+    PageIt it;
+    it.init(p, P0);
+    bool seg_start = true;
+
+    int consumed = 0;
+    for (int i = 0; i < n; ++i) {
+        const int s = i % kStagesPerWarp;
+        if (seg_start) {
+            // query fragments of this (request, KV head): channels 16 ks + tig + 4 f + 8 e
+#pragma unroll
+            for (int k = 0; k < MT; ++k) {
+                const int hd = g + 8 * k;
+                float part0 = 0.f, part1 = 0.f;
+                const float* qr = p.qrot + (((size_t)it.b * p.hkv + it.h) * G + (hd < G ? hd : 0)) * kD;
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    float hv[2][2], lv[2][2];
+#pragma unroll
+                    for (int f = 0; f < 2; ++f)
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            const float q = hd < G ? qr[16 * ks + tig + 4 * f + 8 * e] * kQScaleM : 0.f;
+                            const float h = __half2float(__float2half_rn(q));
+                            const float l = __half2float(__float2half_rn(q - h));
+                            hv[f][e] = h;
+                            lv[f][e] = l;
+                            if (ks < 4) part0 += h + l;
+                            else part1 += h + l;
+                        }
+                    qa[k][ks][0] = pack_h2(hv[0][0], hv[0][1]);
+                    qa[k][ks][1] = pack_h2(lv[0][0], lv[0][1]);
+                    qa[k][ks][2] = pack_h2(hv[1][0], hv[1][1]);
+                    qa[k][ks][3] = pack_h2(lv[1][0], lv[1][1]);
+                }
+                part0 += __shfl_xor_sync(0xffffffffu, part0, 1);
+                part0 += __shfl_xor_sync(0xffffffffu, part0, 2);
+                part1 += __shfl_xor_sync(0xffffffffu, part1, 1);
+                part1 += __shfl_xor_sync(0xffffffffu, part1, 2);
+                qs[k][0] = part0;
+                qs[k][1] = part1;
+                mref[k] = -INFINITY;
+                lsum[k] = 0.f;
+                mv[k][0] = mv[k][1] = 0.f;
+            }
+#pragma unroll
+            for (int c = 0; c < 16; ++c) o[c][0] = o[c][1] = o[c][2] = o[c][3] = 0.f;
+            seg_start = false;
+        }
+        const bool got = wait_full(smem_u32(&sm->full[warp][s]), (i / kStagesPerWarp) & 1, p.err);
+        if (!__all_sync(0xffffffffu, got)) break;      // error word set; stop issuing, drain below
+        consumed = i + 1;
+        const uint8_t* pg = sm->stage[warp][s];
+        const int n_live = min(kPage, int2_tokens(p.len[it.b]) - it.j * kPage);
+
+#pragma unroll 1
+        for (int cbase = 0; cbase < kPage; cbase += CT) {
+            // ---- per-token scales of the chunk (one token per lane), staged in shared memory
+            __syncwarp();
+            if (lane < CT) {
+                const int t = cbase + lane;
+                const bool live = t < n_live;
+                const uint2 ksm = *reinterpret_cast<const uint2*>(pg + kKSm + t * 8);
+                const uint2 vsm = *reinterpret_cast<const uint2*>(pg + kVSm + t * 8);
+                float4 a, v;
+                a.x = live ? kTwo24 * __half2float(__ushort_as_half(ksm.x & 0xffff)) : 0.f;
+                a.y = live ? __half2float(__ushort_as_half(ksm.x >> 16)) : 0.f;
+                a.z = live ? kTwo24 * __half2float(__ushort_as_half(ksm.y & 0xffff)) : 0.f;
+                a.w = live ? __half2float(__ushort_as_half(ksm.y >> 16)) : 0.f;
+                v.x = live ? __half2float(__ushort_as_half(vsm.x & 0xffff)) : 0.f;
+                v.y = live ? __half2float(__ushort_as_half(vsm.x >> 16)) : 0.f;
+                v.z = live ? __half2float(__ushort_as_half(vsm.y & 0xffff)) : 0.f;
+                v.w = live ? __half2float(__ushort_as_half(vsm.y >> 16)) : 0.f;
+                reinterpret_cast<float4*>(sm->tsc[warp][lane])[0] = a;
+                reinterpret_cast<float4*>(sm->tsc[warp][lane])[1] = v;
+            }
+            __syncwarp();
+
+            // ---- scores: acc[k][nt][group]
+            float acc[MT][NT][2][4];
+#pragma unroll
+            for (int k = 0; k < MT; ++k)
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                    for (int gr = 0; gr < 2; ++gr) acc[k][nt][gr][0] = acc[k][nt][gr][1] = acc[k][nt][gr][2] = acc[k][nt][gr][3] = 0.f;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                const int tok = cbase + ptok(nt, g);
+                const uint4 w0 = *reinterpret_cast<const uint4*>(pg + kKCodes + tok * 32);
+                const uint4 w1 = *reinterpret_cast<const uint4*>(pg + kKCodes + tok * 32 + 16);
+                const uint32_t wd[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    const uint32_t b0 = code_pair(wd[ks], tig), b1 = code_pair(wd[ks], tig + 4);
+#pragma unroll
+                    for (int k = 0; k < MT; ++k) mma16816(acc[k][nt][ks >> 2], qa[k][ks], b0, b1);
+                }
+            }
+
+            // ---- logits, online softmax, P' fragments
+            uint32_t pa[2][KK][4];           // [group][k-step][A register]
+#pragma unroll
+            for (int gr = 0; gr < 2; ++gr)
+#pragma unroll
+                for (int kk = 0; kk < KK; ++kk) pa[gr][kk][0] = pa[gr][kk][1] = pa[gr][kk][2] = pa[gr][kk][3] = 0u;
+            float lg[MT][NT][2];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int t = ptok(nt, 2 * tig + e);
+                    const float4 a = reinterpret_cast<const float4*>(sm->tsc[warp][t])[0];
+                    const bool live = cbase + t < n_live;
+#pragma unroll
+                    for (int k = 0; k < MT; ++k) {
+                        const float s0 = acc[k][nt][0][e] + acc[k][nt][0][2 + e];
+                        const float s1 = acc[k][nt][1][e] + acc[k][nt][1][2 + e];
+                        const float x = fmaf(a.x, s0, fmaf(a.z, s1, fmaf(a.y, qs[k][0], a.w * qs[k][1])));
+                        lg[k][nt][e] = live ? x : -INFINITY;
+                    }
+                }
+#pragma unroll
+            for (int k = 0; k < MT; ++k) {
+                float cm = -INFINITY;
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) cm = fmaxf(cm, fmaxf(lg[k][nt][0], lg[k][nt][1]));
+                cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, 1));
+                cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, 2));
+                if (cm > mref[k] + kTauM) {
+                    // raise the reference (rare after the first chunk of a run); rescale this head
+                    const float f = mref[k] == -INFINITY ? 0.f : ex2(mref[k] - cm);
+                    mref[k] = cm;
+                    lsum[k] *= f;
+                    mv[k][0] *= f;
+                    mv[k][1] *= f;
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) {
+                        o[c][2 * k] *= f;
+                        o[c][2 * k + 1] *= f;
+                    }
+                }
+            }
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                float pv[MT][2][2];          // [head slot][group][column e]
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int t = ptok(nt, 2 * tig + e);
+                    const float4 v = reinterpret_cast<const float4*>(sm->tsc[warp][t])[1];
+#pragma unroll
+                    for (int k = 0; k < MT; ++k) {
+                        const float pr = lg[k][nt][e] == -INFINITY ? 0.f : ex2(lg[k][nt][e] - mref[k]);
+                        lsum[k] += pr;
+                        mv[k][0] = fmaf(pr, v.y, mv[k][0]);
+                        mv[k][1] = fmaf(pr, v.w, mv[k][1]);
+                        pv[k][0][e] = pr * v.x;
+                        pv[k][1][e] = pr * v.z;
+                    }
+                }
+                // A fragment of PV k-step nt / 2: registers 0 / 1 (first n-tile), 2 / 3 (second)
+                const int kk = nt >> 1, half = nt & 1;
+#pragma unroll
+                for (int gr = 0; gr < 2; ++gr) {
+                    pa[gr][kk][2 * half] = pack_h2(pv[0][gr][0], pv[0][gr][1]);
+                    if constexpr (MT == 2) pa[gr][kk][2 * half + 1] = pack_h2(pv[1][gr][0], pv[1][gr][1]);
+                }
+            }
+
+            // ---- output: O[ntc] += P'_{group(ntc)} x V[tokens][channel 8 ntc + g]
+#pragma unroll
+            for (int ntc = 0; ntc < 16; ++ntc) {
+                const int c = 8 * ntc + g;
+                const uint32_t* vw = reinterpret_cast<const uint32_t*>(pg + kVCodes + c * 16) + (cbase >> 4);
+#pragma unroll
+                for (int kk = 0; kk < KK; ++kk) {
+                    const uint32_t w = vw[kk];
+                    mma16816(o[ntc], pa[ntc >> 3][kk], code_pair(w, tig), code_pair(w, tig + 4));
+                }
+            }
+        }
+
+        // ---- stage consumed: refill it with the page kStagesPerWarp ahead
+        __syncwarp();
+        fence_proxy_async();
+        if (issued < n) {
+            if (issued >= pt_base + 32) {
+                pt_base += 32;
+                pt_cur = pt_nxt;
+                pt_nxt = fetch_pt(pt_base + 32);
+            }
+            issue();
+        }
+
+        // ---- end of this warp's part of a (request, KV head) run: write the partial result
+        const bool last = (i == n - 1);
+        const int b_now = it.b, h_now = it.h;
+        const bool new_seg = it.next(p);
+        if (last || new_seg) {
+            float* part = p.part_tc + ((size_t)(b_now * p.hkv + h_now) + gw) * G * (2 + kD);
+#pragma unroll
+            for (int k = 0; k < MT; ++k) {
+                const int hd = g + 8 * k;
+                float l = lsum[k], m0 = mv[k][0], m1 = mv[k][1];
+                l += __shfl_xor_sync(0xffffffffu, l, 1);
+                l += __shfl_xor_sync(0xffffffffu, l, 2);
+                m0 += __shfl_xor_sync(0xffffffffu, m0, 1);
+                m0 += __shfl_xor_sync(0xffffffffu, m0, 2);
+                m1 += __shfl_xor_sync(0xffffffffu, m1, 1);
+                m1 += __shfl_xor_sync(0xffffffffu, m1, 2);
+                if (hd < G) {
+                    float* ph = part + (size_t)hd * (2 + kD);
+#pragma unroll
+                    for (int ntc = 0; ntc < 16; ++ntc) {
+                        const float mg = ntc < 8 ? m0 : m1;
+                        const float2 val = make_float2(fmaf(kTwo24, o[ntc][2 * k], mg), fmaf(kTwo24, o[ntc][2 * k + 1], mg));
+                        *reinterpret_cast<float2*>(ph + 2 + 8 * ntc + 2 * tig) = val;
+                    }
+                    if (tig == 0) {
+                        ph[0] = mref[k];
+                        ph[1] = l;
+                    }
+                }
+            }
+            seg_start = true;
+        }
+    }
+    // copies still in flight must land before the warp may exit (only after a timeout)
+    if (lane == 0)
+        for (int q = consumed; q < issued; ++q) wait_full(smem_u32(&sm->full[warp][q % kStagesPerWarp]), (q / kStagesPerWarp) & 1, p.err);
+}
+
+template <int G>
+cudaError_t launch_mma_g(const DecodeParams& p, cudaStream_t s) {
+    const int smem = (int)sizeof(MmaSmem);
+    cudaError_t e = cudaFuncSetAttribute(decode_mma<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    decode_mma<G><<<p.n_warps / kWarpsPerCta, kThreadsMma, smem, s>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+int mma_warps_per_cta() { return kWarpsPerCta; }
+
+cudaError_t launch_decode_mma(const DecodeParams& p, cudaStream_t s) {
+    if (p.total_pages == 0) return cudaSuccess;
+    count_launches(1);
+    switch (p.g) {
+        case 1: return launch_mma_g<1>(p, s);
+        case 2: return launch_mma_g<2>(p, s);
+        case 3: return launch_mma_g<3>(p, s);
+        case 4: return launch_mma_g<4>(p, s);
+        case 5: return launch_mma_g<5>(p, s);
+        case 6: return launch_mma_g<6>(p, s);
+        case 7: return launch_mma_g<7>(p, s);
+        case 8: return launch_mma_g<8>(p, s);
+        case 12: return launch_mma_g<12>(p, s);
+        case 16: return launch_mma_g<16>(p, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace oscar

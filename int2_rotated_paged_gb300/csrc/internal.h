@@ -74,6 +74,10 @@ struct DecodeParams {
     float* part_bf16;      // [batch * hkv][g][2 + 128]
     int32_t* err;          // nonzero after a bounded wait gave up
     int32_t tile_off[kMaxBatch + 1];   // sum over earlier requests of tiles * hkv
+    // warp-MMA path
+    int32_t total_pages;   // INT2 pages over all (request, KV head)
+    int32_t n_warps;       // warps of the warp-MMA kernel
+    int32_t page_off[kMaxBatch + 1];   // sum over earlier requests of pages * hkv
 };
 
 // Split-K partition of one request: INT2 splits of `pps` pages plus one BF16 split.
@@ -97,6 +101,8 @@ __host__ __device__ inline int int2_tiles(int len) {
 cudaError_t launch_append(const AppendParams& p, cudaStream_t s);
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t s);
 cudaError_t launch_decode_tc(const DecodeParams& p, cudaStream_t s);
+cudaError_t launch_decode_mma(const DecodeParams& p, cudaStream_t s);
+int mma_warps_per_cta();
 cudaError_t launch_build_rk(const float* q, int64_t n, int hkv, float* rk, void* ws, cudaStream_t s);
 size_t build_rk_ws_bytes(int hkv);
 

@@ -26,12 +26,15 @@ def _built():
     assert torch.cuda.is_available()
 
 
-@pytest.fixture(params=["tensor", "simt"], autouse=True)
+PATHS = {"mma": K.PATH_WARP_MMA, "tensor": K.PATH_TENSOR, "simt": K.PATH_SIMT}
+
+
+@pytest.fixture(params=list(PATHS), autouse=True)
 def decode_path(request):
-    """Every test runs against both decode kernels: tcgen05 tensor cores and the SIMT baseline."""
-    K.oscar_set_decode_path(K.PATH_TENSOR if request.param == "tensor" else K.PATH_SIMT)
+    """Every test runs against each decode kernel: warp-level MMA, tcgen05 and the SIMT baseline."""
+    K.oscar_set_decode_path(PATHS[request.param])
     yield request.param
-    K.oscar_set_decode_path(K.PATH_TENSOR)
+    K.oscar_set_decode_path(K.PATH_WARP_MMA)
 
 
 def _attend(cache, q, rk_dev, out_dtype=torch.float32):
