@@ -17,9 +17,10 @@
 //            logit = 2^24 s_g S_g + m_g sum_{c in g} q~_c (all in log2 units);
 //   softmax  online, per head, with a lazily raised reference max (output rescaled only when a
 //            logit passes the reference by 2^8);
-//   output   O += P' V on the same MMA: A = P' = p * s_V (fp16) taken straight from the score
-//            accumulators' register layout, B = the value codes (channel-major pages) as fp16
-//            subnormals; the m_V term sum_t p m_V is accumulated on the CUDA cores.
+//   output   O^T += V^T P'^T on the same MMA: A = the value codes (channel-major pages; rows =
+//            16 channels) as fp16 subnormals, B = P' = p * s_V (fp16, columns = 8 heads) taken
+//            straight from the score accumulators' register layout; the m_V term sum_t p m_V is
+//            accumulated on the CUDA cores.
 // The token order inside a page is permuted consistently between the score fragments (the
 // B columns), the probability fragments (the A columns) and the value fragments so that every
 // fragment comes from the thread's own registers.  At the end of each (request, KV head) run
@@ -36,9 +37,9 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kWarpsPerCta = 8;
+constexpr int kWarpsPerCta = 10;
 constexpr int kThreadsMma = kWarpsPerCta * 32;
-constexpr int kStagesPerWarp = 4;
+constexpr int kStagesPerWarp = 3;
 constexpr float kTauM = 8.0f;
 constexpr float kQScaleM = 1.4426950408889634f * 0.08838834764831845f;   // log2(e) / sqrt(128)
 constexpr float kTwo24 = 16777216.0f;
@@ -168,7 +169,7 @@ __global__ void __launch_bounds__(kThreadsMma, 1) decode_mma(const __grid_consta
     uint32_t qa[MT][8][4];          // query fragments (hi rows g, lo rows g + 8) per head slot and k-step
     float qs[MT][2];                // sum over each channel group of (q_hi + q_lo)
     float mref[MT], lsum[MT], mv[MT][2];
-    float o[16][4];                 // output accumulators: channel tile ntc, rows g / g + 8
+    float o[8][MT][4];              // output^T accumulators: channel tile cm, head tile nh
     PageIt it;
     it.init(p, P0);
     bool seg_start = true;
@@ -214,7 +215,9 @@ __global__ void __launch_bounds__(kThreadsMma, 1) decode_mma(const __grid_consta
                 mv[k][0] = mv[k][1] = 0.f;
             }
 #pragma unroll
-            for (int c = 0; c < 16; ++c) o[c][0] = o[c][1] = o[c][2] = o[c][3] = 0.f;
+            for (int c = 0; c < 8; ++c)
+#pragma unroll
+                for (int k = 0; k < MT; ++k) o[c][k][0] = o[c][k][1] = o[c][k][2] = o[c][k][3] = 0.f;
             seg_start = false;
         }
         const bool got = wait_full(smem_u32(&sm->full[warp][s]), (i / kStagesPerWarp) & 1, p.err);
@@ -269,11 +272,7 @@ __global__ void __launch_bounds__(kThreadsMma, 1) decode_mma(const __grid_consta
             }
 
             // ---- logits, online softmax, P' fragments
-            uint32_t pa[2][KK][4];           // [group][k-step][A register]
-#pragma unroll
-            for (int gr = 0; gr < 2; ++gr)
-#pragma unroll
-                for (int kk = 0; kk < KK; ++kk) pa[gr][kk][0] = pa[gr][kk][1] = pa[gr][kk][2] = pa[gr][kk][3] = 0u;
+            uint32_t pb[2][KK][MT][2];       // [group][k-step][head tile][B register]
             float lg[MT][NT][2];
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
@@ -290,6 +289,8 @@ __global__ void __launch_bounds__(kThreadsMma, 1) decode_mma(const __grid_consta
                         lg[k][nt][e] = live ? x : -INFINITY;
                     }
                 }
+            float fown[MT];
+            bool raise = false;
 #pragma unroll
             for (int k = 0; k < MT; ++k) {
                 float cm = -INFINITY;
@@ -297,17 +298,29 @@ __global__ void __launch_bounds__(kThreadsMma, 1) decode_mma(const __grid_consta
                 for (int nt = 0; nt < NT; ++nt) cm = fmaxf(cm, fmaxf(lg[k][nt][0], lg[k][nt][1]));
                 cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, 1));
                 cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, 2));
+                fown[k] = 1.f;
                 if (cm > mref[k] + kTauM) {
-                    // raise the reference (rare after the first chunk of a run); rescale this head
-                    const float f = mref[k] == -INFINITY ? 0.f : ex2(mref[k] - cm);
+                    fown[k] = mref[k] == -INFINITY ? 0.f : ex2(mref[k] - cm);
                     mref[k] = cm;
-                    lsum[k] *= f;
-                    mv[k][0] *= f;
-                    mv[k][1] *= f;
+                    lsum[k] *= fown[k];
+                    mv[k][0] *= fown[k];
+                    mv[k][1] *= fown[k];
+                    raise = true;
+                }
+            }
+            if (__any_sync(0xffffffffu, raise)) {
+                // rare: a head's reference max went up; O^T holds heads 2 tig, 2 tig + 1 (+ 8 nh),
+                // whose factors live in the threads of rows g = head
 #pragma unroll
-                    for (int c = 0; c < 16; ++c) {
-                        o[c][2 * k] *= f;
-                        o[c][2 * k + 1] *= f;
+                for (int k = 0; k < MT; ++k) {
+                    const float f0 = __shfl_sync(0xffffffffu, fown[k], (2 * tig) * 4);
+                    const float f1 = __shfl_sync(0xffffffffu, fown[k], (2 * tig + 1) * 4);
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        o[c][k][0] *= f0;
+                        o[c][k][1] *= f1;
+                        o[c][k][2] *= f0;
+                        o[c][k][3] *= f1;
                     }
                 }
             }
@@ -328,24 +341,27 @@ __global__ void __launch_bounds__(kThreadsMma, 1) decode_mma(const __grid_consta
                         pv[k][1][e] = pr * v.z;
                     }
                 }
-                // A fragment of PV k-step nt / 2: registers 0 / 1 (first n-tile), 2 / 3 (second)
+                // B fragment of PV k-step nt / 2: register 0 (first n-tile of the pair), 1 (second)
                 const int kk = nt >> 1, half = nt & 1;
 #pragma unroll
-                for (int gr = 0; gr < 2; ++gr) {
-                    pa[gr][kk][2 * half] = pack_h2(pv[0][gr][0], pv[0][gr][1]);
-                    if constexpr (MT == 2) pa[gr][kk][2 * half + 1] = pack_h2(pv[1][gr][0], pv[1][gr][1]);
-                }
+                for (int gr = 0; gr < 2; ++gr)
+#pragma unroll
+                    for (int k = 0; k < MT; ++k) pb[gr][kk][k][half] = pack_h2(pv[k][gr][0], pv[k][gr][1]);
             }
 
-            // ---- output: O[ntc] += P'_{group(ntc)} x V[tokens][channel 8 ntc + g]
+            // ---- output^T: O[cm] += V^T[channels 16 cm + g, + 8][tokens] x P'_{group(cm)}
 #pragma unroll
-            for (int ntc = 0; ntc < 16; ++ntc) {
-                const int c = 8 * ntc + g;
-                const uint32_t* vw = reinterpret_cast<const uint32_t*>(pg + kVCodes + c * 16) + (cbase >> 4);
+            for (int cm = 0; cm < 8; ++cm) {
+                const int ca = 16 * cm + g;
+                const uint32_t* va = reinterpret_cast<const uint32_t*>(pg + kVCodes + ca * 16) + (cbase >> 4);
+                const uint32_t* vb = reinterpret_cast<const uint32_t*>(pg + kVCodes + (ca + 8) * 16) + (cbase >> 4);
 #pragma unroll
                 for (int kk = 0; kk < KK; ++kk) {
-                    const uint32_t w = vw[kk];
-                    mma16816(o[ntc], pa[ntc >> 3][kk], code_pair(w, tig), code_pair(w, tig + 4));
+                    const uint32_t wa = va[kk], wb = vb[kk];
+                    const uint32_t av[4] = {code_pair(wa, tig), code_pair(wb, tig), code_pair(wa, tig + 4),
+                                            code_pair(wb, tig + 4)};
+#pragma unroll
+                    for (int k = 0; k < MT; ++k) mma16816(o[cm][k], av, pb[cm >> 2][kk][k][0], pb[cm >> 2][kk][k][1]);
                 }
             }
         }
@@ -370,7 +386,7 @@ __global__ void __launch_bounds__(kThreadsMma, 1) decode_mma(const __grid_consta
             float* part = p.part_tc + ((size_t)(b_now * p.hkv + h_now) + gw) * G * (2 + kD);
 #pragma unroll
             for (int k = 0; k < MT; ++k) {
-                const int hd = g + 8 * k;
+                // per-head totals over the four threads of the head's row group
                 float l = lsum[k], m0 = mv[k][0], m1 = mv[k][1];
                 l += __shfl_xor_sync(0xffffffffu, l, 1);
                 l += __shfl_xor_sync(0xffffffffu, l, 2);
@@ -378,17 +394,25 @@ __global__ void __launch_bounds__(kThreadsMma, 1) decode_mma(const __grid_consta
                 m0 += __shfl_xor_sync(0xffffffffu, m0, 2);
                 m1 += __shfl_xor_sync(0xffffffffu, m1, 1);
                 m1 += __shfl_xor_sync(0xffffffffu, m1, 2);
-                if (hd < G) {
-                    float* ph = part + (size_t)hd * (2 + kD);
+                const int hown = g + 8 * k;
+                if (hown < G && tig == 0) {
+                    part[(size_t)hown * (2 + kD) + 0] = mref[k];
+                    part[(size_t)hown * (2 + kD) + 1] = l;
+                }
+                // this thread's output entries: heads 8 k + 2 tig + e, channels 16 cm + g (+ 8)
 #pragma unroll
-                    for (int ntc = 0; ntc < 16; ++ntc) {
-                        const float mg = ntc < 8 ? m0 : m1;
-                        const float2 val = make_float2(fmaf(kTwo24, o[ntc][2 * k], mg), fmaf(kTwo24, o[ntc][2 * k + 1], mg));
-                        *reinterpret_cast<float2*>(ph + 2 + 8 * ntc + 2 * tig) = val;
-                    }
-                    if (tig == 0) {
-                        ph[0] = mref[k];
-                        ph[1] = l;
+                for (int e = 0; e < 2; ++e) {
+                    const int hd = 8 * k + 2 * tig + e;
+                    const float mh0 = __shfl_sync(0xffffffffu, m0, (2 * tig + e) * 4);
+                    const float mh1 = __shfl_sync(0xffffffffu, m1, (2 * tig + e) * 4);
+                    if (hd < G) {
+                        float* ph = part + (size_t)hd * (2 + kD) + 2;
+#pragma unroll
+                        for (int cm = 0; cm < 8; ++cm) {
+                            const float mg = cm < 4 ? mh0 : mh1;
+                            ph[16 * cm + g] = fmaf(kTwo24, o[cm][k][e], mg);
+                            ph[16 * cm + g + 8] = fmaf(kTwo24, o[cm][k][2 + e], mg);
+                        }
                     }
                 }
             }
