@@ -55,6 +55,7 @@ extern "C" {
 #define OSCAR_EALIGN (-5)     /* a device pointer is not 16-byte aligned */
 #define OSCAR_ERANGE (-6)     /* a request index or position is out of range */
 #define OSCAR_ETIMEOUT (-7)   /* a bounded wait inside a kernel gave up (see oscar_decode_status) */
+#define OSCAR_ESCRATCH (-8)   /* the call needs more scratch than oscar_decode_attention_noalloc has */
 
 #define OSCAR_DTYPE_F32 0
 #define OSCAR_DTYPE_BF16 1
@@ -195,6 +196,29 @@ int oscar_set_decode_path(int32_t path);
  * (OSCAR_ETIMEOUT; its output is then undefined). */
 int oscar_decode_status(const void *workspace, size_t workspace_bytes, const oscar_cache *c,
                         void *stream);
+
+/* oscar_decode_attention_noalloc: oscar_decode_attention without a workspace argument, for
+ * callers that cannot allocate device memory at the time they run attention: code executing
+ * inside a host-side framework hook that forbids allocation (an inference-engine plugin's
+ * enqueue, a real-time loop that must not touch the allocator), or a process whose device
+ * memory is already fully reserved by another runtime.  No counterpart on the OSCAR pages: it
+ * is a deployment convenience of this library.
+ * Scratch comes from one fixed 16 MiB array in the library's device code, which every GPU that
+ * loads the library holds until the process exits.  A call whose scratch (rotated queries,
+ * split-K partials, an error word) would not fit returns OSCAR_ESCRATCH and enqueues nothing;
+ * e.g. 32 requests x 64 query heads (8 KV heads) need about 9.5 MiB.  It always uses the
+ * warp-level MMA decode kernel and gives the same result as oscar_decode_attention on that path.
+ * It calls no cudaMalloc / cudaFree and no allocating library routine.  The first call on a
+ * device looks up the array's device address (cudaGetSymbolAddress) with that device current,
+ * so make that first call before any stream capture.  All calls share the array and it keeps
+ * the last call's contents: calls that may run at the same time on the GPU (other streams,
+ * other threads, two caches) race on it and must be serialised by the caller.  Nothing in the
+ * array has to start at zero: the one word that must (the flag a bounded in-kernel wait sets
+ * when it gives up) is cleared by each call before its kernels read it.  That flag lives in the
+ * fixed array, so oscar_decode_status cannot read it for this variant.  q, rk, out and the
+ * dtypes are as for oscar_decode_attention. */
+int oscar_decode_attention_noalloc(oscar_cache *c, const void *q, int32_t q_dtype, const float *rk,
+                                   void *out, int32_t out_dtype, void *stream);
 
 /* ---------------------------------------------------------------- calibration
  * oscar_build_rk: R_K = U_Q * H_Had * P_br for num_kv_heads heads from n query samples

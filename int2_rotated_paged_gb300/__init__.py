@@ -35,8 +35,9 @@ EXPORTS = [
     "kv_page_table_free_pages", "kv_quant_append", "oscar_decode_workspace_bytes",
     "oscar_decode_attention", "oscar_build_rk_workspace_bytes", "oscar_build_rk", "oscar_read_int2",
     "oscar_read_bf16", "oscar_strerror", "oscar_last_cuda_error", "oscar_launch_count",
-    "oscar_set_decode_path", "oscar_decode_status",
+    "oscar_set_decode_path", "oscar_decode_status", "oscar_decode_attention_noalloc",
 ]
+OSCAR_ESCRATCH = -8
 OSCAR_ETIMEOUT = -7
 PATH_TENSOR = 0
 PATH_SIMT = 1
@@ -98,6 +99,7 @@ def lib() -> ctypes.CDLL:
         "oscar_launch_count": (I64, []),
         "oscar_set_decode_path": (ctypes.c_int, [I32]),
         "oscar_decode_status": (ctypes.c_int, [P, SZ, P, P]),
+        "oscar_decode_attention_noalloc": (ctypes.c_int, [P, P, I32, P, P, I32, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -193,6 +195,12 @@ def oscar_decode_attention(cache, q, q_dtype: int, rk, out, out_dtype: int, work
     nbytes = workspace.numel() * workspace.element_size()
     _check("oscar_decode_attention", lib().oscar_decode_attention(
         cache, _ptr(q), q_dtype, _ptr(rk), _ptr(out), out_dtype, _ptr(workspace), nbytes, _stream(stream)))
+
+
+def oscar_decode_attention_noalloc(cache, q, q_dtype: int, rk, out, out_dtype: int, stream=None):
+    """Decode attention with the library's fixed device scratch (for callers that cannot allocate)."""
+    _check("oscar_decode_attention_noalloc", lib().oscar_decode_attention_noalloc(
+        cache, _ptr(q), q_dtype, _ptr(rk), _ptr(out), out_dtype, _stream(stream)))
 
 
 def oscar_build_rk_workspace_bytes(num_kv_heads: int) -> int:

@@ -538,6 +538,7 @@ const char* oscar_strerror(int code) {
         case OSCAR_EALIGN: return "device pointer not 16-byte aligned";
         case OSCAR_ERANGE: return "index or position out of range";
         case OSCAR_ETIMEOUT: return "a kernel wait timed out";
+        case OSCAR_ESCRATCH: return "call needs more than the library's fixed scratch";
         default: return "unknown error";
     }
 }
@@ -547,3 +548,69 @@ int oscar_last_cuda_error(void) { return g_last_cuda; }
 int64_t oscar_launch_count(void) { return g_launches; }
 
 }  // extern "C"
+
+// ------------------------------------------------------------------ fixed-scratch decode (helper)
+
+namespace oscar {
+
+// Fill the parameters of a warp-MMA decode whose scratch is the compact layout
+//   rotated queries | one partial per (request, KV head) and per warp | BF16 partials | error word
+// inside `scratch` (scratch_bytes long).  Used by oscar_decode_attention_noalloc only.
+int noalloc_decode_params(oscar_cache* c, const void* q, int32_t q_dtype, const float* rk, void* out,
+                          int32_t out_dtype, void* scratch, size_t scratch_bytes, DecodeParams* pp,
+                          cudaStream_t stream) {
+    if (!c || !q || !rk || !out || !pp || !scratch) return OSCAR_EINVAL;
+    if ((q_dtype != OSCAR_DTYPE_F32 && q_dtype != OSCAR_DTYPE_BF16) ||
+        (out_dtype != OSCAR_DTYPE_F32 && out_dtype != OSCAR_DTYPE_BF16))
+        return OSCAR_EINVAL;
+    if (!aligned16(q) || !aligned16(rk) || !aligned16(out)) return OSCAR_EALIGN;
+    DecodeParams& p = *pp;
+    std::memset(&p, 0, sizeof(p));
+    p.batch = c->d.batch;
+    p.hkv = c->d.num_kv_heads;
+    p.g = c->g;
+    p.pps = pick_pps(c);
+    p.max_splits = kMaxSplits;
+    p.q = q;
+    p.q_dtype = q_dtype;
+    p.rk = rk;
+    p.out = out;
+    p.out_dtype = out_dtype;
+    p.pool = c->pool;
+    p.bf16 = c->bf16;
+    p.page_table = c->pt;
+    p.max_pps = c->d.max_pages_per_seq;
+    p.path = OSCAR_PATH_WARP_MMA;
+    int64_t pages = 0;
+    for (int32_t b = 0; b < c->d.batch; ++b) {
+        p.len[b] = (int32_t)c->len[b];
+        p.page_off[b] = (int32_t)pages;
+        pages += (int64_t)int2_pages(p.len[b]) * c->d.num_kv_heads;
+    }
+    p.page_off[c->d.batch] = (int32_t)pages;
+    if (pages > INT32_MAX / 4) return OSCAR_ERANGE;
+    p.total_pages = (int32_t)pages;
+    if (pages > 0) {
+        const int sms = sm_count();
+        if (sms <= 0) return cuda_fail(cudaGetLastError());
+        const int per = mma_warps_per_cta();
+        const int64_t ctas = std::min<int64_t>(std::min(sms, 2 * kMaxCtas / per), (pages + per - 1) / per);
+        p.n_warps = (int32_t)(ctas * per);
+    }
+    const size_t per_part = (size_t)c->g * (2 + kD) * sizeof(float);
+    const size_t bh = (size_t)c->d.batch * c->d.num_kv_heads;
+    const size_t o_qrot = 0;
+    const size_t o_tc = o_qrot + (((size_t)c->d.batch * c->d.num_q_heads * kD * sizeof(float) + 255) & ~(size_t)255);
+    const size_t o_bf16 = o_tc + (bh + (size_t)p.n_warps) * per_part;
+    const size_t o_err = o_bf16 + bh * per_part;
+    if (o_err + 16 > scratch_bytes) return OSCAR_ESCRATCH;
+    uint8_t* ws = (uint8_t*)scratch;
+    p.qrot = (float*)(ws + o_qrot);
+    p.part_tc = (float*)(ws + o_tc);
+    p.part_bf16 = (float*)(ws + o_bf16);
+    p.err = (int32_t*)(ws + o_err);
+    p.partial = nullptr;   // SIMT partials are not used on the warp-MMA path
+    return sync(c, stream);
+}
+
+}  // namespace oscar

@@ -6,6 +6,8 @@
 
 #include <cuda_runtime.h>
 
+struct oscar_cache;
+
 namespace oscar {
 
 constexpr int kD = 128;            // head_dim
@@ -107,5 +109,10 @@ cudaError_t launch_build_rk(const float* q, int64_t n, int hkv, float* rk, void*
 size_t build_rk_ws_bytes(int hkv);
 
 void count_launches(int n);
+
+// Parameters of a warp-MMA decode using one fixed scratch buffer (see noalloc.cu).
+int noalloc_decode_params(oscar_cache* c, const void* q, int32_t q_dtype, const float* rk, void* out,
+                          int32_t out_dtype, void* scratch, size_t scratch_bytes, DecodeParams* p,
+                          cudaStream_t stream);
 
 }  // namespace oscar
