@@ -42,17 +42,20 @@ sys.path.insert(0, ROOT)
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="qwen3_32b")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--cpu-pairs", type=int, default=3, help="(request, KV head) pairs the CPU oracle times")
+    ap.add_argument("--cpu-pairs", type=int, default=12,
+                    help="(request, KV head) pairs the CPU oracle times for cpu_baseline (about 1 s each)")
+    ap.add_argument("--ref-pairs", type=int, default=3,
+                    help="(request, KV head) pairs per step of --impl reference")
     ap.add_argument("--batch", type=int, default=0,
                     help="requests per GPU (0 = the workload's batch); smaller values are for profiling")
-    ap.add_argument("--path", default="mma", choices=["mma", "tensor", "simt"],
-                    help="decode kernel: warp-level MMA (default), tcgen05, or the SIMT baseline")
+    ap.add_argument("--path", default="mma", choices=["mma", "simt"],
+                    help="decode kernel: warp-level MMA (default) or the SIMT baseline")
     return ap.parse_args()
 
 
@@ -68,6 +71,12 @@ def decode_bytes(lens, hkv, hq, q_bytes=4, out_bytes=4):
     return tot + len(lens) * hq * 128 * (q_bytes + out_bytes)
 
 
+def int2_kernel_bytes(lens, hkv, hq):
+    """Algorithmic bytes of one launch of the INT2 attention kernel: every INT2 token's K and V
+    codes (32 + 32 B) and fp16 scale/min (8 + 8 B) per KV head, plus the fp32 rotated queries."""
+    return sum(hkv * max(0, L - 320) * 80 for L in lens) + len(lens) * hq * 128 * 4
+
+
 def peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -77,15 +86,25 @@ def peaks():
         return 6800.0, "fallback"
 
 
-def profiled_traffic(kernel_src: str):
-    """DRAM bytes per decode call from the committed ncu summary, if it still matches the source."""
-    path = os.path.join(ROOT, "profiles", "decode_traffic.json")
-    src = os.path.join(ROOT, "int2_rotated_paged_gb300", "csrc", kernel_src)
+def kernel_source_hash():
+    """Hash of the sources that decide the INT2 attention kernel's memory traffic."""
+    h = hashlib.sha256()
+    for name in ("decode_mma.cu", "internal.h"):
+        h.update(open(os.path.join(ROOT, "int2_rotated_paged_gb300", "csrc", name), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str, scale: float):
+    """DRAM bytes (read + write) per launch of the INT2 attention kernel, from the committed ncu
+    summary: measured on a smaller batch of the same workload and scaled by the INT2 bytes,
+    or None when the kernel changed since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", "decode_mma_traffic.json")
     try:
         with open(path) as f:
             rec = json.load(f)
-        h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-        return rec["bytes_per_call"] if rec.get("source_sha256_16") == h else None
+        if rec.get("source_sha256_16") != kernel_source_hash() or rec.get("workload") != workload:
+            return None
+        return rec["dram_bytes_per_launch"] * scale / rec["int2_bytes_per_launch"]
     except Exception:
         return None
 
@@ -107,7 +126,7 @@ class Clocks:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
         except Exception:
@@ -145,50 +164,68 @@ class Clocks:
 
 # ------------------------------------------------------------------ CPU oracle timing
 
-def cpu_oracle_sample(cfg, lens, n_pairs: int, reps: int = 1):
-    """Time the CPU oracle's decode attention on (request, KV head) pairs of the workload."""
-    import numpy as np
+def cpu_oracle_sample(cfg, lens, n_pairs: int, reps: int = 1, ctx_cap: int = 0):
+    """Time the CPU oracle on (request, KV head) pairs of the workload.  Each rep is one decode
+    step of every sampled pair: append one token (window insert and, past 320 tokens, the
+    eviction of one token to INT2), then attend.  ctx_cap > 0 keeps only the first ctx_cap
+    tokens of each sampled request.  Returns (bytes per rep, seconds per rep, pairs, context)."""
     import oracle
     import synth
     oracle.build()
     pairs = [(b % cfg.batch, (3 * b + 1) % cfg.num_kv_heads) for b in range(n_pairs)]
+    ctx = [min(lens[b], ctx_cap) if ctx_cap > 0 else lens[b] for b in range(len(lens))]
     caches = []
     for (b, h) in pairs:
         rk = oracle.build_rk(synth.calibration_queries(cfg.seed, h, 4096).numpy())[0]
         oc = oracle.OracleCache(rk)
-        oc.append(synth.bf16_bits(synth.keys(cfg.seed, b, h, 0, lens[b])),
-                  synth.bf16_bits(synth.values(cfg.seed, b, h, 0, lens[b])))
+        oc.append(synth.bf16_bits(synth.keys(cfg.seed, b, h, 0, ctx[b] + reps)),
+                  synth.bf16_bits(synth.values(cfg.seed, b, h, 0, ctx[b] + reps)))
         caches.append((b, h, oc))
-    q = synth.queries(cfg.seed, 0, cfg.batch, cfg.num_q_heads, cfg.num_kv_heads, dtype=cfg.q_dtype).numpy()
     g = cfg.group
-    times = []
-    for _ in range(reps):
+    times, nbytes = [], []
+    for r in range(reps):
+        q = synth.queries(cfg.seed, r, cfg.batch, cfg.num_q_heads, cfg.num_kv_heads, dtype=cfg.q_dtype).numpy()
+        steps = [(oc, synth.bf16_bits(synth.keys(cfg.seed, b, h, ctx[b] + r, 1)),
+                  synth.bf16_bits(synth.values(cfg.seed, b, h, ctx[b] + r, 1)), q[b, h * g:(h + 1) * g])
+                 for (b, h, oc) in caches]
         t0 = time.perf_counter()
-        for (b, h, oc) in caches:
-            oc.attend(q[b, h * g:(h + 1) * g])
+        for (oc, k1, v1, qb) in steps:
+            oc.append(k1, v1)
+            oc.attend(qb)
         times.append(time.perf_counter() - t0)
-    nbytes = sum(decode_bytes([lens[b]], 1, g) for (b, h, _) in caches)
-    return nbytes, times, pairs
+        nbytes.append(sum(decode_bytes([ctx[b] + r + 1], 1, g) for (b, h, _) in caches))
+    return nbytes, times, pairs, ctx
 
 
 # ------------------------------------------------------------------ main arms
+
+def workload_config(cfg, lens):
+    return {"workload": f"{cfg.name}: B{cfg.batch} Hq{cfg.num_q_heads}/Hkv{cfg.num_kv_heads} d128 "
+                        f"L{lens[0] if len(set(lens)) == 1 else f'{min(lens)}..{max(lens)}'} INT2 paged decode step "
+                        f"(append 1 token + split-K GQA decode), {cfg.table} pages",
+            "batch_per_gpu": cfg.batch, "context": lens[0] if len(set(lens)) == 1 else [min(lens), max(lens)],
+            "l2": "inputs larger than L2 (about 2.1 GB per step vs 129 MB)"}
+
 
 def run_reference(args, cfg, rank, world):
     if rank != 0:
         return
     lens = [int(x) for x in cfg.ctx]
-    nbytes, times, pairs = cpu_oracle_sample(cfg, lens, args.cpu_pairs, reps=args.warmup + args.steps)
-    t = times[args.warmup:]
-    per = sum(t) / len(t)
-    value = nbytes / per / 1e9
+    reps = args.warmup + args.steps
+    # about 1.2 s per pair per step at 100000 tokens: keep the whole run near two to three minutes
+    cap = int(min(max(lens), 100000 * 150.0 / (reps * args.ref_pairs * 1.2)))
+    nbytes, times, pairs, ctx = cpu_oracle_sample(cfg, lens, args.ref_pairs, reps=reps, ctx_cap=cap)
+    per = sum(times[args.warmup:]) / args.steps
+    value = sum(nbytes[args.warmup:]) / sum(times[args.warmup:]) / 1e9
+    sample = (f"per step: {len(pairs)} of {cfg.batch * cfg.num_kv_heads} (request, KV head) pairs, each "
+              f"appending one token and attending over its first {min(ctx[b] for b, _ in pairs)} tokens "
+              f"(the oracle's cost is linear in the context)")
     line = {
         "impl": "reference", "metric": "decode_attention_hbm_gbs", "value": value, "unit": "GB/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": per * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": f"{cfg.name}: B{cfg.batch} Hq{cfg.num_q_heads}/Hkv{cfg.num_kv_heads} "
-                               f"d128 L{lens[0]} INT2 paged decode", "sample": f"{len(pairs)} (request, KV head) pairs"},
-        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": f"{len(pairs)} of {cfg.batch * cfg.num_kv_heads} (request, KV head) pairs, full context"},
+        "config": workload_config(cfg, lens),
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -203,7 +240,7 @@ def run_ours(args, cfg, rank, world, dist):
     from int2_rotated_paged_gb300 import build as kbuild
 
     kbuild.build()
-    K.oscar_set_decode_path({"mma": K.PATH_WARP_MMA, "tensor": K.PATH_TENSOR, "simt": K.PATH_SIMT}[args.path])
+    K.oscar_set_decode_path({"mma": K.PATH_WARP_MMA, "simt": K.PATH_SIMT}[args.path])
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
     stream = torch.cuda.current_stream()
@@ -265,16 +302,19 @@ def run_ours(args, cfg, rank, world, dist):
     torch.cuda.synchronize()
     lens_at = [cache.length(b) for b in range(B)]
     launches0 = K.oscar_launch_count()
+    K.oscar_kernel_timing(cache.handle, args.steps)     # events around the INT2 attention kernel
     clocks.start()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     dec = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     bytes_steps = 0
+    kbytes = 0
     t0.record(stream)
     for i in range(args.steps):
         s = args.warmup + i
         cache.append(ks[s], vs[s], [1] * B, rk)
         bytes_steps += decode_bytes([lens_at[b] + i + 1 for b in range(B)], hkv, hq)
+        kbytes += int2_kernel_bytes([lens_at[b] + i + 1 for b in range(B)], hkv, hq)
         dec[i][0].record(stream)
         cache.attend(qs[s], rk, out)
         dec[i][1].record(stream)
@@ -285,6 +325,11 @@ def run_ours(args, cfg, rank, world, dist):
     if dist is not None:
         dist.barrier()
     launches = K.oscar_launch_count() - launches0
+    kms = K.oscar_kernel_timing_read(cache.handle, args.steps)
+    K.oscar_kernel_timing(cache.handle, 0)
+    assert len(kms) == args.steps
+    k_t = sum(kms) * 1e-3 / args.steps          # seconds per INT2 attention kernel launch
+    k_bytes = kbytes / args.steps
     elapsed = t0.elapsed_time(t1) * 1e-3
     dec_t = sum(a.elapsed_time(b) for a, b in dec) * 1e-3 / args.steps
     if dist is not None:
@@ -294,7 +339,7 @@ def run_ours(args, cfg, rank, world, dist):
     per_step = elapsed / args.steps
     value = bytes_steps * world / elapsed / 1e9
     dec_bytes = bytes_steps / args.steps
-    achieved = dec_bytes / dec_t / 1e9
+    achieved = k_bytes / k_t / 1e9
     peak, peak_kind = peaks()
 
     # ---- end to end: pinned host inputs in, output out, synchronised every step
@@ -340,22 +385,23 @@ def run_ours(args, cfg, rank, world, dist):
         return
     cpu = None
     if not args.no_cpu_baseline and world == 1:
-        nb, times, pairs = cpu_oracle_sample(cfg, lens0, args.cpu_pairs)
-        cpu = {"value": nb / times[0] / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
-               "sample": f"decode attention of {len(pairs)} of {B * hkv} (request, KV head) pairs at "
-                         f"{lens0[0]} tokens, fp64, single thread"}
+        nb, times, pairs, ctx = cpu_oracle_sample(cfg, lens0, args.cpu_pairs)
+        cpu = {"value": nb[0] / times[0] / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "sample": f"one decode step (append 1 token + attend, fp64, single thread) of {len(pairs)} of "
+                         f"{B * hkv} (request, KV head) pairs at full context, {times[0]:.1f} s"}
+    kname = dict(mma="decode_mma", simt="split_simt")[args.path]
+    workload = workload_config(cfg, lens0)
     line = {
         "metric": "decode_attention_hbm_gbs", "value": value, "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_step * 1e3, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "int2+fp32", "data": "synthetic",
-        "config": {"workload": f"{cfg.name}: B{B} Hq{hq}/Hkv{hkv} d128 L{lens0[0]} INT2 paged decode step "
-                               f"(append 1 token + split-K GQA decode), {cfg.table} pages",
-                   "batch_per_gpu": B, "context": lens0[0], "l2": "inputs larger than L2 (about 2.1 GB per step vs 129 MB)"},
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": workload,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "peak_kind": peak_kind, "kernel": f"oscar_decode_attention, {args.path} path (rotate_q + bf16 split + "
-                               f"{dict(mma='decode_mma', tensor='decode_tc', simt='split_simt')[args.path]} + combine)",
-                     "traffic": profiled_traffic("decode.cu"), "bytes_per_call": dec_bytes,
-                     "ms_per_call": dec_t * 1e3},
+                     "peak_kind": peak_kind, "traffic": profiled_traffic(workload["workload"], k_bytes),
+                     "kernel": kname, "bytes_per_launch": k_bytes, "ms_per_launch": k_t * 1e3,
+                     "timing": "CUDA events recorded by the library on the launching stream around each launch",
+                     "call": {"what": f"oscar_decode_attention: rotate_q + BF16 split + {kname} + combine",
+                              "bytes": dec_bytes, "ms": dec_t * 1e3, "gbs": dec_bytes / dec_t / 1e9}},
         "append": {"prefill_tokens_per_s": tok_append / t_append, "prefill_tokens": tok_append,
                    "step_ms_excl_decode": (per_step - dec_t) * 1e3},
         "clocks": clk,

@@ -65,8 +65,10 @@ extern "C" {
 #define OSCAR_PAGE_TOKENS 64   /* INT2 tokens per page */
 #define OSCAR_GROUP 64         /* channels per quantisation group */
 #define OSCAR_MAX_GQA 16       /* largest num_q_heads / num_kv_heads */
-/* Bytes of one (page, KV head) block: K codes 64x32, K scale/min 64x8,
- * V codes 128x16 (channel-major), V scale/min 64x8. */
+/* Bytes of one (page, KV head) block: K codes 2048 (32 per token), K scale/min 64x8,
+ * V codes 2048, V scale/min 64x8.  Inside the two code regions the 2-bit codes are stored in
+ * the order the decode kernel's tensor-core fragments read them (not the logical order);
+ * oscar_read_int2 returns them in the logical order. */
 #define OSCAR_PAGE_HEAD_BYTES 5120
 
 typedef struct {
@@ -182,15 +184,27 @@ int oscar_decode_attention(oscar_cache *c, const void *q, int32_t q_dtype, const
                            void *out, int32_t out_dtype, void *workspace, size_t workspace_bytes,
                            void *stream);
 
-/* Which decode kernel oscar_decode_attention runs (process-wide; default tensor cores):
- * OSCAR_PATH_TENSOR: persistent warp-specialised kernel, tcgen05 MMAs with the dequantised
- *                    pages in tensor memory; OSCAR_PATH_SIMT: one CTA per split, CUDA-core
- *                    dot products (kept as the baseline the tensor-core path is measured
- *                    against).  Both give the same result within the parity tolerance. */
-#define OSCAR_PATH_TENSOR 0
+/* Which decode kernel oscar_decode_attention runs (process-wide; default OSCAR_PATH_WARP_MMA):
+ * OSCAR_PATH_WARP_MMA: every warp streams its own contiguous run of INT2 pages through a
+ *                      bulk-async-copy ring and runs scores and P.V on warp-level tensor-core
+ *                      MMAs (mma.sync m16n8k16, fp16 in, fp32 accumulate) with the 2-bit
+ *                      codes turned into MMA operands in registers;
+ * OSCAR_PATH_SIMT:     one CTA per split, CUDA-core dot products (the baseline the tensor-core
+ *                      path is measured against).
+ * Both give the same result within the parity tolerance.  Any other value: OSCAR_EINVAL. */
 #define OSCAR_PATH_SIMT 1
 #define OSCAR_PATH_WARP_MMA 2
 int oscar_set_decode_path(int32_t path);
+/* Per-launch device time of the INT2 attention kernel of oscar_decode_attention (the warp-MMA
+ * kernel, or the split kernel on the SIMT path), from two CUDA events recorded on the caller's
+ * stream around that one launch.  oscar_kernel_timing(c, n) creates 2n events (host-side event
+ * objects, no device memory) and records the next n decode calls on c; n = 0 stops and frees
+ * them.  oscar_kernel_timing_read waits for the recorded events, writes up to max_n durations in
+ * milliseconds (call order) to the host array ms, sets *n_out and starts a new record.  Calls
+ * beyond the n recorded ones are not timed.  Not a counterpart of anything on the OSCAR pages: a
+ * measurement aid. */
+int oscar_kernel_timing(oscar_cache *c, int32_t capacity);
+int oscar_kernel_timing_read(oscar_cache *c, float *ms, int32_t max_n, int32_t *n_out);
 /* Synchronise `stream` and report whether the last decode call that used `workspace`
  * completed normally (OSCAR_OK) or one of its bounded in-kernel waits gave up
  * (OSCAR_ETIMEOUT; its output is then undefined). */

@@ -36,10 +36,10 @@ EXPORTS = [
     "oscar_decode_attention", "oscar_build_rk_workspace_bytes", "oscar_build_rk", "oscar_read_int2",
     "oscar_read_bf16", "oscar_strerror", "oscar_last_cuda_error", "oscar_launch_count",
     "oscar_set_decode_path", "oscar_decode_status", "oscar_decode_attention_noalloc",
+    "oscar_kernel_timing", "oscar_kernel_timing_read",
 ]
 OSCAR_ESCRATCH = -8
 OSCAR_ETIMEOUT = -7
-PATH_TENSOR = 0
 PATH_SIMT = 1
 PATH_WARP_MMA = 2
 
@@ -100,6 +100,8 @@ def lib() -> ctypes.CDLL:
         "oscar_set_decode_path": (ctypes.c_int, [I32]),
         "oscar_decode_status": (ctypes.c_int, [P, SZ, P, P]),
         "oscar_decode_attention_noalloc": (ctypes.c_int, [P, P, I32, P, P, I32, P]),
+        "oscar_kernel_timing": (ctypes.c_int, [P, I32]),
+        "oscar_kernel_timing_read": (ctypes.c_int, [P, P, I32, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -246,6 +248,18 @@ def oscar_set_decode_path(path: int):
 def oscar_decode_status(cache, workspace, stream=None):
     nbytes = workspace.numel() * workspace.element_size()
     _check("oscar_decode_status", lib().oscar_decode_status(_ptr(workspace), nbytes, cache, _stream(stream)))
+
+
+def oscar_kernel_timing(cache, capacity: int):
+    _check("oscar_kernel_timing", lib().oscar_kernel_timing(cache, capacity))
+
+
+def oscar_kernel_timing_read(cache, max_n: int):
+    """Durations (ms) of the decode kernel launches recorded since oscar_kernel_timing."""
+    buf = (ctypes.c_float * max(1, max_n))()
+    got = ctypes.c_int32(0)
+    _check("oscar_kernel_timing_read", lib().oscar_kernel_timing_read(cache, buf, max_n, ctypes.byref(got)))
+    return [float(buf[i]) for i in range(got.value)]
 
 
 def oscar_launch_count() -> int:

@@ -23,7 +23,16 @@ struct oscar_cache {
     bool clear_device;                        // the device table / lengths need zeroing
     bool lens_dirty;
     int32_t g;
+    // optional per-launch timing of the decode kernel: event pairs, filled in launch order
+    std::vector<cudaEvent_t> timing_ev;
+    int32_t timing_used = 0;
 };
+
+static void free_timing(oscar_cache* c) {
+    for (cudaEvent_t e : c->timing_ev) cudaEventDestroy(e);
+    c->timing_ev.clear();
+    c->timing_used = 0;
+}
 
 namespace {
 
@@ -169,6 +178,7 @@ int oscar_cache_create(const oscar_cache_desc* d, void* pool, void* bf16, int32_
 }
 
 int oscar_cache_destroy(oscar_cache* c) {
+    if (c) free_timing(c);
     delete c;
     return OSCAR_OK;
 }
@@ -308,7 +318,7 @@ int kv_quant_append(oscar_cache* c, const void* k, const void* v, const int32_t*
 // ------------------------------------------------------------------ read path
 
 static const int kMaxSplits = 64;   // SIMT path: INT2 splits + 1 BF16 split per (request, KV head)
-static std::atomic<int> g_decode_path{0};
+static std::atomic<int> g_decode_path{OSCAR_PATH_WARP_MMA};
 
 static int pick_pps(const oscar_cache* c) {
     int64_t total = 0;
@@ -336,8 +346,18 @@ static int sm_count() {
     return cached[dev];
 }
 
+// Warps of the warp-MMA kernel: one CTA per SM (fewer when there are few pages).
+static int mma_warp_count(int64_t pages, int32_t* n_warps) {
+    const int sms = sm_count();
+    if (sms <= 0) return cuda_fail(cudaGetLastError());
+    const int per = mma_warps_per_cta();
+    const int64_t ctas = std::min<int64_t>(std::min(sms, kMaxMmaWarps / per), (pages + per - 1) / per);
+    *n_warps = (int32_t)(ctas * per);
+    return OSCAR_OK;
+}
+
 struct WsLayout {
-    size_t qrot, simt, tc, bf16, err, total;
+    size_t qrot, simt, mma, bf16, err, total;
 };
 
 static WsLayout ws_layout(const oscar_cache* c) {
@@ -346,8 +366,8 @@ static WsLayout ws_layout(const oscar_cache* c) {
     WsLayout w;
     w.qrot = 0;
     w.simt = w.qrot + (size_t)c->d.batch * c->d.num_q_heads * kD * sizeof(float);
-    w.tc = w.simt + bh * kMaxSplits * per;
-    w.bf16 = w.tc + (bh + kMaxCtas) * 2 * per;   // two token groups per (segment, CTA)
+    w.mma = w.simt + bh * kMaxSplits * per;
+    w.bf16 = w.mma + (bh + kMaxMmaWarps) * per;   // one slot per (request, KV head) run of a warp
     w.err = w.bf16 + bh * per;
     w.total = w.err + 16;
     return w;
@@ -359,7 +379,7 @@ size_t oscar_decode_workspace_bytes(const oscar_cache* c) {
 }
 
 int oscar_set_decode_path(int32_t path) {
-    if (path != OSCAR_PATH_TENSOR && path != OSCAR_PATH_SIMT && path != OSCAR_PATH_WARP_MMA) return OSCAR_EINVAL;
+    if (path != OSCAR_PATH_SIMT && path != OSCAR_PATH_WARP_MMA) return OSCAR_EINVAL;
     g_decode_path = path;
     return OSCAR_OK;
 }
@@ -407,41 +427,58 @@ int oscar_decode_attention(oscar_cache* c, const void* q, int32_t q_dtype, const
     uint8_t* ws = (uint8_t*)workspace;
     p.qrot = (float*)(ws + w.qrot);
     p.partial = (float*)(ws + w.simt);
-    p.part_tc = (float*)(ws + w.tc);
+    p.part_mma = (float*)(ws + w.mma);
     p.part_bf16 = (float*)(ws + w.bf16);
     p.err = (int32_t*)(ws + w.err);
     p.path = g_decode_path;
-    int64_t tiles = 0;
-    for (int32_t b = 0; b < c->d.batch; ++b) {
-        p.len[b] = (int32_t)c->len[b];
-        p.tile_off[b] = (int32_t)tiles;
-        tiles += (int64_t)int2_tiles(p.len[b]) * c->d.num_kv_heads;
-    }
-    p.tile_off[c->d.batch] = (int32_t)tiles;
     int64_t pages = 0;
     for (int32_t b = 0; b < c->d.batch; ++b) {
+        p.len[b] = (int32_t)c->len[b];
         p.page_off[b] = (int32_t)pages;
         pages += (int64_t)int2_pages(p.len[b]) * c->d.num_kv_heads;
     }
     p.page_off[c->d.batch] = (int32_t)pages;
     if (pages > INT32_MAX / 4) return OSCAR_ERANGE;
     p.total_pages = (int32_t)pages;
-    if (p.path == 2 && pages > 0) {
-        const int sms = sm_count();
-        if (sms <= 0) return cuda_fail(cudaGetLastError());
-        const int per = mma_warps_per_cta();
-        const int64_t ctas = std::min<int64_t>(std::min(sms, 2 * kMaxCtas / per), (pages + per - 1) / per);
-        p.n_warps = (int32_t)(ctas * per);
+    if (p.path == OSCAR_PATH_WARP_MMA && pages > 0) {
+        rc = mma_warp_count(pages, &p.n_warps);
+        if (rc != OSCAR_OK) return rc;
     }
-    if (tiles > INT32_MAX / 2) return OSCAR_ERANGE;
-    p.total_tiles = (int32_t)tiles;
-    if (p.path == 0 && tiles > 0) {
-        const int sms = sm_count();
-        if (sms <= 0) return cuda_fail(cudaGetLastError());
-        p.n_cta = (int32_t)std::min<int64_t>(std::min(sms, kMaxCtas), tiles);
+    cudaEvent_t* timing = nullptr;
+    if (c->timing_used * 2 + 1 < (int32_t)c->timing_ev.size()) {
+        timing = &c->timing_ev[2 * c->timing_used];
+        ++c->timing_used;
     }
-    cudaError_t e = launch_decode(p, S(stream));
+    cudaError_t e = launch_decode(p, S(stream), timing);
     return e == cudaSuccess ? OSCAR_OK : cuda_fail(e);
+}
+
+int oscar_kernel_timing(oscar_cache* c, int32_t capacity) {
+    if (!c || capacity < 0 || capacity > (1 << 20)) return OSCAR_EINVAL;
+    free_timing(c);
+    c->timing_ev.resize((size_t)capacity * 2, nullptr);
+    for (auto& ev : c->timing_ev) {
+        cudaError_t e = cudaEventCreate(&ev);
+        if (e != cudaSuccess) {
+            ev = nullptr;
+            free_timing(c);
+            return cuda_fail(e);
+        }
+    }
+    return OSCAR_OK;
+}
+
+int oscar_kernel_timing_read(oscar_cache* c, float* ms, int32_t max_n, int32_t* n_out) {
+    if (!c || !n_out || max_n < 0 || (max_n > 0 && !ms)) return OSCAR_EINVAL;
+    const int32_t n = std::min(max_n, c->timing_used);
+    for (int32_t i = 0; i < n; ++i) {
+        cudaError_t e = cudaEventSynchronize(c->timing_ev[2 * i + 1]);
+        if (e == cudaSuccess) e = cudaEventElapsedTime(&ms[i], c->timing_ev[2 * i], c->timing_ev[2 * i + 1]);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    *n_out = n;
+    c->timing_used = 0;
+    return OSCAR_OK;
 }
 
 // ------------------------------------------------------------------ calibration
@@ -484,14 +521,22 @@ int oscar_read_int2(const oscar_cache* c, int32_t b, int32_t h, int64_t pos0, in
             if (e != cudaSuccess) return cuda_fail(e);
             cur_page = pg;
         }
-        if (k_codes) std::memcpy(k_codes + i * 32, blk.data() + kKCodes + t * 32, 32);
         if (k_sm) std::memcpy(k_sm + i * 4, blk.data() + kKSm + t * 8, 8);
         if (v_sm) std::memcpy(v_sm + i * 4, blk.data() + kVSm + t * 8, 8);
+        // codes: from the page order back to the logical order (channel 4i + j in bits 2j of byte i)
+        if (k_codes) {
+            uint8_t* dst = k_codes + i * 32;
+            std::memset(dst, 0, 32);
+            for (int ch = 0; ch < kD; ++ch) {
+                int code = (blk[kKCodes + t * 32 + k_code_byte(ch)] >> k_code_shift(ch)) & 3;
+                dst[ch / 4] |= (uint8_t)(code << (2 * (ch % 4)));
+            }
+        }
         if (v_codes) {
             uint8_t* dst = v_codes + i * 32;
             std::memset(dst, 0, 32);
             for (int ch = 0; ch < kD; ++ch) {
-                int code = (blk[kVCodes + ch * 16 + t / 4] >> (2 * (t % 4))) & 3;
+                int code = (blk[kVCodes + v_code_byte(t, ch)] >> v_code_shift(ch)) & 3;
                 dst[ch / 4] |= (uint8_t)(code << (2 * (ch % 4)));
             }
         }
@@ -591,22 +636,19 @@ int noalloc_decode_params(oscar_cache* c, const void* q, int32_t q_dtype, const 
     if (pages > INT32_MAX / 4) return OSCAR_ERANGE;
     p.total_pages = (int32_t)pages;
     if (pages > 0) {
-        const int sms = sm_count();
-        if (sms <= 0) return cuda_fail(cudaGetLastError());
-        const int per = mma_warps_per_cta();
-        const int64_t ctas = std::min<int64_t>(std::min(sms, 2 * kMaxCtas / per), (pages + per - 1) / per);
-        p.n_warps = (int32_t)(ctas * per);
+        const int rc = mma_warp_count(pages, &p.n_warps);
+        if (rc != OSCAR_OK) return rc;
     }
     const size_t per_part = (size_t)c->g * (2 + kD) * sizeof(float);
     const size_t bh = (size_t)c->d.batch * c->d.num_kv_heads;
     const size_t o_qrot = 0;
-    const size_t o_tc = o_qrot + (((size_t)c->d.batch * c->d.num_q_heads * kD * sizeof(float) + 255) & ~(size_t)255);
-    const size_t o_bf16 = o_tc + (bh + (size_t)p.n_warps) * per_part;
+    const size_t o_mma = o_qrot + (((size_t)c->d.batch * c->d.num_q_heads * kD * sizeof(float) + 255) & ~(size_t)255);
+    const size_t o_bf16 = o_mma + (bh + (size_t)p.n_warps) * per_part;
     const size_t o_err = o_bf16 + bh * per_part;
     if (o_err + 16 > scratch_bytes) return OSCAR_ESCRATCH;
     uint8_t* ws = (uint8_t*)scratch;
     p.qrot = (float*)(ws + o_qrot);
-    p.part_tc = (float*)(ws + o_tc);
+    p.part_mma = (float*)(ws + o_mma);
     p.part_bf16 = (float*)(ws + o_bf16);
     p.err = (int32_t*)(ws + o_err);
     p.partial = nullptr;   // SIMT partials are not used on the warp-MMA path

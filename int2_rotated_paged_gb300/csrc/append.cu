@@ -106,6 +106,7 @@ __global__ void __launch_bounds__(128) quant_pages(const __grid_constant__ Appen
     float* R = smem;                   // [128][128]
     float* xs = R + kD * kD;           // [kTok][128]
     float* red = xs + kTok * kD;       // [8]
+    __shared__ uint8_t part[2][4][16];  // [K|V][warp][lane < 16]: half-packed code bytes of one token
 
     const int job = blockIdx.x;
     const int h = blockIdx.y;
@@ -124,13 +125,6 @@ __global__ void __launch_bounds__(128) quant_pages(const __grid_constant__ Appen
         float4* dst = reinterpret_cast<float4*>(R);
         for (int i = c; i < kD * kD / 4; i += 128) dst[i] = src[i];
     }
-    // this channel's row of V codes (16 bytes = 64 tokens), updated in registers
-    uint32_t vw[4];
-    {
-        const uint4 cur = *reinterpret_cast<const uint4*>(blk + kVCodes + c * 16);
-        vw[0] = cur.x; vw[1] = cur.y; vw[2] = cur.z; vw[3] = cur.w;
-    }
-
     for (int p0 = pbeg; p0 < pend; p0 += kTok) {
         const int n = min(kTok, pend - p0);
         __syncthreads();
@@ -148,40 +142,41 @@ __global__ void __launch_bounds__(128) quant_pages(const __grid_constant__ Appen
         }
         for (int t = 0; t < n; ++t) {
             const int slot = (p0 + t - kSink) % kPage;
-            // ---- K: token-major codes
-            {
-                const float y = acc[t];
-                const GroupStat g = group_minmax(y, red);
-                const Quant q = quantise(y, g, p.clip_k);
-                uint32_t word = (uint32_t)q.code << (2 * (lane & 15));
-#pragma unroll
-                for (int o = 1; o < 16; o <<= 1) word |= __shfl_xor_sync(0xffffffffu, word, o);
-                if ((lane & 15) == 0)
-                    *reinterpret_cast<uint32_t*>(blk + kKCodes + slot * 32 + (c >> 4) * 4) = word;
-                if ((c & 63) == 0)
-                    *reinterpret_cast<uint32_t*>(blk + kKSm + slot * 8 + (c >> 6) * 4) =
-                        (uint32_t)q.s16 | ((uint32_t)q.m16 << 16);
+            // ---- K (rotated) and V (unrotated): per-token asymmetric INT2 in two 64-channel groups
+            const float yk = acc[t];
+            const Quant qk = quantise(yk, group_minmax(yk, red), p.clip_k);
+            const float yv = bf16_bits_to_f32(token_src(p, b, h, 1, p0 + t)[c]);
+            const Quant qv = quantise(yv, group_minmax(yv, red), p.clip_v);
+            if ((c & 63) == 0) {
+                *reinterpret_cast<uint32_t*>(blk + kKSm + slot * 8 + (c >> 6) * 4) =
+                    (uint32_t)qk.s16 | ((uint32_t)qk.m16 << 16);
+                *reinterpret_cast<uint32_t*>(blk + kVSm + slot * 8 + (c >> 6) * 4) =
+                    (uint32_t)qv.s16 | ((uint32_t)qv.m16 << 16);
             }
-            // ---- V: unrotated, channel-major codes
-            {
-                const float y = bf16_bits_to_f32(token_src(p, b, h, 1, p0 + t)[c]);
-                const GroupStat g = group_minmax(y, red);
-                const Quant q = quantise(y, g, p.clip_v);
-                const int wi = slot >> 4;
-                const int sh = 2 * (slot & 15);
-                const uint32_t m = ~(3u << sh);
-                const uint32_t v = (uint32_t)q.code << sh;
-                if (wi == 0) vw[0] = (vw[0] & m) | v;
-                else if (wi == 1) vw[1] = (vw[1] & m) | v;
-                else if (wi == 2) vw[2] = (vw[2] & m) | v;
-                else vw[3] = (vw[3] & m) | v;
-                if ((c & 63) == 0)
-                    *reinterpret_cast<uint32_t*>(blk + kVSm + slot * 8 + (c >> 6) * 4) =
-                        (uint32_t)q.s16 | ((uint32_t)q.m16 << 16);
+            // ---- pack: every code byte holds the codes of four channels c0 + 16 r (r = 0..3) of
+            // this token, two from lanes l and l ^ 16 of one warp and two from the next warp
+            uint32_t pk = (uint32_t)qk.code << k_code_shift(c);
+            uint32_t pv = (uint32_t)qv.code << v_code_shift(c);
+            pk |= __shfl_xor_sync(0xffffffffu, pk, 16);
+            pv |= __shfl_xor_sync(0xffffffffu, pv, 16);
+            if (lane < 16) {
+                part[0][c >> 5][lane] = (uint8_t)pk;
+                part[1][c >> 5][lane] = (uint8_t)pv;
+            }
+            __syncthreads();
+            if (c < 32) {
+                // key byte c of the token row: channels 64u + 16r + 8y + 2x + e
+                const int x = c >> 3, u = (c >> 2) & 1, e = (c >> 1) & 1, y = c & 1;
+                const int l = 8 * y + 2 * x + e;
+                blk[kKCodes + slot * 32 + c] = part[0][2 * u][l] | part[0][2 * u + 1][l];
+            } else if (c < 64) {
+                // value byte of channels 64q + 16r + 8y + g
+                const int j = c - 32, q = j >> 4, g = (j >> 1) & 7, y = j & 1;
+                const int l = 8 * y + g;
+                blk[kVCodes + v_code_byte(slot, 64 * q + 8 * y + g)] = part[1][2 * q][l] | part[1][2 * q + 1][l];
             }
         }
     }
-    *reinterpret_cast<uint4*>(blk + kVCodes + c * 16) = make_uint4(vw[0], vw[1], vw[2], vw[3]);
 }
 
 // New tokens that stay in BF16 (sink, or the final window) -> their slots.

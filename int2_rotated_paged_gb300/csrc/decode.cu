@@ -99,7 +99,7 @@ __global__ void __launch_bounds__(128) split_simt(const __grid_constant__ Decode
     const int len = p.len[b];
     if (len == 0) return;
     const int nsp = int2_splits(len, p.pps);
-    // tensor-core path: this kernel only handles the BF16 split (one CTA per request and head)
+    // warp-MMA path: this kernel only handles the BF16 split (one CTA per request and head)
     const int s = p.path != 1 ? nsp : (int)blockIdx.x;
     if (s > nsp) return;
     const int w = threadIdx.x >> 5;
@@ -107,7 +107,14 @@ __global__ void __launch_bounds__(128) split_simt(const __grid_constant__ Decode
     const bool bf16_split = (s == nsp);
     const float qscale = kLog2e * rsqrtf((float)kD);
 
-    // this lane's 4 channels of every query head (rotated for INT2 tokens, plain for BF16)
+    // This lane's 4 query channels (rotated for INT2 tokens, plain for BF16) and 4 output
+    // channels.  INT2: the key channels whose codes share byte `lane` of a token row (bits 2j)
+    // and the value channels whose codes share one byte of the value region; BF16: 4 lane + j.
+    auto kch = [&](int j) {
+        return bf16_split ? 4 * lane + j
+                          : 64 * ((lane >> 2) & 1) + 16 * j + 8 * (lane & 1) + 2 * (lane >> 3) + ((lane >> 1) & 1);
+    };
+    auto och = [&](int j) { return bf16_split ? 4 * lane + j : 64 * (lane >> 4) + 16 * j + 8 * ((lane >> 3) & 1) + (lane & 7); };
     float qr[G][4];
     float qsum[G];   // sum of this lane's 4 rotated channels (for the m * sum(q) term)
     const size_t qbase = ((size_t)b * p.hkv * p.g + (size_t)h * p.g) * kD;
@@ -116,7 +123,7 @@ __global__ void __launch_bounds__(128) split_simt(const __grid_constant__ Decode
         qsum[hh] = 0.f;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            const size_t idx = qbase + (size_t)hh * kD + 4 * lane + j;
+            const size_t idx = qbase + (size_t)hh * kD + kch(j);
             qr[hh][j] = (bf16_split ? load_q(p, idx) : p.qrot[idx]) * qscale;
             qsum[hh] += qr[hh][j];
         }
@@ -133,7 +140,8 @@ __global__ void __launch_bounds__(128) split_simt(const __grid_constant__ Decode
     if (!bf16_split) {
         const int n_tok = int2_tokens(len);
         const int pg_end = min((s + 1) * p.pps, int2_pages(len));
-        const int grp = lane >> 4;   // this lane's 4 channels sit in group lane / 16
+        const int kgrp = (lane >> 2) & 1;   // group of this lane's key channels
+        const int vgrp = lane >> 4;         // group of this lane's value channels
         for (int pg = s * p.pps + w; pg < pg_end; pg += 4) {
             const int phys = p.page_table[(size_t)b * p.max_pps + pg];
             const uint8_t* blk = p.pool + ((size_t)phys * p.hkv + h) * kPageHeadBytes;
@@ -141,16 +149,16 @@ __global__ void __launch_bounds__(128) split_simt(const __grid_constant__ Decode
             for (int t4 = 0; t4 < nt; t4 += 4) {
                 float lg[4][G];
                 float vv[4][4];
-                // V: byte (channel 4*lane + j, tokens t4 .. t4+3)
+                // V: one byte per token holds this lane's 4 value channels (bits 2j)
                 uint32_t vb[4];
 #pragma unroll
-                for (int j = 0; j < 4; ++j) vb[j] = blk[kVCodes + (4 * lane + j) * 16 + (t4 >> 2)];
+                for (int i = 0; i < 4; ++i) vb[i] = blk[kVCodes + v_code_byte(t4 + i, och(0))];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const int t = t4 + i;
                     const uint32_t kb = blk[kKCodes + t * 32 + lane];
-                    const uint32_t ksm = *reinterpret_cast<const uint32_t*>(blk + kKSm + t * 8 + grp * 4);
-                    const uint32_t vsm = *reinterpret_cast<const uint32_t*>(blk + kVSm + t * 8 + grp * 4);
+                    const uint32_t ksm = *reinterpret_cast<const uint32_t*>(blk + kKSm + t * 8 + kgrp * 4);
+                    const uint32_t vsm = *reinterpret_cast<const uint32_t*>(blk + kVSm + t * 8 + vgrp * 4);
                     const float ks = h2f(ksm & 0xffff), km = h2f(ksm >> 16);
                     const float vs = h2f(vsm & 0xffff), vm = h2f(vsm >> 16);
 #pragma unroll
@@ -165,7 +173,7 @@ __global__ void __launch_bounds__(128) split_simt(const __grid_constant__ Decode
                     const bool live = t < nt;
 #pragma unroll
                     for (int j = 0; j < 4; ++j)
-                        vv[i][j] = live ? fmaf((float)((vb[j] >> (2 * i)) & 3), vs, vm) : 0.f;
+                        vv[i][j] = live ? fmaf((float)((vb[i] >> (2 * j)) & 3), vs, vm) : 0.f;
                 }
 #pragma unroll
                 for (int i = 0; i < 4; ++i)
@@ -233,7 +241,7 @@ __global__ void __launch_bounds__(128) split_simt(const __grid_constant__ Decode
 #pragma unroll
     for (int hh = 0; hh < G; ++hh)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) sm_o[w][hh][4 * lane + j] = st.o[hh][j];
+        for (int j = 0; j < 4; ++j) sm_o[w][hh][och(j)] = st.o[hh][j];
     __syncthreads();
     const int c = threadIdx.x;
     float* part = p.path != 1 ? p.part_bf16 + ((size_t)b * p.hkv + h) * p.g * (2 + kD)
@@ -258,11 +266,6 @@ __global__ void __launch_bounds__(128) split_simt(const __grid_constant__ Decode
     }
 }
 
-// CTA of the tensor-core kernel that owns tile T (CTA c owns [c T_all / C, (c + 1) T_all / C)).
-__device__ __forceinline__ int cta_of(const DecodeParams& p, int T) {
-    return (int)((((long long)T + 1) * p.n_cta - 1) / p.total_tiles);
-}
-
 __device__ __forceinline__ void merge(const float* ph, int c, float& M, float& L, float& O) {
     const float m = ph[0];
     if (m == -INFINITY) return;
@@ -285,26 +288,7 @@ __global__ void __launch_bounds__(128) combine(const __grid_constant__ DecodePar
     float res = 0.f;
     if (len > 0) {
         float M = -INFINITY, L = 0.f, O = 0.f;
-        if (p.path == 0) {
-            const int u = b * p.hkv + h;
-            merge(p.part_bf16 + ((size_t)u * p.g + hh) * (2 + kD), c, M, L, O);
-            const int tiles = int2_tiles(len);
-            if (tiles > 0) {
-                // segment of (b, h) inside CTA k: tiles [lo, hi); its token groups 0 and 1
-                // took the tiles of even and odd local index, each writing its own partial
-                const int tf = p.tile_off[b] + h * tiles;
-                const int c0 = cta_of(p, tf), c1 = cta_of(p, tf + tiles - 1);
-                for (int k = c0; k <= c1; ++k) {
-                    const int start = (int)(((long long)k * p.total_tiles) / p.n_cta);
-                    const int end = (int)(((long long)(k + 1) * p.total_tiles) / p.n_cta);
-                    const int lo = max(start, tf), hi = min(end, tf + tiles);
-                    for (int w = 0; w < 2; ++w) {
-                        if (hi - lo < 2 && ((lo - start) & 1) != w) continue;   // group w took no tile
-                        merge(p.part_tc + ((((size_t)u + k) * 2 + w) * p.g + hh) * (2 + kD), c, M, L, O);
-                    }
-                }
-            }
-        } else if (p.path == 2) {
+        if (p.path == 2) {
             const int u = b * p.hkv + h;
             merge(p.part_bf16 + ((size_t)u * p.g + hh) * (2 + kD), c, M, L, O);
             const int pages = int2_pages(len);
@@ -318,7 +302,7 @@ __global__ void __launch_bounds__(128) combine(const __grid_constant__ DecodePar
                     const long long lo = ((long long)w * p.total_pages) / p.n_warps;
                     const long long hi = ((long long)(w + 1) * p.total_pages) / p.n_warps;
                     if (lo == hi) continue;
-                    merge(p.part_tc + (((size_t)u + w) * p.g + hh) * (2 + kD), c, M, L, O);
+                    merge(p.part_mma + (((size_t)u + w) * p.g + hh) * (2 + kD), c, M, L, O);
                 }
             }
         } else {
@@ -342,13 +326,15 @@ cudaError_t launch_split(const DecodeParams& p, int max_ns, cudaStream_t s) {
 
 }  // namespace
 
-cudaError_t launch_decode(const DecodeParams& p, cudaStream_t s) {
-    int max_ns = 1;
-    if (p.path != 0)
+cudaError_t launch_decode(const DecodeParams& p, cudaStream_t s, cudaEvent_t* timing) {
+    int max_ns = 1;     // warp-MMA path: the split kernel runs only the BF16 split
+    if (p.path == 1)
         for (int b = 0; b < p.batch; ++b) max_ns = max(max_ns, int2_splits(p.len[b], p.pps) + 1);
     rotate_q<<<dim3(p.hkv, p.batch), 128, 0, s>>>(p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
+    // the INT2 attention kernel: the split kernel on the SIMT path, the warp-MMA kernel otherwise
+    if (timing && p.path == 1 && (e = cudaEventRecord(timing[0], s)) != cudaSuccess) return e;
     switch (p.g) {
         case 1: e = launch_split<1>(p, max_ns, s); break;
         case 2: e = launch_split<2>(p, max_ns, s); break;
@@ -363,12 +349,12 @@ cudaError_t launch_decode(const DecodeParams& p, cudaStream_t s) {
         default: return cudaErrorInvalidValue;
     }
     if (e != cudaSuccess) return e;
-    if (p.path == 0) {
-        e = launch_decode_tc(p, s);
-        if (e != cudaSuccess) return e;
-    } else if (p.path == 2) {
+    if (timing && p.path == 1 && (e = cudaEventRecord(timing[1], s)) != cudaSuccess) return e;
+    if (p.path == 2) {
+        if (timing && (e = cudaEventRecord(timing[0], s)) != cudaSuccess) return e;
         e = launch_decode_mma(p, s);
         if (e != cudaSuccess) return e;
+        if (timing && (e = cudaEventRecord(timing[1], s)) != cudaSuccess) return e;
     }
     combine<<<dim3(p.hkv * p.g, p.batch), 128, 0, s>>>(p);
     count_launches(3);

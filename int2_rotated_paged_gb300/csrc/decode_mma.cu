@@ -7,48 +7,56 @@
 //
 // Every warp works alone on a contiguous range of 64-token INT2 pages of the flattened
 // (request, KV head, page) list, so all warps stream the same number of bytes whatever the
-// request lengths.  A warp keeps its own four-page ring of shared-memory stages filled by
-// bulk-async copies (page-table entries fetched 32 pages ahead), and per 32-token chunk:
+// request lengths.  A warp keeps its own ring of shared-memory stages filled by bulk-async
+// copies (page-table entries fetched 32 pages ahead), and per 32-token chunk (16 for G > 8):
 //   scores   S = Q~ K^T on mma.sync.m16n8k16 (fp16 in, fp32 accumulate): A = the query,
 //            rows = head (fp16 high part) and head + 8 (fp16 low part, the rounding residue),
-//            so S_hi + S_lo carries ~22 bits of q~; B = 2-bit key codes placed in registers as
-//            fp16 subnormals code * 2^-24 (a shift and a mask per pair of codes, exact);
-//            one accumulator per 64-channel group because each group has its own scale:
-//            logit = 2^24 s_g S_g + m_g sum_{c in g} q~_c (all in log2 units);
+//            so S_hi + S_lo carries ~22 bits of q~; B = 2-bit key codes.  The page stores the
+//            codes in fragment order (k_code_byte), so a thread's codes for one token arrive
+//            in one 8-byte load, and each B register is one AND of a code word (or of the word
+//            shifted right by 8) with 0x00030003 << 2r: two fp16 subnormals code * 4^r * 2^-24,
+//            exact.  The 4^r of k-step ks (r = ks mod 4) is taken out of the query side
+//            (A = q~ * 2^(6 - 2r)).  One accumulator per 64-channel group because each group
+//            has its own scale: logit = 2^18 s_g S_g + m_g sum_{c in g} q~_c (log2 units);
 //   softmax  online, per head, with a lazily raised reference max (output rescaled only when a
 //            logit passes the reference by 2^8);
-//   output   O^T += V^T P'^T on the same MMA: A = the value codes (channel-major pages; rows =
-//            16 channels) as fp16 subnormals, B = P' = p * s_V (fp16, columns = 8 heads) taken
-//            straight from the score accumulators' register layout; the m_V term sum_t p m_V is
-//            accumulated on the CUDA cores.
-// The token order inside a page is permuted consistently between the score fragments (the
-// B columns), the probability fragments (the A columns) and the value fragments so that every
-// fragment comes from the thread's own registers.  At the end of each (request, KV head) run
-// the warp writes (reference max, sum, unnormalised output) to the split-K partial buffer.
+//   output   O^T += V^T P'^T on the same MMA: A = the value codes (rows = 16 channels), again
+//            one AND per register from a 16-byte load in fragment order (v_code_byte), with
+//            channel tile cm carrying 4^(cm mod 4) * 2^-24 (removed when the partial is
+//            written); B = P' = p * s_V (fp16, columns = 8 heads) straight from the score
+//            accumulators' register layout; the m_V term sum_t p m_V runs on the CUDA cores.
+// Tokens are in natural order everywhere: n-tile nt of a chunk holds tokens 8 nt .. 8 nt + 7,
+// and PV k-step kk takes n-tiles 2 kk (k 0..7) and 2 kk + 1 (k 8..15).  At the end of each
+// (request, KV head) run the warp writes (reference max, sum, unnormalised output) to the
+// split-K partial buffer.
 //
 // mbarrier waits are bounded; on timeout the kernel records an error word and the warp stops.
 #include <cuda_fp16.h>
 
 #include "internal.h"
-#include "tc_ptx.h"
+#include "ptx_async.h"
 
 namespace oscar {
 namespace {
 
 using namespace ptx;
 
-constexpr int kWarpsPerCta = 10;
+constexpr int kWarpsPerCta = 12;
 constexpr int kThreadsMma = kWarpsPerCta * 32;
 constexpr int kStagesPerWarp = 3;
 constexpr float kTauM = 8.0f;
 constexpr float kQScaleM = 1.4426950408889634f * 0.08838834764831845f;   // log2(e) / sqrt(128)
-constexpr float kTwo24 = 16777216.0f;
+constexpr float kTwo18 = 262144.0f;
 
 struct MmaSmem {
     uint8_t stage[kWarpsPerCta][kStagesPerWarp][kPageHeadBytes];
     uint64_t full[kWarpsPerCta][kStagesPerWarp];
-    float tsc[kWarpsPerCta][32][8];     // per-token scales of the current chunk
+    float tsc[kWarpsPerCta][32][8];     // per-token scales of the current chunk, rows in tsc_row order
 };
+
+// Row of token t (0..31 of a chunk) in the scale table: the four tokens 8 nt + 2 tig + e that the
+// four threads of a row group read together sit in consecutive 32-byte rows (no bank conflict).
+__device__ __forceinline__ int tsc_row(int t) { return (t & ~7) | ((t & 1) << 2) | ((t >> 1) & 3); }
 
 // (request, KV head, page) walk over the flattened page list
 struct PageIt {
@@ -95,8 +103,9 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
-// codes at bits 2r and 2r + 16 of w as two fp16 subnormals code * 2^-24
-__device__ __forceinline__ uint32_t code_pair(uint32_t w, int r) { return (w >> (2 * r)) & 0x00030003u; }
+// codes at bits 2r and 2r + 16 of w as two fp16 subnormals code * 4^r * 2^-24
+template <int R>
+__device__ __forceinline__ uint32_t code_pair(uint32_t w) { return w & (0x00030003u << (2 * R)); }
 
 __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
     asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
@@ -109,10 +118,6 @@ __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
     return *reinterpret_cast<const uint32_t*>(&h);
 }
 
-// token (0..31 of a 32-token chunk) behind score column col of n-tile nt (0..3)
-__device__ __forceinline__ int ptok(int nt, int col) {
-    return 16 * (nt >> 1) + 4 * (nt & 1) + (col >> 1) + 8 * (col & 1);
-}
 
 template <int G>
 __global__ void __launch_bounds__(kThreadsMma, 1) decode_mma(const __grid_constant__ DecodeParams p) {
@@ -178,7 +183,8 @@ __global__ void __launch_bounds__(kThreadsMma, 1) decode_mma(const __grid_consta
     for (int i = 0; i < n; ++i) {
         const int s = i % kStagesPerWarp;
         if (seg_start) {
-            // query fragments of this (request, KV head): channels 16 ks + tig + 4 f + 8 e
+            // query fragments of this (request, KV head): k-step ks holds channels 16 ks + 2 tig + e
+            // (+ 8 for registers 2, 3), scaled by 2^(6 - 2 (ks mod 4)) against the key codes' 4^r
 #pragma unroll
             for (int k = 0; k < MT; ++k) {
                 const int hd = g + 8 * k;
@@ -186,18 +192,23 @@ __global__ void __launch_bounds__(kThreadsMma, 1) decode_mma(const __grid_consta
                 const float* qr = p.qrot + (((size_t)it.b * p.hkv + it.h) * G + (hd < G ? hd : 0)) * kD;
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
+                    const float pw = (float)(64 >> (2 * (ks & 3)));      // 2^(6 - 2r), exact
+                    const float sc = kQScaleM * pw, inv = 1.0f / pw;
+                    const float2 q0 = *reinterpret_cast<const float2*>(qr + 16 * ks + 2 * tig);
+                    const float2 q1 = *reinterpret_cast<const float2*>(qr + 16 * ks + 2 * tig + 8);
+                    const float qv[2][2] = {{q0.x, q0.y}, {q1.x, q1.y}};
                     float hv[2][2], lv[2][2];
 #pragma unroll
                     for (int f = 0; f < 2; ++f)
 #pragma unroll
                         for (int e = 0; e < 2; ++e) {
-                            const float q = hd < G ? qr[16 * ks + tig + 4 * f + 8 * e] * kQScaleM : 0.f;
+                            const float q = hd < G ? qv[f][e] * sc : 0.f;
                             const float h = __half2float(__float2half_rn(q));
                             const float l = __half2float(__float2half_rn(q - h));
                             hv[f][e] = h;
                             lv[f][e] = l;
-                            if (ks < 4) part0 += h + l;
-                            else part1 += h + l;
+                            if (ks < 4) part0 += (h + l) * inv;
+                            else part1 += (h + l) * inv;
                         }
                     qa[k][ks][0] = pack_h2(hv[0][0], hv[0][1]);
                     qa[k][ks][1] = pack_h2(lv[0][0], lv[0][1]);
@@ -228,6 +239,8 @@ __global__ void __launch_bounds__(kThreadsMma, 1) decode_mma(const __grid_consta
 
 #pragma unroll 1
         for (int cbase = 0; cbase < kPage; cbase += CT) {
+            if (cbase >= n_live) break;                 // only the last page of a request is partial
+            const bool partial = cbase + CT > n_live;
             // ---- per-token scales of the chunk (one token per lane), staged in shared memory
             __syncwarp();
             if (lane < CT) {
@@ -236,20 +249,20 @@ __global__ void __launch_bounds__(kThreadsMma, 1) decode_mma(const __grid_consta
                 const uint2 ksm = *reinterpret_cast<const uint2*>(pg + kKSm + t * 8);
                 const uint2 vsm = *reinterpret_cast<const uint2*>(pg + kVSm + t * 8);
                 float4 a, v;
-                a.x = live ? kTwo24 * __half2float(__ushort_as_half(ksm.x & 0xffff)) : 0.f;
+                a.x = live ? kTwo18 * __half2float(__ushort_as_half(ksm.x & 0xffff)) : 0.f;
                 a.y = live ? __half2float(__ushort_as_half(ksm.x >> 16)) : 0.f;
-                a.z = live ? kTwo24 * __half2float(__ushort_as_half(ksm.y & 0xffff)) : 0.f;
+                a.z = live ? kTwo18 * __half2float(__ushort_as_half(ksm.y & 0xffff)) : 0.f;
                 a.w = live ? __half2float(__ushort_as_half(ksm.y >> 16)) : 0.f;
                 v.x = live ? __half2float(__ushort_as_half(vsm.x & 0xffff)) : 0.f;
                 v.y = live ? __half2float(__ushort_as_half(vsm.x >> 16)) : 0.f;
                 v.z = live ? __half2float(__ushort_as_half(vsm.y & 0xffff)) : 0.f;
                 v.w = live ? __half2float(__ushort_as_half(vsm.y >> 16)) : 0.f;
-                reinterpret_cast<float4*>(sm->tsc[warp][lane])[0] = a;
-                reinterpret_cast<float4*>(sm->tsc[warp][lane])[1] = v;
+                reinterpret_cast<float4*>(sm->tsc[warp][tsc_row(lane)])[0] = a;
+                reinterpret_cast<float4*>(sm->tsc[warp][tsc_row(lane)])[1] = v;
             }
             __syncwarp();
 
-            // ---- scores: acc[k][nt][group]
+            // ---- scores: acc[k][nt][group]; n-tile nt = tokens cbase + 8 nt + (0..7)
             float acc[MT][NT][2][4];
 #pragma unroll
             for (int k = 0; k < MT; ++k)
@@ -257,18 +270,28 @@ __global__ void __launch_bounds__(kThreadsMma, 1) decode_mma(const __grid_consta
                 for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
                     for (int gr = 0; gr < 2; ++gr) acc[k][nt][gr][0] = acc[k][nt][gr][1] = acc[k][nt][gr][2] = acc[k][nt][gr][3] = 0.f;
+            {
+                // this thread's 32 codes of token cbase + 8 nt + g: word u = channel group u
+                uint32_t wl[NT][2], wh[NT][2];
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-                const int tok = cbase + ptok(nt, g);
-                const uint4 w0 = *reinterpret_cast<const uint4*>(pg + kKCodes + tok * 32);
-                const uint4 w1 = *reinterpret_cast<const uint4*>(pg + kKCodes + tok * 32 + 16);
-                const uint32_t wd[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-#pragma unroll
-                for (int ks = 0; ks < 8; ++ks) {
-                    const uint32_t b0 = code_pair(wd[ks], tig), b1 = code_pair(wd[ks], tig + 4);
-#pragma unroll
-                    for (int k = 0; k < MT; ++k) mma16816(acc[k][nt][ks >> 2], qa[k][ks], b0, b1);
+                for (int nt = 0; nt < NT; ++nt) {
+                    const uint2 kw = *reinterpret_cast<const uint2*>(pg + kKCodes + (cbase + 8 * nt + g) * 32 + 8 * tig);
+                    wl[nt][0] = kw.x;
+                    wl[nt][1] = kw.y;
+                    wh[nt][0] = kw.x >> 8;
+                    wh[nt][1] = kw.y >> 8;
                 }
+                // k-step 4u + R of every n-tile; consecutive MMAs go to different accumulators
+#define OSCAR_QK_STEP(R)                                                                                    \
+    _Pragma("unroll") for (int nt = 0; nt < NT; ++nt) _Pragma("unroll") for (int u = 0; u < 2; ++u) {      \
+        const uint32_t b0 = code_pair<R>(wl[nt][u]), b1 = code_pair<R>(wh[nt][u]);                          \
+        _Pragma("unroll") for (int k = 0; k < MT; ++k) mma16816(acc[k][nt][u], qa[k][4 * u + R], b0, b1);  \
+    }
+                OSCAR_QK_STEP(0)
+                OSCAR_QK_STEP(1)
+                OSCAR_QK_STEP(2)
+                OSCAR_QK_STEP(3)
+#undef OSCAR_QK_STEP
             }
 
             // ---- logits, online softmax, P' fragments
@@ -278,17 +301,24 @@ __global__ void __launch_bounds__(kThreadsMma, 1) decode_mma(const __grid_consta
             for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
-                    const int t = ptok(nt, 2 * tig + e);
-                    const float4 a = reinterpret_cast<const float4*>(sm->tsc[warp][t])[0];
-                    const bool live = cbase + t < n_live;
+                    const float4 a = reinterpret_cast<const float4*>(sm->tsc[warp][8 * nt + 4 * e + tig])[0];
 #pragma unroll
                     for (int k = 0; k < MT; ++k) {
                         const float s0 = acc[k][nt][0][e] + acc[k][nt][0][2 + e];
                         const float s1 = acc[k][nt][1][e] + acc[k][nt][1][2 + e];
-                        const float x = fmaf(a.x, s0, fmaf(a.z, s1, fmaf(a.y, qs[k][0], a.w * qs[k][1])));
-                        lg[k][nt][e] = live ? x : -INFINITY;
+                        lg[k][nt][e] = fmaf(a.x, s0, fmaf(a.z, s1, fmaf(a.y, qs[k][0], a.w * qs[k][1])));
                     }
                 }
+            if (partial) {
+                // tokens past the request's end: probability 0 (their scales were staged as 0)
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 2; ++e)
+#pragma unroll
+                        for (int k = 0; k < MT; ++k)
+                            if (cbase + 8 * nt + 2 * tig + e >= n_live) lg[k][nt][e] = -INFINITY;
+            }
             float fown[MT];
             bool raise = false;
 #pragma unroll
@@ -324,16 +354,16 @@ __global__ void __launch_bounds__(kThreadsMma, 1) decode_mma(const __grid_consta
                     }
                 }
             }
+            // every chunk holds a live token, so mref is finite here and ex2(-inf - mref) = 0
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
                 float pv[MT][2][2];          // [head slot][group][column e]
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
-                    const int t = ptok(nt, 2 * tig + e);
-                    const float4 v = reinterpret_cast<const float4*>(sm->tsc[warp][t])[1];
+                    const float4 v = reinterpret_cast<const float4*>(sm->tsc[warp][8 * nt + 4 * e + tig])[1];
 #pragma unroll
                     for (int k = 0; k < MT; ++k) {
-                        const float pr = lg[k][nt][e] == -INFINITY ? 0.f : ex2(lg[k][nt][e] - mref[k]);
+                        const float pr = ex2(lg[k][nt][e] - mref[k]);
                         lsum[k] += pr;
                         mv[k][0] = fmaf(pr, v.y, mv[k][0]);
                         mv[k][1] = fmaf(pr, v.w, mv[k][1]);
@@ -350,19 +380,42 @@ __global__ void __launch_bounds__(kThreadsMma, 1) decode_mma(const __grid_consta
             }
 
             // ---- output^T: O[cm] += V^T[channels 16 cm + g, + 8][tokens] x P'_{group(cm)}
+            // value words of this thread for the chunk's k-steps: [channel half q][k-step][s]
+            {
+                const uint8_t* vsrc = pg + kVCodes + 1024 * (cbase >> 5) + 16 * lane;
+                uint32_t vw[2][KK][2];
 #pragma unroll
-            for (int cm = 0; cm < 8; ++cm) {
-                const int ca = 16 * cm + g;
-                const uint32_t* va = reinterpret_cast<const uint32_t*>(pg + kVCodes + ca * 16) + (cbase >> 4);
-                const uint32_t* vb = reinterpret_cast<const uint32_t*>(pg + kVCodes + (ca + 8) * 16) + (cbase >> 4);
-#pragma unroll
-                for (int kk = 0; kk < KK; ++kk) {
-                    const uint32_t wa = va[kk], wb = vb[kk];
-                    const uint32_t av[4] = {code_pair(wa, tig), code_pair(wb, tig), code_pair(wa, tig + 4),
-                                            code_pair(wb, tig + 4)};
-#pragma unroll
-                    for (int k = 0; k < MT; ++k) mma16816(o[cm][k], av, pb[cm >> 2][kk][k][0], pb[cm >> 2][kk][k][1]);
+                for (int q = 0; q < 2; ++q) {
+                    if constexpr (KK == 2) {
+                        const uint4 w4 = *reinterpret_cast<const uint4*>(vsrc + 512 * q);
+                        vw[q][0][0] = w4.x;
+                        vw[q][0][1] = w4.y;
+                        vw[q][1][0] = w4.z;
+                        vw[q][1][1] = w4.w;
+                    } else {
+                        const uint2 w2 = *reinterpret_cast<const uint2*>(vsrc + 512 * q + 8 * ((cbase >> 4) & 1));
+                        vw[q][0][0] = w2.x;
+                        vw[q][0][1] = w2.y;
+                    }
                 }
+#pragma unroll
+                for (int q = 0; q < 2; ++q)
+#pragma unroll
+                    for (int kk = 0; kk < KK; ++kk) {
+                        const uint32_t w0 = vw[q][kk][0], w1 = vw[q][kk][1];
+                        const uint32_t s0 = w0 >> 8, s1 = w1 >> 8;
+#define OSCAR_PV_STEP(R)                                                                                 \
+    {                                                                                                    \
+        const uint32_t av[4] = {code_pair<R>(w0), code_pair<R>(s0), code_pair<R>(w1), code_pair<R>(s1)}; \
+        _Pragma("unroll") for (int k = 0; k < MT; ++k)                                                   \
+            mma16816(o[4 * q + R][k], av, pb[q][kk][k][0], pb[q][kk][k][1]);                             \
+    }
+                        OSCAR_PV_STEP(0)
+                        OSCAR_PV_STEP(1)
+                        OSCAR_PV_STEP(2)
+                        OSCAR_PV_STEP(3)
+#undef OSCAR_PV_STEP
+                    }
             }
         }
 
@@ -383,7 +436,7 @@ __global__ void __launch_bounds__(kThreadsMma, 1) decode_mma(const __grid_consta
         const int b_now = it.b, h_now = it.h;
         const bool new_seg = it.next(p);
         if (last || new_seg) {
-            float* part = p.part_tc + ((size_t)(b_now * p.hkv + h_now) + gw) * G * (2 + kD);
+            float* part = p.part_mma + ((size_t)(b_now * p.hkv + h_now) + gw) * G * (2 + kD);
 #pragma unroll
             for (int k = 0; k < MT; ++k) {
                 // per-head totals over the four threads of the head's row group
@@ -409,9 +462,11 @@ __global__ void __launch_bounds__(kThreadsMma, 1) decode_mma(const __grid_consta
                         float* ph = part + (size_t)hd * (2 + kD) + 2;
 #pragma unroll
                         for (int cm = 0; cm < 8; ++cm) {
+                            // channel tile cm was accumulated at 4^(cm mod 4) * 2^-24 per code
+                            const float sc = (float)(1 << (24 - 2 * (cm & 3)));
                             const float mg = cm < 4 ? mh0 : mh1;
-                            ph[16 * cm + g] = fmaf(kTwo24, o[cm][k][e], mg);
-                            ph[16 * cm + g + 8] = fmaf(kTwo24, o[cm][k][2 + e], mg);
+                            ph[16 * cm + g] = fmaf(sc, o[cm][k][e], mg);
+                            ph[16 * cm + g + 8] = fmaf(sc, o[cm][k][2 + e], mg);
                         }
                     }
                 }

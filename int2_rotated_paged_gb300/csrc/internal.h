@@ -20,11 +20,28 @@ constexpr int kMaxBatch = 256;     // requests per call (kernel-parameter tables
 constexpr int kMaxG = 16;          // query heads per KV head
 
 // Byte layout of one (physical page, KV head) block.
-constexpr int kKCodes = 0;                      // [64 tokens][32 B], channel 4i+j -> byte i bits 2j
+constexpr int kKCodes = 0;                      // [64 tokens][32 B] key codes (k_code_byte / k_code_shift)
 constexpr int kKSm = 2048;                      // [64 tokens][s0 m0 s1 m1] fp16
-constexpr int kVCodes = 2560;                   // [128 channels][16 B], token 4i+j -> byte i bits 2j
+constexpr int kVCodes = 2560;                   // 2048 B of value codes (v_code_byte / v_code_shift)
 constexpr int kVSm = 4608;                      // [64 tokens][s0 m0 s1 m1] fp16
 constexpr int kPageHeadBytes = 5120;
+
+// Where the 2-bit codes sit inside a page.  The order is chosen for the warp-level MMA read
+// path: each thread of a warp finds the codes of its mma.m16n8k16 fragments in one 8-byte
+// (keys) or 16-byte (values) shared-memory load, and every fragment register comes out of a
+// word with one AND (codes land in fp16 subnormals code * 4^r * 2^-24, r = k_code_shift / 2).
+//   keys, token row t (32 B): channel c = 64u + 16r + 8y + 2x + e  ->  byte 8x + 4u + 2e + y, bits 2r
+//   values: token t = 32a + 16k + 8s + 2x + e, channel c = 64q + 16r + 8y + g
+//           ->  byte 1024a + 512q + 16(4g + x) + 4(2k + s) + 2e + y of the value region, bits 2r
+__host__ __device__ inline int k_code_byte(int c) {
+    return 8 * ((c >> 1) & 3) + 4 * (c >> 6) + 2 * (c & 1) + ((c >> 3) & 1);
+}
+__host__ __device__ inline int k_code_shift(int c) { return 2 * ((c >> 4) & 3); }
+__host__ __device__ inline int v_code_byte(int t, int c) {
+    return 1024 * (t >> 5) + 512 * (c >> 6) + 16 * (4 * (c & 7) + ((t >> 1) & 3)) + 4 * (2 * ((t >> 4) & 1) + ((t >> 3) & 1)) +
+           2 * (t & 1) + ((c >> 3) & 1);
+}
+__host__ __device__ inline int v_code_shift(int c) { return 2 * ((c >> 4) & 3); }
 
 // Slot of position p in the BF16 region of one (request, KV head, K|V).
 __host__ __device__ inline int bf16_slot(int64_t p) {
@@ -68,14 +85,10 @@ struct DecodeParams {
     float* qrot;           // [batch][hkv*g][128]
     float* partial;        // SIMT path: [batch][hkv][max_splits][g][2 + 128]
     int32_t len[kMaxBatch];
-    // tensor-core path
-    int32_t path;          // 0 = tensor cores, 1 = SIMT
-    int32_t n_cta;         // persistent CTAs
-    int32_t total_tiles;   // 128-token INT2 tiles over all (request, KV head)
-    float* part_tc;        // [batch * hkv + n_cta][g][2 + 128], segment id = (b * hkv + h) + cta
-    float* part_bf16;      // [batch * hkv][g][2 + 128]
+    int32_t path;          // OSCAR_PATH_SIMT (1) or OSCAR_PATH_WARP_MMA (2)
+    float* part_mma;       // warp-MMA path: [batch * hkv + n_warps][g][2 + 128], slot (b * hkv + h) + warp
+    float* part_bf16;      // [batch * hkv][g][2 + 128]: the BF16 sink / window split
     int32_t* err;          // nonzero after a bounded wait gave up
-    int32_t tile_off[kMaxBatch + 1];   // sum over earlier requests of tiles * hkv
     // warp-MMA path
     int32_t total_pages;   // INT2 pages over all (request, KV head)
     int32_t n_warps;       // warps of the warp-MMA kernel
@@ -93,16 +106,12 @@ __host__ __device__ inline int int2_splits(int len, int pps) {
     return (int2_pages(len) + pps - 1) / pps;
 }
 
-constexpr int kTileTok = 128;          // tokens per tensor-core tile (two pages)
-constexpr int kMaxCtas = 1024;
-__host__ __device__ inline int int2_tiles(int len) {
-    return (int2_tokens(len) + kTileTok - 1) / kTileTok;
-}
+constexpr int kMaxMmaWarps = 2048;     // warps of one warp-MMA launch (partial-buffer slots)
 
 // Launchers (each returns the cudaError_t of its launch).
 cudaError_t launch_append(const AppendParams& p, cudaStream_t s);
-cudaError_t launch_decode(const DecodeParams& p, cudaStream_t s);
-cudaError_t launch_decode_tc(const DecodeParams& p, cudaStream_t s);
+// timing: null, or two events recorded on `s` around the INT2 attention kernel's launch
+cudaError_t launch_decode(const DecodeParams& p, cudaStream_t s, cudaEvent_t* timing = nullptr);
 cudaError_t launch_decode_mma(const DecodeParams& p, cudaStream_t s);
 int mma_warps_per_cta();
 cudaError_t launch_build_rk(const float* q, int64_t n, int hkv, float* rk, void* ws, cudaStream_t s);

@@ -148,3 +148,19 @@ def test_append_argument_errors_before_any_launch(K):
     assert L.oscar_build_rk(FAKE[0], 10, 8, FAKE[1], FAKE[2], 8, None) == K.OSCAR_EWORKSPACE
     assert K.strerror(K.OSCAR_ENOPAGES) == "out of INT2 pages"
     L.oscar_cache_destroy(c)
+
+
+def test_decode_path_and_timing_arguments(K):
+    L = K.lib()
+    assert L.oscar_set_decode_path(0) == K.OSCAR_EINVAL          # no tensor-memory path any more
+    assert L.oscar_set_decode_path(3) == K.OSCAR_EINVAL
+    assert L.oscar_set_decode_path(K.PATH_SIMT) == 0
+    assert L.oscar_set_decode_path(K.PATH_WARP_MMA) == 0
+    c = _create(K, _desc(K))
+    assert L.oscar_kernel_timing(c, -1) == K.OSCAR_EINVAL
+    assert L.oscar_kernel_timing(c, 0) == 0                      # nothing recorded, nothing to free
+    got = ctypes.c_int32(5)
+    assert L.oscar_kernel_timing_read(c, None, 0, ctypes.byref(got)) == 0 and got.value == 0
+    assert L.oscar_kernel_timing_read(c, None, 4, ctypes.byref(got)) == K.OSCAR_EINVAL
+    assert L.oscar_kernel_timing_read(c, None, 0, None) == K.OSCAR_EINVAL
+    L.oscar_cache_destroy(c)

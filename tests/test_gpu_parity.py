@@ -26,12 +26,12 @@ def _built():
     assert torch.cuda.is_available()
 
 
-PATHS = {"mma": K.PATH_WARP_MMA, "tensor": K.PATH_TENSOR, "simt": K.PATH_SIMT}
+PATHS = {"mma": K.PATH_WARP_MMA, "simt": K.PATH_SIMT}
 
 
 @pytest.fixture(params=list(PATHS), autouse=True)
 def decode_path(request):
-    """Every test runs against each decode kernel: warp-level MMA, tcgen05 and the SIMT baseline."""
+    """Every test runs against each decode kernel: warp-level MMA and the SIMT baseline."""
     K.oscar_set_decode_path(PATHS[request.param])
     yield request.param
     K.oscar_set_decode_path(K.PATH_WARP_MMA)
