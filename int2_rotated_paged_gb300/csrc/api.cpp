@@ -347,10 +347,10 @@ static int sm_count() {
 }
 
 // Warps of the warp-MMA kernel: one CTA per SM (fewer when there are few pages).
-static int mma_warp_count(int64_t pages, int32_t* n_warps) {
+static int mma_warp_count(int32_t g, int64_t pages, int32_t* n_warps) {
     const int sms = sm_count();
     if (sms <= 0) return cuda_fail(cudaGetLastError());
-    const int per = mma_warps_per_cta();
+    const int per = mma_warps_per_cta(g);
     const int64_t ctas = std::min<int64_t>(std::min(sms, kMaxMmaWarps / per), (pages + per - 1) / per);
     *n_warps = (int32_t)(ctas * per);
     return OSCAR_OK;
@@ -441,7 +441,7 @@ int oscar_decode_attention(oscar_cache* c, const void* q, int32_t q_dtype, const
     if (pages > INT32_MAX / 4) return OSCAR_ERANGE;
     p.total_pages = (int32_t)pages;
     if (p.path == OSCAR_PATH_WARP_MMA && pages > 0) {
-        rc = mma_warp_count(pages, &p.n_warps);
+        rc = mma_warp_count(c->g, pages, &p.n_warps);
         if (rc != OSCAR_OK) return rc;
     }
     cudaEvent_t* timing = nullptr;
@@ -636,7 +636,7 @@ int noalloc_decode_params(oscar_cache* c, const void* q, int32_t q_dtype, const 
     if (pages > INT32_MAX / 4) return OSCAR_ERANGE;
     p.total_pages = (int32_t)pages;
     if (pages > 0) {
-        const int rc = mma_warp_count(pages, &p.n_warps);
+        const int rc = mma_warp_count(c->g, pages, &p.n_warps);
         if (rc != OSCAR_OK) return rc;
     }
     const size_t per_part = (size_t)c->g * (2 + kD) * sizeof(float);

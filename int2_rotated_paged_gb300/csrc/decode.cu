@@ -47,12 +47,17 @@ __global__ void __launch_bounds__(128) rotate_q(const __grid_constant__ DecodePa
     float acc[kMaxG];
 #pragma unroll
     for (int i = 0; i < kMaxG; ++i) acc[i] = 0.f;
-    const float* R = p.rk + (size_t)h * kD * kD;
-    for (int j = 0; j < kD; ++j) {
-        const float r = R[j * kD + c];
+    // column c of R_h, 32 rows at a time so that the loads are in flight together
+    const float* R = p.rk + (size_t)h * kD * kD + c;
+    for (int j0 = 0; j0 < kD; j0 += 32) {
+        float r[32];
 #pragma unroll
-        for (int i = 0; i < kMaxG; ++i)
-            if (i < p.g) acc[i] = fmaf(qs[i][j], r, acc[i]);
+        for (int j = 0; j < 32; ++j) r[j] = __ldg(R + (size_t)(j0 + j) * kD);
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+#pragma unroll
+            for (int i = 0; i < kMaxG; ++i)
+                if (i < p.g) acc[i] = fmaf(qs[i][j0 + j], r[j], acc[i]);
     }
     for (int i = 0; i < p.g; ++i) p.qrot[qbase + (size_t)i * kD + c] = acc[i];
 }

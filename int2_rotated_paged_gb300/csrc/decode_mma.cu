@@ -490,7 +490,7 @@ cudaError_t launch_mma_g(const DecodeParams& p, cudaStream_t s) {
 
 }  // namespace
 
-int mma_warps_per_cta() { return kWarpsPerCta; }
+int mma_warps_per_cta(int) { return kWarpsPerCta; }
 
 cudaError_t launch_decode_mma(const DecodeParams& p, cudaStream_t s) {
     if (p.total_pages == 0) return cudaSuccess;
