@@ -220,7 +220,7 @@ int oscar_decode_status(const void *workspace, size_t workspace_bytes, const osc
  * Scratch comes from one fixed 16 MiB array in the library's device code, which every GPU that
  * loads the library holds until the process exits.  A call whose scratch (rotated queries,
  * split-K partials, an error word) would not fit returns OSCAR_ESCRATCH and enqueues nothing;
- * e.g. 32 requests x 64 query heads (8 KV heads) need about 9.5 MiB.  It always uses the
+ * e.g. 32 requests x 64 query heads (8 KV heads) need about 10.5 MiB.  It always uses the
  * warp-level MMA decode kernel and gives the same result as oscar_decode_attention on that path.
  * It calls no cudaMalloc / cudaFree and no allocating library routine.  The first call on a
  * device looks up the array's device address (cudaGetSymbolAddress) with that device current,
