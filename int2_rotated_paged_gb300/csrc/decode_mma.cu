@@ -19,7 +19,10 @@
 //            (A = q~ * 2^(6 - 2r)).  One accumulator per 64-channel group because each group
 //            has its own scale: logit = 2^18 s_g S_g + m_g sum_{c in g} q~_c (log2 units);
 //   softmax  online, per head, with a lazily raised reference max (output rescaled only when a
-//            logit passes the reference by 2^8);
+//            logit passes the reference by 2^8); logits are formed relative to the reference
+//            and all the per-token arithmetic runs on packed fp32 pairs (f32x2 FMA / MUL / ADD:
+//            the two tokens 2 tig, 2 tig + 1 of a score column pair), which halves the FP32
+//            instructions that share the datapath with the MMAs;
 //   output   O^T += V^T P'^T on the same MMA: A = the value codes (rows = 16 channels), again
 //            one AND per register from a 16-byte load in fragment order (v_code_byte), with
 //            channel tile cm carrying 4^(cm mod 4) * 2^-24 (removed when the partial is
@@ -51,12 +54,12 @@ constexpr float kTwo18 = 262144.0f;
 struct MmaSmem {
     uint8_t stage[kWarpsPerCta][kStagesPerWarp][kPageHeadBytes];
     uint64_t full[kWarpsPerCta][kStagesPerWarp];
-    float tsc[kWarpsPerCta][32][8];     // per-token scales of the current chunk, rows in tsc_row order
+    // per-token scales of the current chunk, token pairs (2p, 2p + 1) side by side:
+    // [0] key (2^18 s0, 2^18 s0'), (m0, m0'); [1] key (2^18 s1, ...), (m1, ...); [2] value (s0, ...), (m0, ...);
+    // [3] value (s1, ...), (m1, ...)
+    float4 tsc[kWarpsPerCta][4][16];
 };
 
-// Row of token t (0..31 of a chunk) in the scale table: the four tokens 8 nt + 2 tig + e that the
-// four threads of a row group read together sit in consecutive 32-byte rows (no bank conflict).
-__device__ __forceinline__ int tsc_row(int t) { return (t & ~7) | ((t & 1) << 2) | ((t >> 1) & 3); }
 
 // (request, KV head, page) walk over the flattened page list
 struct PageIt {
@@ -173,7 +176,9 @@ __global__ void __launch_bounds__(kThreadsMma, 1) decode_mma(const __grid_consta
     // ---- per-segment state
     uint32_t qa[MT][8][4];          // query fragments (hi rows g, lo rows g + 8) per head slot and k-step
     float qs[MT][2];                // sum over each channel group of (q_hi + q_lo)
-    float mref[MT], lsum[MT], mv[MT][2];
+    float mref[MT];
+    float2 lsum[MT], mv[MT][2];     // per token parity e, summed when the partial is written
+    bool fresh = true;
     float o[8][MT][4];              // output^T accumulators: channel tile cm, head tile nh
     PageIt it;
     it.init(p, P0);
@@ -221,15 +226,15 @@ __global__ void __launch_bounds__(kThreadsMma, 1) decode_mma(const __grid_consta
                 part1 += __shfl_xor_sync(0xffffffffu, part1, 2);
                 qs[k][0] = part0;
                 qs[k][1] = part1;
-                mref[k] = -INFINITY;
-                lsum[k] = 0.f;
-                mv[k][0] = mv[k][1] = 0.f;
+                mref[k] = 0.f;
+                lsum[k] = mv[k][0] = mv[k][1] = make_float2(0.f, 0.f);
             }
 #pragma unroll
             for (int c = 0; c < 8; ++c)
 #pragma unroll
                 for (int k = 0; k < MT; ++k) o[c][k][0] = o[c][k][1] = o[c][k][2] = o[c][k][3] = 0.f;
             seg_start = false;
+            fresh = true;
         }
         const bool got = wait_full(smem_u32(&sm->full[warp][s]), (i / kStagesPerWarp) & 1, p.err);
         if (!__all_sync(0xffffffffu, got)) break;      // error word set; stop issuing, drain below
@@ -237,7 +242,7 @@ __global__ void __launch_bounds__(kThreadsMma, 1) decode_mma(const __grid_consta
         const uint8_t* pg = sm->stage[warp][s];
         const int n_live = min(kPage, int2_tokens(p.len[it.b]) - it.j * kPage);
 
-#pragma unroll 1
+#pragma unroll
         for (int cbase = 0; cbase < kPage; cbase += CT) {
             if (cbase >= n_live) break;                 // only the last page of a request is partial
             const bool partial = cbase + CT > n_live;
@@ -248,17 +253,21 @@ __global__ void __launch_bounds__(kThreadsMma, 1) decode_mma(const __grid_consta
                 const bool live = t < n_live;
                 const uint2 ksm = *reinterpret_cast<const uint2*>(pg + kKSm + t * 8);
                 const uint2 vsm = *reinterpret_cast<const uint2*>(pg + kVSm + t * 8);
-                float4 a, v;
-                a.x = live ? kTwo18 * __half2float(__ushort_as_half(ksm.x & 0xffff)) : 0.f;
-                a.y = live ? __half2float(__ushort_as_half(ksm.x >> 16)) : 0.f;
-                a.z = live ? kTwo18 * __half2float(__ushort_as_half(ksm.y & 0xffff)) : 0.f;
-                a.w = live ? __half2float(__ushort_as_half(ksm.y >> 16)) : 0.f;
-                v.x = live ? __half2float(__ushort_as_half(vsm.x & 0xffff)) : 0.f;
-                v.y = live ? __half2float(__ushort_as_half(vsm.x >> 16)) : 0.f;
-                v.z = live ? __half2float(__ushort_as_half(vsm.y & 0xffff)) : 0.f;
-                v.w = live ? __half2float(__ushort_as_half(vsm.y >> 16)) : 0.f;
-                reinterpret_cast<float4*>(sm->tsc[warp][tsc_row(lane)])[0] = a;
-                reinterpret_cast<float4*>(sm->tsc[warp][tsc_row(lane)])[1] = v;
+                const float val[8] = {
+                    live ? kTwo18 * __half2float(__ushort_as_half(ksm.x & 0xffff)) : 0.f,
+                    live ? __half2float(__ushort_as_half(ksm.x >> 16)) : 0.f,
+                    live ? kTwo18 * __half2float(__ushort_as_half(ksm.y & 0xffff)) : 0.f,
+                    live ? __half2float(__ushort_as_half(ksm.y >> 16)) : 0.f,
+                    live ? __half2float(__ushort_as_half(vsm.x & 0xffff)) : 0.f,
+                    live ? __half2float(__ushort_as_half(vsm.x >> 16)) : 0.f,
+                    live ? __half2float(__ushort_as_half(vsm.y & 0xffff)) : 0.f,
+                    live ? __half2float(__ushort_as_half(vsm.y >> 16)) : 0.f};
+                float* row = reinterpret_cast<float*>(&sm->tsc[warp][0][lane >> 1]);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    row[j * 64 + (lane & 1)] = val[2 * j];
+                    row[j * 64 + 2 + (lane & 1)] = val[2 * j + 1];
+                }
             }
             __syncwarp();
 
@@ -294,21 +303,26 @@ __global__ void __launch_bounds__(kThreadsMma, 1) decode_mma(const __grid_consta
 #undef OSCAR_QK_STEP
             }
 
-            // ---- logits, online softmax, P' fragments
+            // ---- logits (packed over the token pair e = 0, 1 of each n-tile column pair), relative
+            // to the reference max
             uint32_t pb[2][KK][MT][2];       // [group][k-step][head tile][B register]
-            float lg[MT][NT][2];
+            float2 lg[MT][NT];
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
+            for (int nt = 0; nt < NT; ++nt) {
+                const float4 k0 = sm->tsc[warp][0][4 * nt + tig], k1 = sm->tsc[warp][1][4 * nt + tig];
 #pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const float4 a = reinterpret_cast<const float4*>(sm->tsc[warp][8 * nt + 4 * e + tig])[0];
-#pragma unroll
-                    for (int k = 0; k < MT; ++k) {
-                        const float s0 = acc[k][nt][0][e] + acc[k][nt][0][2 + e];
-                        const float s1 = acc[k][nt][1][e] + acc[k][nt][1][2 + e];
-                        lg[k][nt][e] = fmaf(a.x, s0, fmaf(a.z, s1, fmaf(a.y, qs[k][0], a.w * qs[k][1])));
-                    }
+                for (int k = 0; k < MT; ++k) {
+                    const float2 s0 = __fadd2_rn(make_float2(acc[k][nt][0][0], acc[k][nt][0][1]),
+                                                 make_float2(acc[k][nt][0][2], acc[k][nt][0][3]));
+                    const float2 s1 = __fadd2_rn(make_float2(acc[k][nt][1][0], acc[k][nt][1][1]),
+                                                 make_float2(acc[k][nt][1][2], acc[k][nt][1][3]));
+                    float2 x = __ffma2_rn(make_float2(k1.z, k1.w), make_float2(qs[k][1], qs[k][1]),
+                                          make_float2(-mref[k], -mref[k]));
+                    x = __ffma2_rn(make_float2(k0.z, k0.w), make_float2(qs[k][0], qs[k][0]), x);
+                    x = __ffma2_rn(make_float2(k1.x, k1.y), s1, x);
+                    lg[k][nt] = __ffma2_rn(make_float2(k0.x, k0.y), s0, x);
                 }
+            }
             if (partial) {
                 // tokens past the request's end: probability 0 (their scales were staged as 0)
 #pragma unroll
@@ -317,28 +331,36 @@ __global__ void __launch_bounds__(kThreadsMma, 1) decode_mma(const __grid_consta
                     for (int e = 0; e < 2; ++e)
 #pragma unroll
                         for (int k = 0; k < MT; ++k)
-                            if (cbase + 8 * nt + 2 * tig + e >= n_live) lg[k][nt][e] = -INFINITY;
+                            if (cbase + 8 * nt + 2 * tig + e >= n_live) (e ? lg[k][nt].y : lg[k][nt].x) = -INFINITY;
             }
-            float fown[MT];
+            float fown[MT], cmx[MT];
             bool raise = false;
 #pragma unroll
             for (int k = 0; k < MT; ++k) {
                 float cm = -INFINITY;
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt) cm = fmaxf(cm, fmaxf(lg[k][nt][0], lg[k][nt][1]));
+                for (int nt = 0; nt < NT; ++nt) cm = fmaxf(cm, fmaxf(lg[k][nt].x, lg[k][nt].y));
                 cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, 1));
                 cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, 2));
                 fown[k] = 1.f;
-                if (cm > mref[k] + kTauM) {
-                    fown[k] = mref[k] == -INFINITY ? 0.f : ex2(mref[k] - cm);
-                    mref[k] = cm;
-                    lsum[k] *= fown[k];
-                    mv[k][0] *= fown[k];
-                    mv[k][1] *= fown[k];
+                cmx[k] = 0.f;
+                if (fresh || cm > kTauM) {
+                    fown[k] = fresh ? 0.f : ex2(-cm);
+                    mref[k] += cm;
+                    cmx[k] = cm;
+                    const float2 f2 = make_float2(fown[k], fown[k]);
+                    lsum[k] = __fmul2_rn(lsum[k], f2);
+                    mv[k][0] = __fmul2_rn(mv[k][0], f2);
+                    mv[k][1] = __fmul2_rn(mv[k][1], f2);
                     raise = true;
                 }
             }
             if (__any_sync(0xffffffffu, raise)) {
+                fresh = false;
+#pragma unroll
+                for (int k = 0; k < MT; ++k)
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) lg[k][nt] = __fadd2_rn(lg[k][nt], make_float2(-cmx[k], -cmx[k]));
                 // rare: a head's reference max went up; O^T holds heads 2 tig, 2 tig + 1 (+ 8 nh),
                 // whose factors live in the threads of rows g = head
 #pragma unroll
@@ -354,29 +376,22 @@ __global__ void __launch_bounds__(kThreadsMma, 1) decode_mma(const __grid_consta
                     }
                 }
             }
-            // every chunk holds a live token, so mref is finite here and ex2(-inf - mref) = 0
+            // probabilities (ex2(-inf) = 0) and P' = p * s_V rounded once to fp16, packed per token pair
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
-                float pv[MT][2][2];          // [head slot][group][column e]
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const float4 v = reinterpret_cast<const float4*>(sm->tsc[warp][8 * nt + 4 * e + tig])[1];
-#pragma unroll
-                    for (int k = 0; k < MT; ++k) {
-                        const float pr = ex2(lg[k][nt][e] - mref[k]);
-                        lsum[k] += pr;
-                        mv[k][0] = fmaf(pr, v.y, mv[k][0]);
-                        mv[k][1] = fmaf(pr, v.w, mv[k][1]);
-                        pv[k][0][e] = pr * v.x;
-                        pv[k][1][e] = pr * v.z;
-                    }
-                }
-                // B fragment of PV k-step nt / 2: register 0 (first n-tile of the pair), 1 (second)
+                const float4 v0 = sm->tsc[warp][2][4 * nt + tig], v1 = sm->tsc[warp][3][4 * nt + tig];
                 const int kk = nt >> 1, half = nt & 1;
 #pragma unroll
-                for (int gr = 0; gr < 2; ++gr)
-#pragma unroll
-                    for (int k = 0; k < MT; ++k) pb[gr][kk][k][half] = pack_h2(pv[k][gr][0], pv[k][gr][1]);
+                for (int k = 0; k < MT; ++k) {
+                    const float2 pr = make_float2(ex2(lg[k][nt].x), ex2(lg[k][nt].y));
+                    lsum[k] = __fadd2_rn(lsum[k], pr);
+                    mv[k][0] = __ffma2_rn(pr, make_float2(v0.z, v0.w), mv[k][0]);
+                    mv[k][1] = __ffma2_rn(pr, make_float2(v1.z, v1.w), mv[k][1]);
+                    const float2 p0 = __fmul2_rn(pr, make_float2(v0.x, v0.y));
+                    const float2 p1 = __fmul2_rn(pr, make_float2(v1.x, v1.y));
+                    pb[0][kk][k][half] = pack_h2(p0.x, p0.y);
+                    pb[1][kk][k][half] = pack_h2(p1.x, p1.y);
+                }
             }
 
             // ---- output^T: O[cm] += V^T[channels 16 cm + g, + 8][tokens] x P'_{group(cm)}
@@ -440,7 +455,7 @@ __global__ void __launch_bounds__(kThreadsMma, 1) decode_mma(const __grid_consta
 #pragma unroll
             for (int k = 0; k < MT; ++k) {
                 // per-head totals over the four threads of the head's row group
-                float l = lsum[k], m0 = mv[k][0], m1 = mv[k][1];
+                float l = lsum[k].x + lsum[k].y, m0 = mv[k][0].x + mv[k][0].y, m1 = mv[k][1].x + mv[k][1].y;
                 l += __shfl_xor_sync(0xffffffffu, l, 1);
                 l += __shfl_xor_sync(0xffffffffu, l, 2);
                 m0 += __shfl_xor_sync(0xffffffffu, m0, 1);
