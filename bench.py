@@ -406,7 +406,7 @@ def run_ours(args, cfg, rank, world, dist):
                      "peak_kind": peak_kind, "traffic": profiled_traffic(workload["workload"], k_bytes),
                      "kernel": kname, "bytes_per_launch": k_bytes, "ms_per_launch": k_t * 1e3,
                      "timing": "CUDA events recorded by the library on the launching stream around each launch",
-                     "call": {"what": f"oscar_decode_attention: rotate_q + BF16 split + {kname} + combine",
+                     "call": {"what": (f"oscar_decode_attention: prep (q rotation + BF16 sink/window attention) + {kname} + combine" if args.path == "mma" else f"oscar_decode_attention: rotate_q + {kname} (INT2 and BF16 splits) + combine"),
                               "bytes": dec_bytes, "ms": dec_t * 1e3, "gbs": dec_bytes / dec_t / 1e9}},
         "append": {"prefill_tokens_per_s": tok_append / t_append, "prefill_tokens": tok_append,
                    "step_ms_excl_decode": (per_step - dec_t) * 1e3},

@@ -104,8 +104,7 @@ __global__ void __launch_bounds__(128) split_simt(const __grid_constant__ Decode
     const int len = p.len[b];
     if (len == 0) return;
     const int nsp = int2_splits(len, p.pps);
-    // warp-MMA path: this kernel only handles the BF16 split (one CTA per request and head)
-    const int s = p.path != 1 ? nsp : (int)blockIdx.x;
+    const int s = (int)blockIdx.x;
     if (s > nsp) return;
     const int w = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -249,8 +248,7 @@ __global__ void __launch_bounds__(128) split_simt(const __grid_constant__ Decode
         for (int j = 0; j < 4; ++j) sm_o[w][hh][och(j)] = st.o[hh][j];
     __syncthreads();
     const int c = threadIdx.x;
-    float* part = p.path != 1 ? p.part_bf16 + ((size_t)b * p.hkv + h) * p.g * (2 + kD)
-                              : p.partial + (((size_t)b * p.hkv + h) * p.max_splits + s) * p.g * (2 + kD);
+    float* part = p.partial + (((size_t)b * p.hkv + h) * p.max_splits + s) * p.g * (2 + kD);
     for (int hh = 0; hh < G; ++hh) {
         float M = -INFINITY;
 #pragma unroll
@@ -294,20 +292,34 @@ __global__ void __launch_bounds__(128) combine(const __grid_constant__ DecodePar
     if (len > 0) {
         float M = -INFINITY, L = 0.f, O = 0.f;
         if (p.path == 2) {
+            // the BF16 partial and one partial per warp w0 .. w1 that owned pages of (b, h)
+            // (warps whose page range is empty wrote nothing); first the common max, then the sums
             const int u = b * p.hkv + h;
-            merge(p.part_bf16 + ((size_t)u * p.g + hh) * (2 + kD), c, M, L, O);
+            const float* pb = p.part_bf16 + ((size_t)u * p.g + hh) * (2 + kD);
             const int pages = int2_pages(len);
+            int w0 = 0, w1 = -1;
             if (pages > 0) {
-                // warps w0 .. w1 own the pages of (b, h); each wrote one partial at u + w
                 const int pf = p.page_off[b] + h * pages;
-                const int w0 = (int)((((long long)pf + 1) * p.n_warps - 1) / p.total_pages);
-                const int w1 = (int)((((long long)pf + pages) * p.n_warps - 1) / p.total_pages);
+                w0 = (int)((((long long)pf + 1) * p.n_warps - 1) / p.total_pages);
+                w1 = (int)((((long long)pf + pages) * p.n_warps - 1) / p.total_pages);
+            }
+            auto slot = [&](int w) { return p.part_mma + (((size_t)u + w) * p.g + hh) * (2 + kD); };
+            auto owns = [&](int w) {
+                return ((long long)w * p.total_pages) / p.n_warps != ((long long)(w + 1) * p.total_pages) / p.n_warps;
+            };
+            M = pb[0];
+            for (int w = w0; w <= w1; ++w)
+                if (owns(w)) M = fmaxf(M, slot(w)[0]);
+            if (M != -INFINITY) {
+                const float fb = pb[0] == -INFINITY ? 0.f : exp2f(pb[0] - M);
+                L = fb * pb[1];
+                O = fb * pb[2 + c];
                 for (int w = w0; w <= w1; ++w) {
-                    // warps whose page range is empty (more warps than pages) wrote nothing
-                    const long long lo = ((long long)w * p.total_pages) / p.n_warps;
-                    const long long hi = ((long long)(w + 1) * p.total_pages) / p.n_warps;
-                    if (lo == hi) continue;
-                    merge(p.part_mma + (((size_t)u + w) * p.g + hh) * (2 + kD), c, M, L, O);
+                    if (!owns(w)) continue;
+                    const float* ph = slot(w);
+                    const float f = exp2f(ph[0] - M);
+                    L = fmaf(f, ph[1], L);
+                    O = fmaf(f, ph[2 + c], O);
                 }
             }
         } else {
@@ -332,37 +344,43 @@ cudaError_t launch_split(const DecodeParams& p, int max_ns, cudaStream_t s) {
 }  // namespace
 
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t s, cudaEvent_t* timing) {
-    int max_ns = 1;     // warp-MMA path: the split kernel runs only the BF16 split
-    if (p.path == 1)
-        for (int b = 0; b < p.batch; ++b) max_ns = max(max_ns, int2_splits(p.len[b], p.pps) + 1);
-    rotate_q<<<dim3(p.hkv, p.batch), 128, 0, s>>>(p);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    // the INT2 attention kernel: the split kernel on the SIMT path, the warp-MMA kernel otherwise
-    if (timing && p.path == 1 && (e = cudaEventRecord(timing[0], s)) != cudaSuccess) return e;
-    switch (p.g) {
-        case 1: e = launch_split<1>(p, max_ns, s); break;
-        case 2: e = launch_split<2>(p, max_ns, s); break;
-        case 3: e = launch_split<3>(p, max_ns, s); break;
-        case 4: e = launch_split<4>(p, max_ns, s); break;
-        case 5: e = launch_split<5>(p, max_ns, s); break;
-        case 6: e = launch_split<6>(p, max_ns, s); break;
-        case 7: e = launch_split<7>(p, max_ns, s); break;
-        case 8: e = launch_split<8>(p, max_ns, s); break;
-        case 12: e = launch_split<12>(p, max_ns, s); break;
-        case 16: e = launch_split<16>(p, max_ns, s); break;
-        default: return cudaErrorInvalidValue;
-    }
-    if (e != cudaSuccess) return e;
-    if (timing && p.path == 1 && (e = cudaEventRecord(timing[1], s)) != cudaSuccess) return e;
+    cudaError_t e;
     if (p.path == 2) {
+        // warp-MMA path: prep (q rotation + BF16 part) -> INT2 attention -> combine
+        e = launch_prep(p, s);
+        if (e != cudaSuccess) return e;
+        count_launches(1);
         if (timing && (e = cudaEventRecord(timing[0], s)) != cudaSuccess) return e;
         e = launch_decode_mma(p, s);
         if (e != cudaSuccess) return e;
         if (timing && (e = cudaEventRecord(timing[1], s)) != cudaSuccess) return e;
+    } else {
+        // SIMT path: q rotation -> INT2 splits + BF16 split -> combine
+        int max_ns = 1;
+        for (int b = 0; b < p.batch; ++b) max_ns = max(max_ns, int2_splits(p.len[b], p.pps) + 1);
+        rotate_q<<<dim3(p.hkv, p.batch), 128, 0, s>>>(p);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        if (timing && (e = cudaEventRecord(timing[0], s)) != cudaSuccess) return e;
+        switch (p.g) {
+            case 1: e = launch_split<1>(p, max_ns, s); break;
+            case 2: e = launch_split<2>(p, max_ns, s); break;
+            case 3: e = launch_split<3>(p, max_ns, s); break;
+            case 4: e = launch_split<4>(p, max_ns, s); break;
+            case 5: e = launch_split<5>(p, max_ns, s); break;
+            case 6: e = launch_split<6>(p, max_ns, s); break;
+            case 7: e = launch_split<7>(p, max_ns, s); break;
+            case 8: e = launch_split<8>(p, max_ns, s); break;
+            case 12: e = launch_split<12>(p, max_ns, s); break;
+            case 16: e = launch_split<16>(p, max_ns, s); break;
+            default: return cudaErrorInvalidValue;
+        }
+        if (e != cudaSuccess) return e;
+        if (timing && (e = cudaEventRecord(timing[1], s)) != cudaSuccess) return e;
+        count_launches(2);
     }
     combine<<<dim3(p.hkv * p.g, p.batch), 128, 0, s>>>(p);
-    count_launches(3);
+    count_launches(1);
     return cudaGetLastError();
 }
 

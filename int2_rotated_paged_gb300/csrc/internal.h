@@ -113,6 +113,7 @@ cudaError_t launch_append(const AppendParams& p, cudaStream_t s);
 // timing: null, or two events recorded on `s` around the INT2 attention kernel's launch
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t s, cudaEvent_t* timing = nullptr);
 cudaError_t launch_decode_mma(const DecodeParams& p, cudaStream_t s);
+cudaError_t launch_prep(const DecodeParams& p, cudaStream_t s);
 int mma_warps_per_cta(int g);   // warps per CTA of the warp-MMA kernel for G query heads per KV head
 cudaError_t launch_build_rk(const float* q, int64_t n, int hkv, float* rk, void* ws, cudaStream_t s);
 size_t build_rk_ws_bytes(int hkv);

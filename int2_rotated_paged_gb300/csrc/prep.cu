@@ -1,0 +1,244 @@
+// prep.cu -- first kernel of a warp-MMA decode call, one CTA per (KV head, request):
+//   1. q~ = q . R_K for the G query heads of the KV head (fp32), the queries of the INT2 pages
+//      (axbrief.com OSCAR page, section "attention-statistics rotation + Triton kernels": scores
+//      against rotated keys; rotating q once equals inverse-rotating every key, R_K orthogonal);
+//   2. attention of the plain queries over the request's BF16 sink + window tokens (same page,
+//      section "OSCAR release": BF16 sink and recent window), written as one split-K partial
+//      (reference max, sum, unnormalised output) that combine merges with the INT2 partials.
+// Scores of the BF16 part run on mma.sync m16n8k16 with bf16 operands: A = the query (rows: the
+// bf16 high part of 8 heads, then their bf16 low parts, ~16 bits in all), B = key rows read
+// straight from the BF16 region (a fragment register is two adjacent channels of one token).
+// The online softmax runs per warp over 8-slot tiles; P.V runs on the CUDA cores with the
+// probabilities shared through shared memory (lane = 4 output channels).
+// All softmax arithmetic is in base 2 (logits pre-scaled by log2(e) / sqrt(128)).
+#include <cuda_bf16.h>
+
+#include "internal.h"
+
+namespace oscar {
+namespace {
+
+constexpr int kPrepWarps = 4;
+constexpr float kQScaleP = 1.4426950408889634f * 0.08838834764831845f;   // log2(e) / sqrt(128)
+
+__device__ __forceinline__ float bf16_to_f(uint16_t b) { return __uint_as_float(((uint32_t)b) << 16); }
+
+__device__ __forceinline__ float load_query(const DecodeParams& p, size_t idx) {
+    return p.q_dtype == 0 ? reinterpret_cast<const float*>(p.q)[idx]
+                          : bf16_to_f(reinterpret_cast<const uint16_t*>(p.q)[idx]);
+}
+
+__device__ __forceinline__ float exp2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// slot s of the BF16 region holds a token of a request of length len
+__device__ __forceinline__ bool slot_live(int s, int n_sink, int n_win) {
+    return s < n_sink || (s >= kSink && s < kSink + n_win);
+}
+
+template <int G>
+__global__ void __launch_bounds__(32 * kPrepWarps) prep(const __grid_constant__ DecodeParams p) {
+    constexpr int MT = (G + 7) / 8;                  // head tiles (rows g and g + 8 of each)
+    __shared__ float qs[G][kD];                      // plain queries
+    __shared__ float ps[kPrepWarps][8][8 * MT];      // probabilities of a warp's current tile [slot][head]
+    __shared__ float fs[kPrepWarps][8 * MT];         // rescale of a warp's running sums [head]
+    __shared__ float mw[kPrepWarps][G], lw[kPrepWarps][G];
+    __shared__ float ow[kPrepWarps][G][kD];
+    const int h = blockIdx.x, b = blockIdx.y, c = threadIdx.x;
+    const int warp = c >> 5, lane = c & 31, g = lane >> 2, tig = lane & 3;
+    if (b == 0 && h == 0 && c == 0 && p.err) *p.err = 0;
+    const size_t qbase = ((size_t)b * p.hkv + h) * G * kD;
+    for (int i = 0; i < G; ++i) qs[i][c] = load_query(p, qbase + (size_t)i * kD + c);
+    __syncthreads();
+
+    // ---- q~[i][c] = sum_j q[i][j] R_h[j][c]: column c of R_h, 32 rows in flight
+    {
+        float acc[G];
+#pragma unroll
+        for (int i = 0; i < G; ++i) acc[i] = 0.f;
+        const float* R = p.rk + (size_t)h * kD * kD + c;
+        for (int j0 = 0; j0 < kD; j0 += 32) {
+            float r[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) r[j] = __ldg(R + (size_t)(j0 + j) * kD);
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+#pragma unroll
+                for (int i = 0; i < G; ++i) acc[i] = fmaf(qs[i][j0 + j], r[j], acc[i]);
+        }
+#pragma unroll
+        for (int i = 0; i < G; ++i) p.qrot[qbase + (size_t)i * kD + c] = acc[i];
+    }
+
+    // ---- BF16 sink + window
+    const int len = p.len[b];
+    const int n_sink = min(len, kSink), n_win = min(kWindow, max(0, len - kSink));
+    // query fragments: k-step ks holds channels 16 ks + 2 tig + e (+ 8 for registers 2, 3);
+    // row g = bf16 high part of head g + 8 k, row g + 8 = its bf16 low part
+    uint32_t qa[MT][8][4];
+#pragma unroll
+    for (int k = 0; k < MT; ++k) {
+        const int hd = g + 8 * k;
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+            float hv[2][2], lv[2][2];
+#pragma unroll
+            for (int f = 0; f < 2; ++f)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const float x = hd < G ? qs[hd][16 * ks + 8 * f + 2 * tig + e] * kQScaleP : 0.f;
+                    const float hi = __bfloat162float(__float2bfloat16_rn(x));
+                    hv[f][e] = hi;
+                    lv[f][e] = x - hi;
+                }
+            qa[k][ks][0] = pack_bf16x2(hv[0][0], hv[0][1]);
+            qa[k][ks][1] = pack_bf16x2(lv[0][0], lv[0][1]);
+            qa[k][ks][2] = pack_bf16x2(hv[1][0], hv[1][1]);
+            qa[k][ks][3] = pack_bf16x2(lv[1][0], lv[1][1]);
+        }
+    }
+    const uint16_t* kb = p.bf16 + (((size_t)b * p.hkv + h) * 2 + 0) * kSlots * kD;
+    const uint16_t* vb = p.bf16 + (((size_t)b * p.hkv + h) * 2 + 1) * kSlots * kD;
+    float m[MT], lpart[MT];           // running max of head g + 8 k (base 2); this thread's part of the sum
+#pragma unroll
+    for (int k = 0; k < MT; ++k) m[k] = -INFINITY, lpart[k] = 0.f;
+    float o[G][4];                    // unnormalised output, channels 4 lane .. 4 lane + 3
+#pragma unroll
+    for (int i = 0; i < G; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+
+    for (int nt = warp; nt < kSlots / 8; nt += kPrepWarps) {
+        const int s0 = 8 * nt;
+        if (!slot_live(s0, n_sink, n_win) && !slot_live(s0 + 7, n_sink, n_win)) continue;   // whole tile empty
+        // scores of slots s0 .. s0 + 7
+        float acc[MT][4];
+#pragma unroll
+        for (int k = 0; k < MT; ++k) acc[k][0] = acc[k][1] = acc[k][2] = acc[k][3] = 0.f;
+        const uint16_t* krow = kb + (size_t)(s0 + g) * kD + 2 * tig;
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+            const uint32_t b0 = *reinterpret_cast<const uint32_t*>(krow + 16 * ks);
+            const uint32_t b1 = *reinterpret_cast<const uint32_t*>(krow + 16 * ks + 8);
+#pragma unroll
+            for (int k = 0; k < MT; ++k) mma_bf16(acc[k], qa[k][ks], b0, b1);
+        }
+        // online softmax of head g + 8 k over the tile's slots 2 tig, 2 tig + 1
+#pragma unroll
+        for (int k = 0; k < MT; ++k) {
+            float x[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e)
+                x[e] = slot_live(s0 + 2 * tig + e, n_sink, n_win) ? acc[k][e] + acc[k][2 + e] : -INFINITY;
+            float cm = fmaxf(x[0], x[1]);
+            cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, 1));
+            cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, 2));
+            const float mn = fmaxf(m[k], cm);            // finite: the tile holds a live slot
+            const float f = m[k] == -INFINITY ? 0.f : exp2_approx(m[k] - mn);
+            const float p0 = exp2_approx(x[0] - mn), p1 = exp2_approx(x[1] - mn);
+            lpart[k] = fmaf(lpart[k], f, p0 + p1);
+            m[k] = mn;
+            ps[warp][2 * tig][g + 8 * k] = p0;
+            ps[warp][2 * tig + 1][g + 8 * k] = p1;
+            if (tig == 0) fs[warp][g + 8 * k] = f;
+        }
+        __syncwarp();
+        // P.V on the CUDA cores
+        float v[8][4];
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+            const bool live = slot_live(s0 + t, n_sink, n_win);
+            const uint2 w = *reinterpret_cast<const uint2*>(vb + (size_t)(s0 + t) * kD + 4 * lane);
+            v[t][0] = live ? bf16_to_f(w.x & 0xffff) : 0.f;     // dead slots may hold anything
+            v[t][1] = live ? bf16_to_f(w.x >> 16) : 0.f;
+            v[t][2] = live ? bf16_to_f(w.y & 0xffff) : 0.f;
+            v[t][3] = live ? bf16_to_f(w.y >> 16) : 0.f;
+        }
+#pragma unroll
+        for (int i = 0; i < G; ++i) {
+            const float f = fs[warp][i];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) o[i][j] *= f;
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+                const float pr = ps[warp][t][i];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) o[i][j] = fmaf(pr, v[t][j], o[i][j]);
+            }
+        }
+        __syncwarp();
+    }
+
+    // ---- merge the warps' partials and write this request's BF16 partial
+#pragma unroll
+    for (int k = 0; k < MT; ++k) {
+        float l = lpart[k];
+        l += __shfl_xor_sync(0xffffffffu, l, 1);
+        l += __shfl_xor_sync(0xffffffffu, l, 2);
+        const int hd = g + 8 * k;
+        if (tig == 0 && hd < G) {
+            mw[warp][hd] = m[k];
+            lw[warp][hd] = l;
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < G; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) ow[warp][i][4 * lane + j] = o[i][j];
+    __syncthreads();
+    float* part = p.part_bf16 + ((size_t)b * p.hkv + h) * G * (2 + kD);
+    for (int i = 0; i < G; ++i) {
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kPrepWarps; ++w) M = fmaxf(M, mw[w][i]);
+        float L = 0.f, O = 0.f;
+        if (M != -INFINITY) {
+#pragma unroll
+            for (int w = 0; w < kPrepWarps; ++w) {
+                const float f = mw[w][i] == -INFINITY ? 0.f : exp2_approx(mw[w][i] - M);
+                L = fmaf(f, lw[w][i], L);
+                O = fmaf(f, ow[w][i][c], O);
+            }
+        }
+        float* ph = part + (size_t)i * (2 + kD);
+        if (c == 0) {
+            ph[0] = M;
+            ph[1] = L;
+        }
+        ph[2 + c] = O;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_prep(const DecodeParams& p, cudaStream_t s) {
+    const dim3 grid(p.hkv, p.batch);
+    switch (p.g) {
+        case 1: prep<1><<<grid, 32 * kPrepWarps, 0, s>>>(p); break;
+        case 2: prep<2><<<grid, 32 * kPrepWarps, 0, s>>>(p); break;
+        case 3: prep<3><<<grid, 32 * kPrepWarps, 0, s>>>(p); break;
+        case 4: prep<4><<<grid, 32 * kPrepWarps, 0, s>>>(p); break;
+        case 5: prep<5><<<grid, 32 * kPrepWarps, 0, s>>>(p); break;
+        case 6: prep<6><<<grid, 32 * kPrepWarps, 0, s>>>(p); break;
+        case 7: prep<7><<<grid, 32 * kPrepWarps, 0, s>>>(p); break;
+        case 8: prep<8><<<grid, 32 * kPrepWarps, 0, s>>>(p); break;
+        case 12: prep<12><<<grid, 32 * kPrepWarps, 0, s>>>(p); break;
+        case 16: prep<16><<<grid, 32 * kPrepWarps, 0, s>>>(p); break;
+        default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace oscar
