@@ -291,38 +291,7 @@ __global__ void __launch_bounds__(128) combine(const __grid_constant__ DecodePar
     float res = 0.f;
     if (len > 0) {
         float M = -INFINITY, L = 0.f, O = 0.f;
-        if (p.path == 2) {
-            // the BF16 partial and one partial per warp w0 .. w1 that owned pages of (b, h)
-            // (warps whose page range is empty wrote nothing); first the common max, then the sums
-            const int u = b * p.hkv + h;
-            const float* pb = p.part_bf16 + ((size_t)u * p.g + hh) * (2 + kD);
-            const int pages = int2_pages(len);
-            int w0 = 0, w1 = -1;
-            if (pages > 0) {
-                const int pf = p.page_off[b] + h * pages;
-                w0 = (int)((((long long)pf + 1) * p.n_warps - 1) / p.total_pages);
-                w1 = (int)((((long long)pf + pages) * p.n_warps - 1) / p.total_pages);
-            }
-            auto slot = [&](int w) { return p.part_mma + (((size_t)u + w) * p.g + hh) * (2 + kD); };
-            auto owns = [&](int w) {
-                return ((long long)w * p.total_pages) / p.n_warps != ((long long)(w + 1) * p.total_pages) / p.n_warps;
-            };
-            M = pb[0];
-            for (int w = w0; w <= w1; ++w)
-                if (owns(w)) M = fmaxf(M, slot(w)[0]);
-            if (M != -INFINITY) {
-                const float fb = pb[0] == -INFINITY ? 0.f : exp2f(pb[0] - M);
-                L = fb * pb[1];
-                O = fb * pb[2 + c];
-                for (int w = w0; w <= w1; ++w) {
-                    if (!owns(w)) continue;
-                    const float* ph = slot(w);
-                    const float f = exp2f(ph[0] - M);
-                    L = fmaf(f, ph[1], L);
-                    O = fmaf(f, ph[2 + c], O);
-                }
-            }
-        } else {
+        {
             const int ns = int2_splits(len, p.pps) + 1;
             const float* part = p.partial + ((size_t)b * p.hkv + h) * p.max_splits * p.g * (2 + kD);
             for (int s = 0; s < ns; ++s) merge(part + ((size_t)s * p.g + hh) * (2 + kD), c, M, L, O);
@@ -333,6 +302,63 @@ __global__ void __launch_bounds__(128) combine(const __grid_constant__ DecodePar
         reinterpret_cast<float*>(p.out)[oidx] = res;
     else
         reinterpret_cast<__nv_bfloat16*>(p.out)[oidx] = __float2bfloat16_rn(res);
+}
+
+// Warp-MMA path: one CTA per (KV head, request), one warp per query head, lane = channels
+// 2 lane, 2 lane + 1, 64 + 2 lane, 65 + 2 lane.  Merges the BF16 partial with the partials of the
+// warps w0 .. w1 that owned pages of (b, h) (warps whose page range is empty wrote nothing):
+// first the common max, then the sums, so that every load is independent of the merge.
+__global__ void __launch_bounds__(32 * kMaxG) combine_mma(const __grid_constant__ DecodeParams p) {
+    const int h = blockIdx.x, b = blockIdx.y;
+    const int hh = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int len = p.len[b];
+    const int u = b * p.hkv + h;
+    float2 r0 = make_float2(0.f, 0.f), r1 = r0;
+    if (len > 0) {
+        const float* pb = p.part_bf16 + ((size_t)u * p.g + hh) * (2 + kD);
+        const int pages = int2_pages(len);
+        int w0 = 0, w1 = -1;
+        if (pages > 0) {
+            const int pf = p.page_off[b] + h * pages;
+            w0 = (int)((((long long)pf + 1) * p.n_warps - 1) / p.total_pages);
+            w1 = (int)((((long long)pf + pages) * p.n_warps - 1) / p.total_pages);
+        }
+        auto slot = [&](int w) { return p.part_mma + (((size_t)u + w) * p.g + hh) * (2 + kD); };
+        auto owns = [&](int w) {
+            return ((long long)w * p.total_pages) / p.n_warps != ((long long)(w + 1) * p.total_pages) / p.n_warps;
+        };
+        float M = pb[0];
+        for (int w = w0; w <= w1; ++w)
+            if (owns(w)) M = fmaxf(M, slot(w)[0]);
+        float L = 0.f;
+        float2 o0 = r0, o1 = r0;
+        auto add = [&](const float* ph, float f) {
+            L = fmaf(f, ph[1], L);
+            const float2 a = *reinterpret_cast<const float2*>(ph + 2 + 2 * lane);
+            const float2 c = *reinterpret_cast<const float2*>(ph + 2 + 64 + 2 * lane);
+            o0 = make_float2(fmaf(f, a.x, o0.x), fmaf(f, a.y, o0.y));
+            o1 = make_float2(fmaf(f, c.x, o1.x), fmaf(f, c.y, o1.y));
+        };
+        if (pb[0] != -INFINITY) add(pb, exp2f(pb[0] - M));
+        for (int w = w0; w <= w1; ++w)
+            if (owns(w)) {
+                const float* ph = slot(w);
+                add(ph, exp2f(ph[0] - M));
+            }
+        const float inv = 1.f / L;
+        r0 = make_float2(o0.x * inv, o0.y * inv);
+        r1 = make_float2(o1.x * inv, o1.y * inv);
+    }
+    const size_t obase = ((size_t)b * p.hkv * p.g + (size_t)h * p.g + hh) * kD;
+    if (p.out_dtype == 0) {
+        float* out = reinterpret_cast<float*>(p.out) + obase;
+        *reinterpret_cast<float2*>(out + 2 * lane) = r0;
+        *reinterpret_cast<float2*>(out + 64 + 2 * lane) = r1;
+    } else {
+        __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out) + obase;
+        *reinterpret_cast<__nv_bfloat162*>(out + 2 * lane) = __floats2bfloat162_rn(r0.x, r0.y);
+        *reinterpret_cast<__nv_bfloat162*>(out + 64 + 2 * lane) = __floats2bfloat162_rn(r1.x, r1.y);
+    }
 }
 
 template <int G>
@@ -379,7 +405,10 @@ cudaError_t launch_decode(const DecodeParams& p, cudaStream_t s, cudaEvent_t* ti
         if (timing && (e = cudaEventRecord(timing[1], s)) != cudaSuccess) return e;
         count_launches(2);
     }
-    combine<<<dim3(p.hkv * p.g, p.batch), 128, 0, s>>>(p);
+    if (p.path == 2)
+        combine_mma<<<dim3(p.hkv, p.batch), 32 * p.g, 0, s>>>(p);
+    else
+        combine<<<dim3(p.hkv * p.g, p.batch), 128, 0, s>>>(p);
     count_launches(1);
     return cudaGetLastError();
 }

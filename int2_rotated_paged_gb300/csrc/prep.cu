@@ -18,7 +18,8 @@
 namespace oscar {
 namespace {
 
-constexpr int kPrepWarps = 4;
+// warps per CTA: 8 when the per-warp output partials of G <= 8 heads fit in static shared memory
+__host__ __device__ constexpr int prep_warps(int G) { return G <= 8 ? 8 : 4; }
 constexpr float kQScaleP = 1.4426950408889634f * 0.08838834764831845f;   // log2(e) / sqrt(128)
 
 __device__ __forceinline__ float bf16_to_f(uint16_t b) { return __uint_as_float(((uint32_t)b) << 16); }
@@ -51,8 +52,10 @@ __device__ __forceinline__ bool slot_live(int s, int n_sink, int n_win) {
 }
 
 template <int G>
-__global__ void __launch_bounds__(32 * kPrepWarps) prep(const __grid_constant__ DecodeParams p) {
+__global__ void __launch_bounds__(32 * prep_warps(G)) prep(const __grid_constant__ DecodeParams p) {
     constexpr int MT = (G + 7) / 8;                  // head tiles (rows g and g + 8 of each)
+    constexpr int kPrepWarps = prep_warps(G);
+    constexpr int NT = 32 * kPrepWarps;
     __shared__ float qs[G][kD];                      // plain queries
     __shared__ float ps[kPrepWarps][8][8 * MT];      // probabilities of a warp's current tile [slot][head]
     __shared__ float fs[kPrepWarps][8 * MT];         // rescale of a warp's running sums [head]
@@ -62,15 +65,18 @@ __global__ void __launch_bounds__(32 * kPrepWarps) prep(const __grid_constant__ 
     const int warp = c >> 5, lane = c & 31, g = lane >> 2, tig = lane & 3;
     if (b == 0 && h == 0 && c == 0 && p.err) *p.err = 0;
     const size_t qbase = ((size_t)b * p.hkv + h) * G * kD;
-    for (int i = 0; i < G; ++i) qs[i][c] = load_query(p, qbase + (size_t)i * kD + c);
+    for (int i = c; i < G * kD; i += NT) qs[i / kD][i % kD] = load_query(p, qbase + (size_t)i);
     __syncthreads();
 
-    // ---- q~[i][c] = sum_j q[i][j] R_h[j][c]: column c of R_h, 32 rows in flight
+    // ---- q~[i][col] = sum_j q[i][j] R_h[j][col]: column col of R_h, 32 rows in flight; with
+    // 8 warps the two halves of the CTA take alternate heads
     {
-        float acc[G];
+        constexpr int HS = kPrepWarps / 4;           // head stride
+        const int col = c & (kD - 1), h0 = c / kD;
+        float acc[(G + HS - 1) / HS];
 #pragma unroll
-        for (int i = 0; i < G; ++i) acc[i] = 0.f;
-        const float* R = p.rk + (size_t)h * kD * kD + c;
+        for (int i = 0; i < (G + HS - 1) / HS; ++i) acc[i] = 0.f;
+        const float* R = p.rk + (size_t)h * kD * kD + col;
         for (int j0 = 0; j0 < kD; j0 += 32) {
             float r[32];
 #pragma unroll
@@ -78,10 +84,12 @@ __global__ void __launch_bounds__(32 * kPrepWarps) prep(const __grid_constant__ 
 #pragma unroll
             for (int j = 0; j < 32; ++j)
 #pragma unroll
-                for (int i = 0; i < G; ++i) acc[i] = fmaf(qs[i][j0 + j], r[j], acc[i]);
+                for (int i = 0; i < (G + HS - 1) / HS; ++i)
+                    if (h0 + HS * i < G) acc[i] = fmaf(qs[h0 + HS * i][j0 + j], r[j], acc[i]);
         }
 #pragma unroll
-        for (int i = 0; i < G; ++i) p.qrot[qbase + (size_t)i * kD + c] = acc[i];
+        for (int i = 0; i < (G + HS - 1) / HS; ++i)
+            if (h0 + HS * i < G) p.qrot[qbase + (size_t)(h0 + HS * i) * kD + col] = acc[i];
     }
 
     // ---- BF16 sink + window
@@ -199,7 +207,8 @@ __global__ void __launch_bounds__(32 * kPrepWarps) prep(const __grid_constant__ 
         for (int j = 0; j < 4; ++j) ow[warp][i][4 * lane + j] = o[i][j];
     __syncthreads();
     float* part = p.part_bf16 + ((size_t)b * p.hkv + h) * G * (2 + kD);
-    for (int i = 0; i < G; ++i) {
+    const int col = c & (kD - 1);
+    for (int i = c / kD; i < G; i += NT / kD) {
         float M = -INFINITY;
 #pragma unroll
         for (int w = 0; w < kPrepWarps; ++w) M = fmaxf(M, mw[w][i]);
@@ -209,15 +218,15 @@ __global__ void __launch_bounds__(32 * kPrepWarps) prep(const __grid_constant__ 
             for (int w = 0; w < kPrepWarps; ++w) {
                 const float f = mw[w][i] == -INFINITY ? 0.f : exp2_approx(mw[w][i] - M);
                 L = fmaf(f, lw[w][i], L);
-                O = fmaf(f, ow[w][i][c], O);
+                O = fmaf(f, ow[w][i][col], O);
             }
         }
         float* ph = part + (size_t)i * (2 + kD);
-        if (c == 0) {
+        if (col == 0) {
             ph[0] = M;
             ph[1] = L;
         }
-        ph[2 + c] = O;
+        ph[2 + col] = O;
     }
 }
 
@@ -226,16 +235,16 @@ __global__ void __launch_bounds__(32 * kPrepWarps) prep(const __grid_constant__ 
 cudaError_t launch_prep(const DecodeParams& p, cudaStream_t s) {
     const dim3 grid(p.hkv, p.batch);
     switch (p.g) {
-        case 1: prep<1><<<grid, 32 * kPrepWarps, 0, s>>>(p); break;
-        case 2: prep<2><<<grid, 32 * kPrepWarps, 0, s>>>(p); break;
-        case 3: prep<3><<<grid, 32 * kPrepWarps, 0, s>>>(p); break;
-        case 4: prep<4><<<grid, 32 * kPrepWarps, 0, s>>>(p); break;
-        case 5: prep<5><<<grid, 32 * kPrepWarps, 0, s>>>(p); break;
-        case 6: prep<6><<<grid, 32 * kPrepWarps, 0, s>>>(p); break;
-        case 7: prep<7><<<grid, 32 * kPrepWarps, 0, s>>>(p); break;
-        case 8: prep<8><<<grid, 32 * kPrepWarps, 0, s>>>(p); break;
-        case 12: prep<12><<<grid, 32 * kPrepWarps, 0, s>>>(p); break;
-        case 16: prep<16><<<grid, 32 * kPrepWarps, 0, s>>>(p); break;
+        case 1: prep<1><<<grid, 32 * prep_warps(1), 0, s>>>(p); break;
+        case 2: prep<2><<<grid, 32 * prep_warps(2), 0, s>>>(p); break;
+        case 3: prep<3><<<grid, 32 * prep_warps(3), 0, s>>>(p); break;
+        case 4: prep<4><<<grid, 32 * prep_warps(4), 0, s>>>(p); break;
+        case 5: prep<5><<<grid, 32 * prep_warps(5), 0, s>>>(p); break;
+        case 6: prep<6><<<grid, 32 * prep_warps(6), 0, s>>>(p); break;
+        case 7: prep<7><<<grid, 32 * prep_warps(7), 0, s>>>(p); break;
+        case 8: prep<8><<<grid, 32 * prep_warps(8), 0, s>>>(p); break;
+        case 12: prep<12><<<grid, 32 * prep_warps(12), 0, s>>>(p); break;
+        case 16: prep<16><<<grid, 32 * prep_warps(16), 0, s>>>(p); break;
         default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();
