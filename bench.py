@@ -48,10 +48,10 @@ def parse():
     ap.add_argument("--config", default="qwen3_32b")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--cpu-pairs", type=int, default=12,
-                    help="(request, KV head) pairs the CPU oracle times for cpu_baseline (about 1 s each)")
-    ap.add_argument("--ref-pairs", type=int, default=3,
-                    help="(request, KV head) pairs per step of --impl reference")
+    ap.add_argument("--cpu-pairs", type=int, default=max(8, os.cpu_count() or 1),
+                    help="(request, KV head) pairs the CPU oracle times for cpu_baseline (about 1 s each, one per host core)")
+    ap.add_argument("--ref-pairs", type=int, default=max(3, os.cpu_count() or 1),
+                    help="(request, KV head) pairs per step of --impl reference (one per host core)")
     ap.add_argument("--batch", type=int, default=0,
                     help="requests per GPU (0 = the workload's batch); smaller values are for profiling")
     ap.add_argument("--path", default="mma", choices=["mma", "simt"],
@@ -176,36 +176,46 @@ def max_over_ranks(x: float, dist, device) -> float:
 
 # ------------------------------------------------------------------ CPU oracle timing
 
-def cpu_oracle_sample(cfg, lens, n_pairs: int, reps: int = 1, ctx_cap: int = 0):
+def cpu_oracle_sample(cfg, lens, n_pairs: int, reps: int = 1, ctx_cap: int = 0, threads: int = 1):
     """Time the CPU oracle on (request, KV head) pairs of the workload.  Each rep is one decode
     step of every sampled pair: append one token (window insert and, past 320 tokens, the
     eviction of one token to INT2), then attend.  ctx_cap > 0 keeps only the first ctx_cap
-    tokens of each sampled request.  Returns (bytes per rep, seconds per rep, pairs, context)."""
+    tokens of each sampled request.  The pairs run on `threads` host threads (the oracle's C
+    calls release the interpreter lock).  Returns (bytes per rep, seconds per rep, pairs, context)."""
+    from concurrent.futures import ThreadPoolExecutor
     import oracle
     import synth
     oracle.build()
     pairs = [(b % cfg.batch, (3 * b + 1) % cfg.num_kv_heads) for b in range(n_pairs)]
     ctx = [min(lens[b], ctx_cap) if ctx_cap > 0 else lens[b] for b in range(len(lens))]
-    caches = []
-    for (b, h) in pairs:
+
+    def make(bh):
+        b, h = bh
         rk = oracle.build_rk(synth.calibration_queries(cfg.seed, h, 4096).numpy())[0]
         oc = oracle.OracleCache(rk)
         oc.append(synth.bf16_bits(synth.keys(cfg.seed, b, h, 0, ctx[b] + reps)),
                   synth.bf16_bits(synth.values(cfg.seed, b, h, 0, ctx[b] + reps)))
-        caches.append((b, h, oc))
+        return (b, h, oc)
+
     g = cfg.group
     times, nbytes = [], []
-    for r in range(reps):
-        q = synth.queries(cfg.seed, r, cfg.batch, cfg.num_q_heads, cfg.num_kv_heads, dtype=cfg.q_dtype).numpy()
-        steps = [(oc, synth.bf16_bits(synth.keys(cfg.seed, b, h, ctx[b] + r, 1)),
-                  synth.bf16_bits(synth.values(cfg.seed, b, h, ctx[b] + r, 1)), q[b, h * g:(h + 1) * g])
-                 for (b, h, oc) in caches]
-        t0 = time.perf_counter()
-        for (oc, k1, v1, qb) in steps:
-            oc.append(k1, v1)
-            oc.attend(qb)
-        times.append(time.perf_counter() - t0)
-        nbytes.append(sum(decode_bytes([ctx[b] + r + 1], 1, g) for (b, h, _) in caches))
+    with ThreadPoolExecutor(max_workers=threads) as pool:
+        caches = list(pool.map(make, pairs))
+        for r in range(reps):
+            q = synth.queries(cfg.seed, r, cfg.batch, cfg.num_q_heads, cfg.num_kv_heads, dtype=cfg.q_dtype).numpy()
+            steps = [(oc, synth.bf16_bits(synth.keys(cfg.seed, b, h, ctx[b] + r, 1)),
+                      synth.bf16_bits(synth.values(cfg.seed, b, h, ctx[b] + r, 1)), q[b, h * g:(h + 1) * g])
+                     for (b, h, oc) in caches]
+
+            def run(st):
+                oc, k1, v1, qb = st
+                oc.append(k1, v1)
+                oc.attend(qb)
+
+            t0 = time.perf_counter()
+            list(pool.map(run, steps))
+            times.append(time.perf_counter() - t0)
+            nbytes.append(sum(decode_bytes([ctx[b] + r + 1], 1, g) for (b, h, _) in caches))
     return nbytes, times, pairs, ctx
 
 
@@ -224,9 +234,12 @@ def run_reference(args, cfg, rank, world):
         return
     lens = [int(x) for x in cfg.ctx]
     reps = args.warmup + args.steps
-    # about 1.2 s per pair per step at 100000 tokens: keep the whole run near two to three minutes
-    cap = int(min(max(lens), 100000 * 150.0 / (reps * args.ref_pairs * 1.2)))
-    nbytes, times, pairs, ctx = cpu_oracle_sample(cfg, lens, args.ref_pairs, reps=reps, ctx_cap=cap)
+    threads = max(1, min(args.ref_pairs, os.cpu_count() or 1))
+    # about 1.2 s per pair per step at 100000 tokens on one core: keep the whole run near two to
+    # three minutes
+    waves = -(-args.ref_pairs // threads)
+    cap = int(min(max(lens), 100000 * 150.0 / (reps * waves * 1.2)))
+    nbytes, times, pairs, ctx = cpu_oracle_sample(cfg, lens, args.ref_pairs, reps=reps, ctx_cap=cap, threads=threads)
     per = sum(times[args.warmup:]) / args.steps
     value = sum(nbytes[args.warmup:]) / sum(times[args.warmup:]) / 1e9
     sample = (f"per step: {len(pairs)} of {cfg.batch * cfg.num_kv_heads} (request, KV head) pairs, each "
@@ -237,7 +250,7 @@ def run_reference(args, cfg, rank, world):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": per * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": workload_config(cfg, lens),
-        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -391,10 +404,12 @@ def run_ours(args, cfg, rank, world, dist):
         return
     cpu = None
     if not args.no_cpu_baseline and world == 1:
-        nb, times, pairs, ctx = cpu_oracle_sample(cfg, lens0, args.cpu_pairs, reps=3)
-        cpu = {"value": sum(nb) / sum(times) / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
-               "sample": f"three decode steps (append 1 token + attend, fp64, single thread) of {len(pairs)} of "
-                         f"{B * hkv} (request, KV head) pairs at full context, {sum(times):.1f} s of CPU time"}
+        threads = max(1, min(args.cpu_pairs, os.cpu_count() or 1))
+        nb, times, pairs, ctx = cpu_oracle_sample(cfg, lens0, args.cpu_pairs, reps=2, threads=threads)
+        cpu = {"value": sum(nb) / sum(times) / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
+               "sample": f"two decode steps (append 1 token + attend, fp64) of {len(pairs)} of {B * hkv} "
+                         f"(request, KV head) pairs at full context on {threads} threads, "
+                         f"{sum(times):.1f} s wall ({sum(times) * threads:.0f} thread-s)"}
     kname = dict(mma="decode_mma", simt="split_simt")[args.path]
     workload = workload_config(cfg, lens0)
     line = {
