@@ -1,7 +1,8 @@
 // append.cu -- write path of the INT2 rotated paged KV cache (sm_103a).
 //
 // kv_quant_append runs two kernels on the caller's stream:
-//   1. quant_pages: one CTA per (touched INT2 page, KV head).  Every position that
+//   1. quant_few (decode steps: at most 8 tokens per page and head) or quant_pages (prefill,
+//      chunked appends): one CTA per (touched INT2 page, KV head).  Every position that
 //      leaves the BF16 window in this call (or goes straight to INT2 in a long
 //      append) is rotated (keys only), clipped, quantised to asymmetric INT2 in two
 //      64-channel groups and packed into its page (axbrief.com OSCAR page, section
@@ -25,8 +26,6 @@
 
 namespace oscar {
 namespace {
-
-constexpr int kTok = 8;   // tokens rotated together per thread (independent FMA chains)
 
 __device__ __forceinline__ float bf16_bits_to_f32(uint16_t b) {
     return __uint_as_float(((uint32_t)b) << 16);
@@ -55,28 +54,6 @@ struct GroupStat {
     float mn, mx;
 };
 
-// Min and max over the 64 channels of each group (threads 0..63 and 64..127).
-__device__ __forceinline__ GroupStat group_minmax(float y, float* red) {
-    float mn = y, mx = y;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    }
-    const int w = threadIdx.x >> 5;
-    if ((threadIdx.x & 31) == 0) {
-        red[2 * w] = mn;
-        red[2 * w + 1] = mx;
-    }
-    __syncthreads();
-    const int w0 = w & ~1;
-    GroupStat g;
-    g.mn = fminf(red[2 * w0], red[2 * w0 + 2]);
-    g.mx = fmaxf(red[2 * w0 + 1], red[2 * w0 + 3]);
-    __syncthreads();
-    return g;
-}
-
 struct Quant {
     int code;
     uint16_t s16, m16;
@@ -101,11 +78,37 @@ __device__ __forceinline__ Quant quantise(float y, GroupStat g, float clip) {
     return q;
 }
 
-__global__ void __launch_bounds__(128) quant_pages(const __grid_constant__ AppendParams p) {
+// Min and max over the 64 channels of each group (threads 0..63 and 64..127).
+__device__ __forceinline__ GroupStat group_minmax(float y, float* red) {
+    float mn = y, mx = y;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    }
+    const int w = threadIdx.x >> 5;
+    if ((threadIdx.x & 31) == 0) {
+        red[2 * w] = mn;
+        red[2 * w + 1] = mx;
+    }
+    __syncthreads();
+    const int w0 = w & ~1;
+    GroupStat g;
+    g.mn = fminf(red[2 * w0], red[2 * w0 + 2]);
+    g.mx = fmaxf(red[2 * w0 + 1], red[2 * w0 + 3]);
+    __syncthreads();
+    return g;
+}
+
+constexpr int kFew = 8;   // tokens per (page, KV head) up to which quant_few is used
+
+// Appends that quantise at most kFew tokens per (page, KV head) -- every decode step: thread =
+// channel, the kFew tokens' rotation chains side by side, block-wide group min / max per token.
+__global__ void __launch_bounds__(128) quant_few(const __grid_constant__ AppendParams p) {
     extern __shared__ __align__(16) float smem[];
     float* R = smem;                   // [128][128]
-    float* xs = R + kD * kD;           // [kTok][128]
-    float* red = xs + kTok * kD;       // [8]
+    float* xs = R + kD * kD;           // [kFew][128]
+    float* red = xs + kFew * kD;       // [8]
     __shared__ uint8_t part[2][4][16];  // [K|V][warp][lane < 16]: half-packed code bytes of one token
 
     const int job = blockIdx.x;
@@ -125,20 +128,20 @@ __global__ void __launch_bounds__(128) quant_pages(const __grid_constant__ Appen
         float4* dst = reinterpret_cast<float4*>(R);
         for (int i = c; i < kD * kD / 4; i += 128) dst[i] = src[i];
     }
-    for (int p0 = pbeg; p0 < pend; p0 += kTok) {
-        const int n = min(kTok, pend - p0);
+    for (int p0 = pbeg; p0 < pend; p0 += kFew) {
+        const int n = min(kFew, pend - p0);
         __syncthreads();
         for (int t = 0; t < n; ++t) xs[t * kD + c] = bf16_bits_to_f32(token_src(p, b, h, 0, p0 + t)[c]);
         __syncthreads();
         // keys: k~_c = sum_j x_j R[j][c], serial fused multiply-add in ascending j
-        float acc[kTok];
+        float acc[kFew];
 #pragma unroll
-        for (int t = 0; t < kTok; ++t) acc[t] = 0.0f;
+        for (int t = 0; t < kFew; ++t) acc[t] = 0.0f;
 #pragma unroll 4
         for (int j = 0; j < kD; ++j) {
             const float rj = R[j * kD + c];
 #pragma unroll
-            for (int t = 0; t < kTok; ++t) acc[t] = __fmaf_rn(xs[t * kD + j], rj, acc[t]);
+            for (int t = 0; t < kFew; ++t) acc[t] = __fmaf_rn(xs[t * kD + j], rj, acc[t]);
         }
         for (int t = 0; t < n; ++t) {
             const int slot = (p0 + t - kSink) % kPage;
@@ -179,6 +182,164 @@ __global__ void __launch_bounds__(128) quant_pages(const __grid_constant__ Appen
     }
 }
 
+// OR of a value over the four lanes whose channel blocks differ in bits 1..2 (code position r)
+__device__ __forceinline__ uint32_t or_over_r(uint32_t v) {
+    v |= __shfl_xor_sync(0xffffffffu, v, 2);
+    v |= __shfl_xor_sync(0xffffffffu, v, 4);
+    return v;
+}
+
+// min / max over the 8 lanes of a 64-channel group (channel blocks differing in bits 0..2)
+__device__ __forceinline__ GroupStat group_minmax8(float mn, float mx) {
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) {
+        mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    }
+    GroupStat g;
+    g.mn = mn;
+    g.mx = mx;
+    return g;
+}
+
+// One CTA per (touched INT2 page, KV head), 128 threads.  Thread t owns the 8 page slots
+// 8 (t >> 4) .. + 7 and the 8 channels 8 cb .. 8 cb + 7 (cb = t & 15), so a token's 128 channels sit
+// in 16 lanes of one warp and a 64-channel group in 8 of them: group min / max and the packing of
+// four codes per byte are warp shuffles, with no block-wide barrier per token.
+// Keys: the 64 x 128 tile times R_K with each output the serial fmaf chain over ascending j
+// (the bit-exact contract), 8 tokens x 8 channels of independent chains per thread.
+__global__ void __launch_bounds__(128) quant_pages(const __grid_constant__ AppendParams p) {
+    extern __shared__ __align__(16) float smem[];
+    float* R = smem;                   // [128][128]
+    float* xt = R + kD * kD;           // [128][64]: key inputs, channel-major (xt[j][slot])
+
+    const int job = blockIdx.x;
+    const int h = blockIdx.y;
+    const int t = threadIdx.x;
+    const int tb = t >> 4, cb = t & 15;
+    const int b = find_request(p, job);
+    const AppendReq& r = p.req[b];
+    const int pg = r.page0 + (job - r.job0);
+    const int page_pos = kSink + pg * kPage;                 // position of slot 0
+    const int pbeg = max(r.e0, page_pos);
+    const int pend = min(r.e1, page_pos + kPage);
+    const int sbeg = pbeg - page_pos, send = pend - page_pos;
+    const int phys = p.page_table[(size_t)b * p.max_pps + pg];
+    uint8_t* blk = p.pool + ((size_t)phys * p.hkv + h) * kPageHeadBytes;
+
+    {   // stage R_K of this head and the key inputs of the page's live slots
+        const float4* src = reinterpret_cast<const float4*>(p.rk + (size_t)h * kD * kD);
+        float4* dst = reinterpret_cast<float4*>(R);
+        for (int i = t; i < kD * kD / 4; i += 128) dst[i] = src[i];
+        // 16-byte loads (8 channels of one token), 8 independent ones per thread
+        for (int idx = t; idx < kPage * (kD / 8); idx += 128) {
+            const int s = idx >> 4, ch = 8 * (idx & 15);
+            if (s < sbeg || s >= send) continue;
+            const uint4 w = *reinterpret_cast<const uint4*>(token_src(p, b, h, 0, page_pos + s) + ch);
+            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                xt[(ch + 2 * k) * kPage + s] = bf16_bits_to_f32((uint16_t)(ws[k] & 0xffff));
+                xt[(ch + 2 * k + 1) * kPage + s] = bf16_bits_to_f32((uint16_t)(ws[k] >> 16));
+            }
+        }
+    }
+    __syncthreads();
+
+    // ---- keys: k~[s][c] = sum_j x[s][j] R[j][c], serial fused multiply-add in ascending j
+    float acc[8][8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) acc[i][jj] = 0.0f;
+#pragma unroll 2
+    for (int j = 0; j < kD; ++j) {
+        const float4 x0 = *reinterpret_cast<const float4*>(xt + j * kPage + 8 * tb);
+        const float4 x1 = *reinterpret_cast<const float4*>(xt + j * kPage + 8 * tb + 4);
+        const float4 r0 = *reinterpret_cast<const float4*>(R + j * kD + 8 * cb);
+        const float4 r1 = *reinterpret_cast<const float4*>(R + j * kD + 8 * cb + 4);
+        const float xv[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+        const float rv[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj) acc[i][jj] = __fmaf_rn(xv[i], rv[jj], acc[i][jj]);
+    }
+
+    // ---- per token: clip, quantise, pack.  Channel c = 8 cb + jj: group u = cb >> 3, code
+    // position r = (cb >> 1) & 3, y = cb & 1 in both page orders.
+    const int u = cb >> 3, rpos = (cb >> 1) & 3, y = cb & 1;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int s = 8 * tb + i;
+        const bool live = s >= sbeg && s < send;      // same for the 16 lanes of the token
+        if (!__any_sync(0xffffffffu, live)) continue;
+        // keys
+        {
+            float mn = acc[i][0], mx = acc[i][0];
+#pragma unroll
+            for (int jj = 1; jj < 8; ++jj) mn = fminf(mn, acc[i][jj]), mx = fmaxf(mx, acc[i][jj]);
+            const GroupStat gs = group_minmax8(mn, mx);
+            uint32_t bytes[8];                         // byte 8x + 4u + 2e + y of the row, x = jj >> 1, e = jj & 1
+            uint16_t s16 = 0, m16 = 0;
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj) {
+                const Quant q = quantise(acc[i][jj], gs, p.clip_k);
+                bytes[jj] = (uint32_t)q.code << (2 * rpos);
+                s16 = q.s16;
+                m16 = q.m16;
+            }
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj) bytes[jj] = or_over_r(bytes[jj]);
+            if (live && rpos == 0) {
+#pragma unroll
+                for (int jj = 0; jj < 8; ++jj)
+                    blk[kKCodes + s * 32 + 8 * (jj >> 1) + 4 * u + 2 * (jj & 1) + y] = (uint8_t)bytes[jj];
+            }
+            if (live && (cb & 7) == 0)
+                *reinterpret_cast<uint32_t*>(blk + kKSm + s * 8 + u * 4) = (uint32_t)s16 | ((uint32_t)m16 << 16);
+        }
+        // values (unrotated): this thread's 8 channels of the token, straight from the source row
+        {
+            float vx[8];
+            if (live) {
+                const uint4 w = *reinterpret_cast<const uint4*>(token_src(p, b, h, 1, page_pos + s) + 8 * cb);
+                const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    vx[2 * k] = bf16_bits_to_f32((uint16_t)(ws[k] & 0xffff));
+                    vx[2 * k + 1] = bf16_bits_to_f32((uint16_t)(ws[k] >> 16));
+                }
+            } else {
+#pragma unroll
+                for (int k = 0; k < 8; ++k) vx[k] = 0.f;
+            }
+            float mn = vx[0], mx = vx[0];
+#pragma unroll
+            for (int jj = 1; jj < 8; ++jj) mn = fminf(mn, vx[jj]), mx = fmaxf(mx, vx[jj]);
+            const GroupStat gs = group_minmax8(mn, mx);
+            uint32_t bytes[8];
+            uint16_t s16 = 0, m16 = 0;
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj) {
+                const Quant q = quantise(vx[jj], gs, p.clip_v);
+                bytes[jj] = (uint32_t)q.code << (2 * rpos);
+                s16 = q.s16;
+                m16 = q.m16;
+            }
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj) bytes[jj] = or_over_r(bytes[jj]);
+            // channel 8 cb + jj = 64 u + 16 rpos + 8 y + jj: the byte of (slot s, channel 64 u + 8 y + jj)
+            if (live && rpos == 0) {
+#pragma unroll
+                for (int jj = 0; jj < 8; ++jj) blk[kVCodes + v_code_byte(s, 64 * u + 8 * y + jj)] = (uint8_t)bytes[jj];
+            }
+            if (live && (cb & 7) == 0)
+                *reinterpret_cast<uint32_t*>(blk + kVSm + s * 8 + u * 4) = (uint32_t)s16 | ((uint32_t)m16 << 16);
+        }
+    }
+}
+
 // New tokens that stay in BF16 (sink, or the final window) -> their slots.
 __global__ void __launch_bounds__(128) insert_bf16(const __grid_constant__ AppendParams p) {
     const int b = blockIdx.x;
@@ -203,17 +364,28 @@ __global__ void __launch_bounds__(128) insert_bf16(const __grid_constant__ Appen
 }  // namespace
 
 cudaError_t launch_append(const AppendParams& p, cudaStream_t s) {
-    const size_t smem = (size_t)(kD * kD + kTok * kD + 8) * sizeof(float);
+    // at most kFew tokens leave the window per request (every decode step): the per-channel
+    // kernel; otherwise (prefill, chunked appends) the tiled one
+    int most = 0;
+    for (int b = 0; b < p.batch; ++b) most = max(most, p.req[b].e1 - p.req[b].e0);
+    const bool few = most <= kFew;
+    const size_t smem_tiled = (size_t)(kD * kD + kD * kPage) * sizeof(float);
+    const size_t smem_few = (size_t)(kD * kD + kFew * kD + 8) * sizeof(float);
     static bool attr_set = false;
     if (!attr_set) {
         cudaError_t e = cudaFuncSetAttribute(quant_pages, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)smem);
+                                             (int)smem_tiled);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(quant_few, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_few);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
     int n = 0;
     if (p.n_jobs > 0) {
-        quant_pages<<<dim3(p.n_jobs, p.hkv), 128, smem, s>>>(p);
+        if (few)
+            quant_few<<<dim3(p.n_jobs, p.hkv), 128, smem_few, s>>>(p);
+        else
+            quant_pages<<<dim3(p.n_jobs, p.hkv), 128, smem_tiled, s>>>(p);
         ++n;
     }
     insert_bf16<<<dim3(p.batch, p.hkv), 128, 0, s>>>(p);
