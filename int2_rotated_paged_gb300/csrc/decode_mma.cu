@@ -44,20 +44,22 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kWarpsPerCta = 12;
-constexpr int kThreadsMma = kWarpsPerCta * 32;
+// warps per CTA: 12 (168 registers each) when one m-tile holds the G heads (G <= 8); 8 (255
+// registers) for two head tiles, whose query fragments and accumulators need twice the registers
+__host__ __device__ constexpr int warps_for(int G) { return G <= 8 ? 12 : 8; }
 constexpr int kStagesPerWarp = 3;
 constexpr float kTauM = 8.0f;
 constexpr float kQScaleM = 1.4426950408889634f * 0.08838834764831845f;   // log2(e) / sqrt(128)
 constexpr float kTwo18 = 262144.0f;
 
+template <int W>
 struct MmaSmem {
-    uint8_t stage[kWarpsPerCta][kStagesPerWarp][kPageHeadBytes];
-    uint64_t full[kWarpsPerCta][kStagesPerWarp];
+    uint8_t stage[W][kStagesPerWarp][kPageHeadBytes];
+    uint64_t full[W][kStagesPerWarp];
     // per-token scales of the current chunk, token pairs (2p, 2p + 1) side by side:
     // [0] key (2^18 s0, 2^18 s0'), (m0, m0'); [1] key (2^18 s1, ...), (m1, ...); [2] value (s0, ...), (m0, ...);
     // [3] value (s1, ...), (m1, ...)
-    float4 tsc[kWarpsPerCta][4][16];
+    float4 tsc[W][4][16];
 };
 
 
@@ -123,17 +125,18 @@ __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
 
 
 template <int G>
-__global__ void __launch_bounds__(kThreadsMma, 1) decode_mma(const __grid_constant__ DecodeParams p) {
+__global__ void __launch_bounds__(32 * warps_for(G), 1) decode_mma(const __grid_constant__ DecodeParams p) {
     constexpr int MT = (G + 7) / 8;              // heads per thread (rows g and g + 8 of each m-tile)
     constexpr int NT = MT == 1 ? 4 : 2;          // score n-tiles per chunk (8 tokens each)
     constexpr int CT = 8 * NT;                   // tokens per chunk
     constexpr int KK = NT / 2;                   // PV k-steps per chunk
     extern __shared__ __align__(128) uint8_t smem_raw[];
-    MmaSmem* sm = reinterpret_cast<MmaSmem*>(smem_raw);
+    constexpr int W = warps_for(G);
+    MmaSmem<W>* sm = reinterpret_cast<MmaSmem<W>*>(smem_raw);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int g = lane >> 2, tig = lane & 3;
-    const int gw = blockIdx.x * kWarpsPerCta + warp;
+    const int gw = blockIdx.x * W + warp;
     const int P0 = (int)(((long long)gw * p.total_pages) / p.n_warps);
     const int P1 = (int)(((long long)(gw + 1) * p.total_pages) / p.n_warps);
     const int n = P1 - P0;
@@ -496,16 +499,17 @@ __global__ void __launch_bounds__(kThreadsMma, 1) decode_mma(const __grid_consta
 
 template <int G>
 cudaError_t launch_mma_g(const DecodeParams& p, cudaStream_t s) {
-    const int smem = (int)sizeof(MmaSmem);
+    constexpr int W = warps_for(G);
+    const int smem = (int)sizeof(MmaSmem<W>);
     cudaError_t e = cudaFuncSetAttribute(decode_mma<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    decode_mma<G><<<p.n_warps / kWarpsPerCta, kThreadsMma, smem, s>>>(p);
+    decode_mma<G><<<p.n_warps / W, 32 * W, smem, s>>>(p);
     return cudaGetLastError();
 }
 
 }  // namespace
 
-int mma_warps_per_cta(int) { return kWarpsPerCta; }
+int mma_warps_per_cta(int g) { return warps_for(g); }
 
 cudaError_t launch_decode_mma(const DecodeParams& p, cudaStream_t s) {
     if (p.total_pages == 0) return cudaSuccess;
