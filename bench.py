@@ -405,9 +405,9 @@ def run_ours(args, cfg, rank, world, dist):
     cpu = None
     if not args.no_cpu_baseline and world == 1:
         threads = max(1, min(args.cpu_pairs, os.cpu_count() or 1))
-        nb, times, pairs, ctx = cpu_oracle_sample(cfg, lens0, args.cpu_pairs, reps=2, threads=threads)
+        nb, times, pairs, ctx = cpu_oracle_sample(cfg, lens0, args.cpu_pairs, reps=4, threads=threads)
         cpu = {"value": sum(nb) / sum(times) / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
-               "sample": f"two decode steps (append 1 token + attend, fp64) of {len(pairs)} of {B * hkv} "
+               "sample": f"four decode steps (append 1 token + attend, fp64) of {len(pairs)} of {B * hkv} "
                          f"(request, KV head) pairs at full context on {threads} threads, "
                          f"{sum(times):.1f} s wall ({sum(times) * threads:.0f} thread-s)"}
     kname = dict(mma="decode_mma", simt="split_simt")[args.path]
