@@ -8,7 +8,10 @@
 // Every warp works alone on a contiguous range of 64-token INT2 pages of the flattened
 // (request, KV head, page) list, so all warps stream the same number of bytes whatever the
 // request lengths.  A warp keeps its own ring of shared-memory stages filled by bulk-async
-// copies (page-table entries fetched 32 pages ahead), and per 32-token chunk (16 for G > 8):
+// copies (page-table entries fetched 32 pages ahead).  Per page it converts the fp16 per-token
+// scales and minima once into an fp32 table in shared memory, then runs 32-token chunks (16 for
+// G > 8); every page but the last of a request takes a copy of the chunk loop without tail checks,
+// so the chunks of a page form one straight-line block the compiler can interleave.  Per chunk:
 //   scores   S = Q~ K^T on mma.sync.m16n8k16 (fp16 in, fp32 accumulate): A = the query,
 //            rows = head (fp16 high part) and head + 8 (fp16 low part, the rounding residue),
 //            so S_hi + S_lo carries ~22 bits of q~; B = 2-bit key codes.  The page stores the
@@ -19,7 +22,8 @@
 //            (A = q~ * 2^(6 - 2r)).  One accumulator per 64-channel group because each group
 //            has its own scale: logit = 2^18 s_g S_g + m_g sum_{c in g} q~_c (log2 units);
 //   softmax  online, per head, with a lazily raised reference max (output rescaled only when a
-//            logit passes the reference by 2^8); logits are formed relative to the reference
+//            logit passes the reference by 2^8, tested per thread first, so the row-group max
+//            reduction runs only on that rare path); logits are formed relative to the reference
 //            and all the per-token arithmetic runs on packed fp32 pairs (f32x2 FMA / MUL / ADD:
 //            the two tokens 2 tig, 2 tig + 1 of a score column pair), which halves the FP32
 //            instructions that share the datapath with the MMAs;
@@ -56,10 +60,10 @@ template <int W>
 struct MmaSmem {
     uint8_t stage[W][kStagesPerWarp][kPageHeadBytes];
     uint64_t full[W][kStagesPerWarp];
-    // per-token scales of the current chunk, token pairs (2p, 2p + 1) side by side:
+    // per-token scales of the current page, token pairs (2p, 2p + 1) side by side:
     // [0] key (2^18 s0, 2^18 s0'), (m0, m0'); [1] key (2^18 s1, ...), (m1, ...); [2] value (s0, ...), (m0, ...);
     // [3] value (s1, ...), (m1, ...)
-    float4 tsc[W][4][16];
+    float4 tsc[W][4][32];
 };
 
 
@@ -245,35 +249,33 @@ __global__ void __launch_bounds__(32 * warps_for(G), 1) decode_mma(const __grid_
         const uint8_t* pg = sm->stage[warp][s];
         const int n_live = min(kPage, int2_tokens(p.len[it.b]) - it.j * kPage);
 
+        // ---- per-token scales of the page (tokens lane and lane + 32), staged in shared memory;
+        // the warp barrier before the stage refill orders the previous page's reads before these writes
 #pragma unroll
-        for (int cbase = 0; cbase < kPage; cbase += CT) {
-            if (cbase >= n_live) break;                 // only the last page of a request is partial
-            const bool partial = cbase + CT > n_live;
-            // ---- per-token scales of the chunk (one token per lane), staged in shared memory
-            __syncwarp();
-            if (lane < CT) {
-                const int t = cbase + lane;
-                const bool live = t < n_live;
-                const uint2 ksm = *reinterpret_cast<const uint2*>(pg + kKSm + t * 8);
-                const uint2 vsm = *reinterpret_cast<const uint2*>(pg + kVSm + t * 8);
-                const float val[8] = {
-                    live ? kTwo18 * __half2float(__ushort_as_half(ksm.x & 0xffff)) : 0.f,
-                    live ? __half2float(__ushort_as_half(ksm.x >> 16)) : 0.f,
-                    live ? kTwo18 * __half2float(__ushort_as_half(ksm.y & 0xffff)) : 0.f,
-                    live ? __half2float(__ushort_as_half(ksm.y >> 16)) : 0.f,
-                    live ? __half2float(__ushort_as_half(vsm.x & 0xffff)) : 0.f,
-                    live ? __half2float(__ushort_as_half(vsm.x >> 16)) : 0.f,
-                    live ? __half2float(__ushort_as_half(vsm.y & 0xffff)) : 0.f,
-                    live ? __half2float(__ushort_as_half(vsm.y >> 16)) : 0.f};
-                float* row = reinterpret_cast<float*>(&sm->tsc[warp][0][lane >> 1]);
+        for (int hh = 0; hh < 2; ++hh) {
+            const int t = lane + 32 * hh;
+            const bool live = t < n_live;
+            const uint2 ksm = *reinterpret_cast<const uint2*>(pg + kKSm + t * 8);
+            const uint2 vsm = *reinterpret_cast<const uint2*>(pg + kVSm + t * 8);
+            const float val[8] = {
+                live ? kTwo18 * __half2float(__ushort_as_half(ksm.x & 0xffff)) : 0.f,
+                live ? __half2float(__ushort_as_half(ksm.x >> 16)) : 0.f,
+                live ? kTwo18 * __half2float(__ushort_as_half(ksm.y & 0xffff)) : 0.f,
+                live ? __half2float(__ushort_as_half(ksm.y >> 16)) : 0.f,
+                live ? __half2float(__ushort_as_half(vsm.x & 0xffff)) : 0.f,
+                live ? __half2float(__ushort_as_half(vsm.x >> 16)) : 0.f,
+                live ? __half2float(__ushort_as_half(vsm.y & 0xffff)) : 0.f,
+                live ? __half2float(__ushort_as_half(vsm.y >> 16)) : 0.f};
+            float* row = reinterpret_cast<float*>(&sm->tsc[warp][0][t >> 1]);
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    row[j * 64 + (lane & 1)] = val[2 * j];
-                    row[j * 64 + 2 + (lane & 1)] = val[2 * j + 1];
-                }
+            for (int j = 0; j < 4; ++j) {
+                row[j * 128 + (t & 1)] = val[2 * j];
+                row[j * 128 + 2 + (t & 1)] = val[2 * j + 1];
             }
-            __syncwarp();
+        }
+        __syncwarp();
 
+        auto chunk = [&](const int cbase, const bool partial) {
             // ---- scores: acc[k][nt][group]; n-tile nt = tokens cbase + 8 nt + (0..7)
             float acc[MT][NT][2][4];
 #pragma unroll
@@ -312,7 +314,7 @@ __global__ void __launch_bounds__(32 * warps_for(G), 1) decode_mma(const __grid_
             float2 lg[MT][NT];
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
-                const float4 k0 = sm->tsc[warp][0][4 * nt + tig], k1 = sm->tsc[warp][1][4 * nt + tig];
+                const float4 k0 = sm->tsc[warp][0][(cbase >> 1) + 4 * nt + tig], k1 = sm->tsc[warp][1][(cbase >> 1) + 4 * nt + tig];
 #pragma unroll
                 for (int k = 0; k < MT; ++k) {
                     const float2 s0 = __fadd2_rn(make_float2(acc[k][nt][0][0], acc[k][nt][0][1]),
@@ -336,35 +338,43 @@ __global__ void __launch_bounds__(32 * warps_for(G), 1) decode_mma(const __grid_
                         for (int k = 0; k < MT; ++k)
                             if (cbase + 8 * nt + 2 * tig + e >= n_live) (e ? lg[k][nt].y : lg[k][nt].x) = -INFINITY;
             }
-            float fown[MT], cmx[MT];
-            bool raise = false;
+            // thread-local test first: the row-group reduction runs only when some logit of the
+            // warp passed the reference by 2^tau (or the segment is fresh)
+            float cml[MT];
+            bool hot = fresh;
 #pragma unroll
             for (int k = 0; k < MT; ++k) {
                 float cm = -INFINITY;
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) cm = fmaxf(cm, fmaxf(lg[k][nt].x, lg[k][nt].y));
-                cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, 1));
-                cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, 2));
-                fown[k] = 1.f;
-                cmx[k] = 0.f;
-                if (fresh || cm > kTauM) {
-                    fown[k] = fresh ? 0.f : ex2(-cm);
-                    mref[k] += cm;
-                    cmx[k] = cm;
-                    const float2 f2 = make_float2(fown[k], fown[k]);
-                    lsum[k] = __fmul2_rn(lsum[k], f2);
-                    mv[k][0] = __fmul2_rn(mv[k][0], f2);
-                    mv[k][1] = __fmul2_rn(mv[k][1], f2);
-                    raise = true;
-                }
+                cml[k] = cm;
+                hot = hot || cm > kTauM;
             }
-            if (__any_sync(0xffffffffu, raise)) {
+            if (__any_sync(0xffffffffu, hot)) {
+                float fown[MT], cmx[MT];
+#pragma unroll
+                for (int k = 0; k < MT; ++k) {
+                    float cm = cml[k];
+                    cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, 1));
+                    cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, 2));
+                    fown[k] = 1.f;
+                    cmx[k] = 0.f;
+                    if (fresh || cm > kTauM) {
+                        fown[k] = fresh ? 0.f : ex2(-cm);
+                        mref[k] += cm;
+                        cmx[k] = cm;
+                        const float2 f2 = make_float2(fown[k], fown[k]);
+                        lsum[k] = __fmul2_rn(lsum[k], f2);
+                        mv[k][0] = __fmul2_rn(mv[k][0], f2);
+                        mv[k][1] = __fmul2_rn(mv[k][1], f2);
+                    }
+                }
                 fresh = false;
 #pragma unroll
                 for (int k = 0; k < MT; ++k)
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt) lg[k][nt] = __fadd2_rn(lg[k][nt], make_float2(-cmx[k], -cmx[k]));
-                // rare: a head's reference max went up; O^T holds heads 2 tig, 2 tig + 1 (+ 8 nh),
+                // a head's reference max went up; O^T holds heads 2 tig, 2 tig + 1 (+ 8 nh),
                 // whose factors live in the threads of rows g = head
 #pragma unroll
                 for (int k = 0; k < MT; ++k) {
@@ -382,7 +392,7 @@ __global__ void __launch_bounds__(32 * warps_for(G), 1) decode_mma(const __grid_
             // probabilities (ex2(-inf) = 0) and P' = p * s_V rounded once to fp16, packed per token pair
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
-                const float4 v0 = sm->tsc[warp][2][4 * nt + tig], v1 = sm->tsc[warp][3][4 * nt + tig];
+                const float4 v0 = sm->tsc[warp][2][(cbase >> 1) + 4 * nt + tig], v1 = sm->tsc[warp][3][(cbase >> 1) + 4 * nt + tig];
                 const int kk = nt >> 1, half = nt & 1;
 #pragma unroll
                 for (int k = 0; k < MT; ++k) {
@@ -434,6 +444,16 @@ __global__ void __launch_bounds__(32 * warps_for(G), 1) decode_mma(const __grid_
                         OSCAR_PV_STEP(3)
 #undef OSCAR_PV_STEP
                     }
+            }
+        };
+        if (n_live == kPage) {   // every page but the last of a request: no tail checks
+#pragma unroll
+            for (int cbase = 0; cbase < kPage; cbase += CT) chunk(cbase, false);
+        } else {
+#pragma unroll
+            for (int cbase = 0; cbase < kPage; cbase += CT) {
+                if (cbase >= n_live) break;
+                chunk(cbase, cbase + CT > n_live);
             }
         }
 
