@@ -10,8 +10,9 @@
 // request lengths.  A warp keeps its own ring of shared-memory stages filled by bulk-async
 // copies (page-table entries fetched 32 pages ahead).  Per page it converts the fp16 per-token
 // scales and minima once into an fp32 table in shared memory, then runs 32-token chunks (16 for
-// G > 8); every page but the last of a request takes a copy of the chunk loop without tail checks,
-// so the chunks of a page form one straight-line block the compiler can interleave.  Per chunk:
+// G > 8); every page but the last of a request takes a copy of the chunk loop without tail checks
+// in which the output MMAs of chunk c - 1 follow the score MMAs of chunk c, so that the chunks of a
+// page form straight-line blocks the compiler can interleave.  Per chunk:
 //   scores   S = Q~ K^T on mma.sync.m16n8k16 (fp16 in, fp32 accumulate): A = the query,
 //            rows = head (fp16 high part) and head + 8 (fp16 low part, the rounding residue),
 //            so S_hi + S_lo carries ~22 bits of q~; B = 2-bit key codes.  The page stores the
@@ -275,7 +276,8 @@ __global__ void __launch_bounds__(32 * warps_for(G), 1) decode_mma(const __grid_
         }
         __syncwarp();
 
-        auto chunk = [&](const int cbase, const bool partial) {
+        // scores and logits of one chunk, relative to the current reference max
+        auto scores = [&](const int cbase, const bool partial, float2 (&lg)[MT][NT]) {
             // ---- scores: acc[k][nt][group]; n-tile nt = tokens cbase + 8 nt + (0..7)
             float acc[MT][NT][2][4];
 #pragma unroll
@@ -310,8 +312,6 @@ __global__ void __launch_bounds__(32 * warps_for(G), 1) decode_mma(const __grid_
 
             // ---- logits (packed over the token pair e = 0, 1 of each n-tile column pair), relative
             // to the reference max
-            uint32_t pb[2][KK][MT][2];       // [group][k-step][head tile][B register]
-            float2 lg[MT][NT];
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
                 const float4 k0 = sm->tsc[warp][0][(cbase >> 1) + 4 * nt + tig], k1 = sm->tsc[warp][1][(cbase >> 1) + 4 * nt + tig];
@@ -338,6 +338,9 @@ __global__ void __launch_bounds__(32 * warps_for(G), 1) decode_mma(const __grid_
                         for (int k = 0; k < MT; ++k)
                             if (cbase + 8 * nt + 2 * tig + e >= n_live) (e ? lg[k][nt].y : lg[k][nt].x) = -INFINITY;
             }
+        };
+        // reference-max update (thread-local test, rare warp-wide raise)
+        auto update = [&](float2 (&lg)[MT][NT]) {
             // thread-local test first: the row-group reduction runs only when some logit of the
             // warp passed the reference by 2^tau (or the segment is fresh)
             float cml[MT];
@@ -389,6 +392,9 @@ __global__ void __launch_bounds__(32 * warps_for(G), 1) decode_mma(const __grid_
                     }
                 }
             }
+        };
+        // probabilities and P' of one chunk
+        auto probs = [&](const int cbase, const float2 (&lg)[MT][NT], uint32_t (&pb)[2][KK][MT][2]) {
             // probabilities (ex2(-inf) = 0) and P' = p * s_V rounded once to fp16, packed per token pair
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
@@ -407,6 +413,9 @@ __global__ void __launch_bounds__(32 * warps_for(G), 1) decode_mma(const __grid_
                 }
             }
 
+        };
+        // O^T += V^T P'^T of one chunk
+        auto pv = [&](const int cbase, const uint32_t (&pb)[2][KK][MT][2]) {
             // ---- output^T: O[cm] += V^T[channels 16 cm + g, + 8][tokens] x P'_{group(cm)}
             // value words of this thread for the chunk's k-steps: [channel half q][k-step][s]
             {
@@ -446,14 +455,28 @@ __global__ void __launch_bounds__(32 * warps_for(G), 1) decode_mma(const __grid_
                     }
             }
         };
-        if (n_live == kPage) {   // every page but the last of a request: no tail checks
+        constexpr int NC = kPage / CT;
+        if (n_live == kPage) {   // every page but the last of a request: output MMAs of chunk c - 1 after the scores of chunk c
+            float2 lg[MT][NT];
+            uint32_t pbs[2][2][KK][MT][2];
 #pragma unroll
-            for (int cbase = 0; cbase < kPage; cbase += CT) chunk(cbase, false);
+            for (int c = 0; c < NC; ++c) {
+                scores(c * CT, false, lg);
+                if (c > 0) pv((c - 1) * CT, pbs[(c - 1) & 1]);
+                update(lg);
+                probs(c * CT, lg, pbs[c & 1]);
+            }
+            pv((NC - 1) * CT, pbs[(NC - 1) & 1]);
         } else {
 #pragma unroll
             for (int cbase = 0; cbase < kPage; cbase += CT) {
                 if (cbase >= n_live) break;
-                chunk(cbase, cbase + CT > n_live);
+                float2 lg[MT][NT];
+                uint32_t pb[2][KK][MT][2];
+                scores(cbase, cbase + CT > n_live, lg);
+                update(lg);
+                probs(cbase, lg, pb);
+                pv(cbase, pb);
             }
         }
 
