@@ -29,6 +29,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -87,10 +88,14 @@ def peaks():
 
 
 def kernel_source_hash():
-    """Hash of the sources that decide the INT2 attention kernel's memory traffic."""
+    """Hash of the sources that decide the INT2 attention kernel's memory traffic, with comments
+    and blank space removed so that editing a comment keeps the recorded counters valid."""
     h = hashlib.sha256()
     for name in ("decode_mma.cu", "internal.h"):
-        h.update(open(os.path.join(ROOT, "int2_rotated_paged_gb300", "csrc", name), "rb").read())
+        text = open(os.path.join(ROOT, "int2_rotated_paged_gb300", "csrc", name)).read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 

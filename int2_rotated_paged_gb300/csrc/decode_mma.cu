@@ -27,7 +27,7 @@
 //            reduction runs only on that rare path); logits are formed relative to the reference
 //            and all the per-token arithmetic runs on packed fp32 pairs (f32x2 FMA / MUL / ADD:
 //            the two tokens 2 tig, 2 tig + 1 of a score column pair), which halves the FP32
-//            instructions that share the datapath with the MMAs;
+//            instructions and, unlike scalar FFMA, overlaps the MMAs almost fully;
 //   output   O^T += V^T P'^T on the same MMA: A = the value codes (rows = 16 channels), again
 //            one AND per register from a 16-byte load in fragment order (v_code_byte), with
 //            channel tile cm carrying 4^(cm mod 4) * 2^-24 (removed when the partial is
