@@ -123,25 +123,37 @@ __global__ void __launch_bounds__(128) quant_few(const __grid_constant__ AppendP
     const int phys = p.page_table[(size_t)b * p.max_pps + pg];
     uint8_t* blk = p.pool + ((size_t)phys * p.hkv + h) * kPageHeadBytes;
 
-    {   // stage R_K of this head
+    {   // stage R_K of this head with asynchronous 16-byte copies, all of a thread's 32 in flight
+        // at once (waited for before the first __syncthreads below)
         const float4* src = reinterpret_cast<const float4*>(p.rk + (size_t)h * kD * kD);
-        float4* dst = reinterpret_cast<float4*>(R);
-        for (int i = c; i < kD * kD / 4; i += 128) dst[i] = src[i];
+        const uint32_t dst = (uint32_t)__cvta_generic_to_shared(R);
+#pragma unroll
+        for (int i = 0; i < kD * kD / 4 / 128; ++i)
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst + 16u * (c + 128 * i)),
+                         "l"(src + c + 128 * i)
+                         : "memory");
     }
     for (int p0 = pbeg; p0 < pend; p0 += kFew) {
         const int n = min(kFew, pend - p0);
         __syncthreads();
         for (int t = 0; t < n; ++t) xs[t * kD + c] = bf16_bits_to_f32(token_src(p, b, h, 0, p0 + t)[c]);
+        if (p0 == pbeg) asm volatile("cp.async.wait_all;" ::: "memory");   // R_K has landed
         __syncthreads();
-        // keys: k~_c = sum_j x_j R[j][c], serial fused multiply-add in ascending j
+        // keys: k~_c = sum_j x_j R[j][c], serial fused multiply-add in ascending j (one chain per
+        // token; a decode step brings one token per (page, KV head), which takes the single chain)
         float acc[kFew];
 #pragma unroll
         for (int t = 0; t < kFew; ++t) acc[t] = 0.0f;
+        if (n == 1) {
+#pragma unroll 8
+            for (int j = 0; j < kD; ++j) acc[0] = __fmaf_rn(xs[j], R[j * kD + c], acc[0]);
+        } else {
 #pragma unroll 4
-        for (int j = 0; j < kD; ++j) {
-            const float rj = R[j * kD + c];
+            for (int j = 0; j < kD; ++j) {
+                const float rj = R[j * kD + c];
 #pragma unroll
-            for (int t = 0; t < kFew; ++t) acc[t] = __fmaf_rn(xs[t * kD + j], rj, acc[t]);
+                for (int t = 0; t < kFew; ++t) acc[t] = __fmaf_rn(xs[t * kD + j], rj, acc[t]);
+            }
         }
         for (int t = 0; t < n; ++t) {
             const int slot = (p0 + t - kSink) % kPage;
@@ -227,10 +239,15 @@ __global__ void __launch_bounds__(128) quant_pages(const __grid_constant__ Appen
     const int phys = p.page_table[(size_t)b * p.max_pps + pg];
     uint8_t* blk = p.pool + ((size_t)phys * p.hkv + h) * kPageHeadBytes;
 
-    {   // stage R_K of this head and the key inputs of the page's live slots
+    {   // stage R_K of this head (asynchronous 16-byte copies, all in flight while the key inputs
+        // of the page's live slots are loaded) and those key inputs
         const float4* src = reinterpret_cast<const float4*>(p.rk + (size_t)h * kD * kD);
-        float4* dst = reinterpret_cast<float4*>(R);
-        for (int i = t; i < kD * kD / 4; i += 128) dst[i] = src[i];
+        const uint32_t dst = (uint32_t)__cvta_generic_to_shared(R);
+#pragma unroll
+        for (int i = 0; i < kD * kD / 4 / 128; ++i)
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst + 16u * (t + 128 * i)),
+                         "l"(src + t + 128 * i)
+                         : "memory");
         // 16-byte loads (8 channels of one token), 8 independent ones per thread
         for (int idx = t; idx < kPage * (kD / 8); idx += 128) {
             const int s = idx >> 4, ch = 8 * (idx & 15);
@@ -243,6 +260,7 @@ __global__ void __launch_bounds__(128) quant_pages(const __grid_constant__ Appen
                 xt[(ch + 2 * k + 1) * kPage + s] = bf16_bits_to_f32((uint16_t)(ws[k] >> 16));
             }
         }
+        asm volatile("cp.async.wait_all;" ::: "memory");
     }
     __syncthreads();
 
