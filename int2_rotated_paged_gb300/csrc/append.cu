@@ -223,7 +223,9 @@ __device__ __forceinline__ GroupStat group_minmax8(float mn, float mx) {
 __global__ void __launch_bounds__(128) quant_pages(const __grid_constant__ AppendParams p) {
     extern __shared__ __align__(16) float smem[];
     float* R = smem;                   // [128][128]
-    float* xt = R + kD * kD;           // [128][64]: key inputs, channel-major (xt[j][slot])
+    float* xt = R + kD * kD;           // [128][64]: key inputs, channel-major (xt[j][slot]); after the
+                                       // rotation, the page-head block being built (full pages)
+    uint16_t* vt = reinterpret_cast<uint16_t*>(xt + kD * kPage);   // [64][128]: value rows (bf16)
 
     const int job = blockIdx.x;
     const int h = blockIdx.y;
@@ -248,9 +250,20 @@ __global__ void __launch_bounds__(128) quant_pages(const __grid_constant__ Appen
             asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst + 16u * (t + 128 * i)),
                          "l"(src + t + 128 * i)
                          : "memory");
-        // 16-byte loads (8 channels of one token), 8 independent ones per thread
+        // value rows of the live slots, also asynchronous (read by the quantisation below)
+        const uint32_t vdst = (uint32_t)__cvta_generic_to_shared(vt);
+#pragma unroll
+        for (int i = 0; i < kPage * (kD / 8) / 128; ++i) {
+            const int idx = t + 128 * i, s = idx >> 4, ch = 8 * (idx & 15);
+            if (s >= sbeg && s < send)
+                asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(vdst + 2u * (s * kD + ch)),
+                             "l"(token_src(p, b, h, 1, page_pos + s) + ch)
+                             : "memory");
+        }
+        // key inputs: 16-byte loads (8 channels of one token), 8 independent ones per thread; the 32
+        // lanes of a warp take 32 slots of one channel block, so the transposed stores hit 32 banks
         for (int idx = t; idx < kPage * (kD / 8); idx += 128) {
-            const int s = idx >> 4, ch = 8 * (idx & 15);
+            const int s = idx & (kPage - 1), ch = 8 * (idx >> 6);
             if (s < sbeg || s >= send) continue;
             const uint4 w = *reinterpret_cast<const uint4*>(token_src(p, b, h, 0, page_pos + s) + ch);
             const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
@@ -283,6 +296,11 @@ __global__ void __launch_bounds__(128) quant_pages(const __grid_constant__ Appen
 #pragma unroll
             for (int jj = 0; jj < 8; ++jj) acc[i][jj] = __fmaf_rn(xv[i], rv[jj], acc[i][jj]);
     }
+    // a page filled completely by this call is built in shared memory (in the key-input space, free
+    // now) and written out with 16-byte stores; a partly filled one is updated byte by byte in place
+    const bool whole = sbeg == 0 && send == kPage;
+    uint8_t* ob = whole ? reinterpret_cast<uint8_t*>(xt) : blk;
+    __syncthreads();
 
     // ---- per token: clip, quantise, pack.  Channel c = 8 cb + jj: group u = cb >> 3, code
     // position r = (cb >> 1) & 3, y = cb & 1 in both page orders.
@@ -312,16 +330,16 @@ __global__ void __launch_bounds__(128) quant_pages(const __grid_constant__ Appen
             if (live && rpos == 0) {
 #pragma unroll
                 for (int jj = 0; jj < 8; ++jj)
-                    blk[kKCodes + s * 32 + 8 * (jj >> 1) + 4 * u + 2 * (jj & 1) + y] = (uint8_t)bytes[jj];
+                    ob[kKCodes + s * 32 + 8 * (jj >> 1) + 4 * u + 2 * (jj & 1) + y] = (uint8_t)bytes[jj];
             }
             if (live && (cb & 7) == 0)
-                *reinterpret_cast<uint32_t*>(blk + kKSm + s * 8 + u * 4) = (uint32_t)s16 | ((uint32_t)m16 << 16);
+                *reinterpret_cast<uint32_t*>(ob + kKSm + s * 8 + u * 4) = (uint32_t)s16 | ((uint32_t)m16 << 16);
         }
         // values (unrotated): this thread's 8 channels of the token, straight from the source row
         {
             float vx[8];
             if (live) {
-                const uint4 w = *reinterpret_cast<const uint4*>(token_src(p, b, h, 1, page_pos + s) + 8 * cb);
+                const uint4 w = *reinterpret_cast<const uint4*>(vt + s * kD + 8 * cb);
                 const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
@@ -350,11 +368,16 @@ __global__ void __launch_bounds__(128) quant_pages(const __grid_constant__ Appen
             // channel 8 cb + jj = 64 u + 16 rpos + 8 y + jj: the byte of (slot s, channel 64 u + 8 y + jj)
             if (live && rpos == 0) {
 #pragma unroll
-                for (int jj = 0; jj < 8; ++jj) blk[kVCodes + v_code_byte(s, 64 * u + 8 * y + jj)] = (uint8_t)bytes[jj];
+                for (int jj = 0; jj < 8; ++jj) ob[kVCodes + v_code_byte(s, 64 * u + 8 * y + jj)] = (uint8_t)bytes[jj];
             }
             if (live && (cb & 7) == 0)
-                *reinterpret_cast<uint32_t*>(blk + kVSm + s * 8 + u * 4) = (uint32_t)s16 | ((uint32_t)m16 << 16);
+                *reinterpret_cast<uint32_t*>(ob + kVSm + s * 8 + u * 4) = (uint32_t)s16 | ((uint32_t)m16 << 16);
         }
+    }
+    if (whole) {
+        __syncthreads();
+        for (int i = t; i < kPageHeadBytes / 16; i += 128)
+            reinterpret_cast<uint4*>(blk)[i] = reinterpret_cast<const uint4*>(ob)[i];
     }
 }
 
@@ -387,7 +410,7 @@ cudaError_t launch_append(const AppendParams& p, cudaStream_t s) {
     int most = 0;
     for (int b = 0; b < p.batch; ++b) most = max(most, p.req[b].e1 - p.req[b].e0);
     const bool few = most <= kFew;
-    const size_t smem_tiled = (size_t)(kD * kD + kD * kPage) * sizeof(float);
+    const size_t smem_tiled = (size_t)(kD * kD + kD * kPage) * sizeof(float) + (size_t)kPage * kD * sizeof(uint16_t);
     const size_t smem_few = (size_t)(kD * kD + kFew * kD + 8) * sizeof(float);
     static bool attr_set = false;
     if (!attr_set) {
