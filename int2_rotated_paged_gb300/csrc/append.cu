@@ -214,13 +214,16 @@ __device__ __forceinline__ GroupStat group_minmax8(float mn, float mx) {
     return g;
 }
 
+constexpr int kQPThreads = 256;   // threads of quant_pages
+constexpr int kSPT = kPage * 16 / kQPThreads;   // page slots per thread (16 lanes per slot)
+
 // One CTA per (touched INT2 page, KV head), 128 threads.  Thread t owns the 8 page slots
 // 8 (t >> 4) .. + 7 and the 8 channels 8 cb .. 8 cb + 7 (cb = t & 15), so a token's 128 channels sit
 // in 16 lanes of one warp and a 64-channel group in 8 of them: group min / max and the packing of
 // four codes per byte are warp shuffles, with no block-wide barrier per token.
 // Keys: the 64 x 128 tile times R_K with each output the serial fmaf chain over ascending j
 // (the bit-exact contract), 8 tokens x 8 channels of independent chains per thread.
-__global__ void __launch_bounds__(128) quant_pages(const __grid_constant__ AppendParams p) {
+__global__ void __launch_bounds__(kQPThreads) quant_pages(const __grid_constant__ AppendParams p) {
     extern __shared__ __align__(16) float smem[];
     float* R = smem;                   // [128][128]
     float* xt = R + kD * kD;           // [128][64]: key inputs, channel-major (xt[j][slot]); after the
@@ -246,15 +249,15 @@ __global__ void __launch_bounds__(128) quant_pages(const __grid_constant__ Appen
         const float4* src = reinterpret_cast<const float4*>(p.rk + (size_t)h * kD * kD);
         const uint32_t dst = (uint32_t)__cvta_generic_to_shared(R);
 #pragma unroll
-        for (int i = 0; i < kD * kD / 4 / 128; ++i)
-            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst + 16u * (t + 128 * i)),
-                         "l"(src + t + 128 * i)
+        for (int i = 0; i < kD * kD / 4 / kQPThreads; ++i)
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst + 16u * (t + kQPThreads * i)),
+                         "l"(src + t + kQPThreads * i)
                          : "memory");
         // value rows of the live slots, also asynchronous (read by the quantisation below)
         const uint32_t vdst = (uint32_t)__cvta_generic_to_shared(vt);
 #pragma unroll
-        for (int i = 0; i < kPage * (kD / 8) / 128; ++i) {
-            const int idx = t + 128 * i, s = idx >> 4, ch = 8 * (idx & 15);
+        for (int i = 0; i < kPage * (kD / 8) / kQPThreads; ++i) {
+            const int idx = t + kQPThreads * i, s = idx >> 4, ch = 8 * (idx & 15);
             if (s >= sbeg && s < send)
                 asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(vdst + 2u * (s * kD + ch)),
                              "l"(token_src(p, b, h, 1, page_pos + s) + ch)
@@ -262,7 +265,7 @@ __global__ void __launch_bounds__(128) quant_pages(const __grid_constant__ Appen
         }
         // key inputs: 16-byte loads (8 channels of one token), 8 independent ones per thread; the 32
         // lanes of a warp take 32 slots of one channel block, so the transposed stores hit 32 banks
-        for (int idx = t; idx < kPage * (kD / 8); idx += 128) {
+        for (int idx = t; idx < kPage * (kD / 8); idx += kQPThreads) {
             const int s = idx & (kPage - 1), ch = 8 * (idx >> 6);
             if (s < sbeg || s >= send) continue;
             const uint4 w = *reinterpret_cast<const uint4*>(token_src(p, b, h, 0, page_pos + s) + ch);
@@ -278,21 +281,20 @@ __global__ void __launch_bounds__(128) quant_pages(const __grid_constant__ Appen
     __syncthreads();
 
     // ---- keys: k~[s][c] = sum_j x[s][j] R[j][c], serial fused multiply-add in ascending j
-    float acc[8][8];
+    float acc[kSPT][8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
+    for (int i = 0; i < kSPT; ++i)
 #pragma unroll
         for (int jj = 0; jj < 8; ++jj) acc[i][jj] = 0.0f;
 #pragma unroll 2
     for (int j = 0; j < kD; ++j) {
-        const float4 x0 = *reinterpret_cast<const float4*>(xt + j * kPage + 8 * tb);
-        const float4 x1 = *reinterpret_cast<const float4*>(xt + j * kPage + 8 * tb + 4);
+        const float4 x0 = *reinterpret_cast<const float4*>(xt + j * kPage + kSPT * tb);
         const float4 r0 = *reinterpret_cast<const float4*>(R + j * kD + 8 * cb);
         const float4 r1 = *reinterpret_cast<const float4*>(R + j * kD + 8 * cb + 4);
-        const float xv[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+        const float xv[kSPT] = {x0.x, x0.y, x0.z, x0.w};
         const float rv[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
+        for (int i = 0; i < kSPT; ++i)
 #pragma unroll
             for (int jj = 0; jj < 8; ++jj) acc[i][jj] = __fmaf_rn(xv[i], rv[jj], acc[i][jj]);
     }
@@ -306,8 +308,8 @@ __global__ void __launch_bounds__(128) quant_pages(const __grid_constant__ Appen
     // position r = (cb >> 1) & 3, y = cb & 1 in both page orders.
     const int u = cb >> 3, rpos = (cb >> 1) & 3, y = cb & 1;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const int s = 8 * tb + i;
+    for (int i = 0; i < kSPT; ++i) {
+        const int s = kSPT * tb + i;
         const bool live = s >= sbeg && s < send;      // same for the 16 lanes of the token
         if (!__any_sync(0xffffffffu, live)) continue;
         // keys
@@ -376,7 +378,7 @@ __global__ void __launch_bounds__(128) quant_pages(const __grid_constant__ Appen
     }
     if (whole) {
         __syncthreads();
-        for (int i = t; i < kPageHeadBytes / 16; i += 128)
+        for (int i = t; i < kPageHeadBytes / 16; i += kQPThreads)
             reinterpret_cast<uint4*>(blk)[i] = reinterpret_cast<const uint4*>(ob)[i];
     }
 }
@@ -426,7 +428,7 @@ cudaError_t launch_append(const AppendParams& p, cudaStream_t s) {
         if (few)
             quant_few<<<dim3(p.n_jobs, p.hkv), 128, smem_few, s>>>(p);
         else
-            quant_pages<<<dim3(p.n_jobs, p.hkv), 128, smem_tiled, s>>>(p);
+            quant_pages<<<dim3(p.n_jobs, p.hkv), kQPThreads, smem_tiled, s>>>(p);
         ++n;
     }
     insert_bf16<<<dim3(p.batch, p.hkv), 128, 0, s>>>(p);
