@@ -318,21 +318,27 @@ __global__ void __launch_bounds__(kQPThreads) quant_pages(const __grid_constant_
 #pragma unroll
             for (int jj = 1; jj < 8; ++jj) mn = fminf(mn, acc[i][jj]), mx = fmaxf(mx, acc[i][jj]);
             const GroupStat gs = group_minmax8(mn, mx);
-            uint32_t bytes[8];                         // byte 8x + 4u + 2e + y of the row, x = jj >> 1, e = jj & 1
+            // code of channel 8 cb + jj at bits 2 rpos of byte jj & 3 of word jj >> 2; after the OR
+            // over the four code positions every byte is complete
+            uint32_t w[2] = {0u, 0u};
             uint16_t s16 = 0, m16 = 0;
 #pragma unroll
             for (int jj = 0; jj < 8; ++jj) {
                 const Quant q = quantise(acc[i][jj], gs, p.clip_k);
-                bytes[jj] = (uint32_t)q.code << (2 * rpos);
+                w[jj >> 2] |= (uint32_t)q.code << (8 * (jj & 3) + 2 * rpos);
                 s16 = q.s16;
                 m16 = q.m16;
             }
-#pragma unroll
-            for (int jj = 0; jj < 8; ++jj) bytes[jj] = or_over_r(bytes[jj]);
+            w[0] = or_over_r(w[0]);
+            w[1] = or_over_r(w[1]);
+            // the row's word at 8 x + 4 u holds the bytes (e, y) = (0, 0), (0, 1), (1, 0), (1, 1) of
+            // channels 2 x + e: the y = 0 lane writes x = 0, 1 and the y = 1 lane x = 2, 3
+            const uint32_t p0 = __shfl_xor_sync(0xffffffffu, w[0], 1), p1 = __shfl_xor_sync(0xffffffffu, w[1], 1);
             if (live && rpos == 0) {
-#pragma unroll
-                for (int jj = 0; jj < 8; ++jj)
-                    ob[kKCodes + s * 32 + 8 * (jj >> 1) + 4 * u + 2 * (jj & 1) + y] = (uint8_t)bytes[jj];
+                const uint32_t lo = y ? p1 : w[0], hi = y ? w[1] : p0;   // bytes of lane y = 0 / y = 1
+                uint8_t* row = ob + kKCodes + s * 32 + 16 * y + 4 * u;
+                *reinterpret_cast<uint32_t*>(row) = __byte_perm(lo, hi, 0x5140);
+                *reinterpret_cast<uint32_t*>(row + 8) = __byte_perm(lo, hi, 0x7362);
             }
             if (live && (cb & 7) == 0)
                 *reinterpret_cast<uint32_t*>(ob + kKSm + s * 8 + u * 4) = (uint32_t)s16 | ((uint32_t)m16 << 16);
@@ -356,21 +362,22 @@ __global__ void __launch_bounds__(kQPThreads) quant_pages(const __grid_constant_
 #pragma unroll
             for (int jj = 1; jj < 8; ++jj) mn = fminf(mn, vx[jj]), mx = fmaxf(mx, vx[jj]);
             const GroupStat gs = group_minmax8(mn, mx);
-            uint32_t bytes[8];
+            uint32_t w[2] = {0u, 0u};
             uint16_t s16 = 0, m16 = 0;
 #pragma unroll
             for (int jj = 0; jj < 8; ++jj) {
                 const Quant q = quantise(vx[jj], gs, p.clip_v);
-                bytes[jj] = (uint32_t)q.code << (2 * rpos);
+                w[jj >> 2] |= (uint32_t)q.code << (8 * (jj & 3) + 2 * rpos);
                 s16 = q.s16;
                 m16 = q.m16;
             }
-#pragma unroll
-            for (int jj = 0; jj < 8; ++jj) bytes[jj] = or_over_r(bytes[jj]);
+            w[0] = or_over_r(w[0]);
+            w[1] = or_over_r(w[1]);
             // channel 8 cb + jj = 64 u + 16 rpos + 8 y + jj: the byte of (slot s, channel 64 u + 8 y + jj)
             if (live && rpos == 0) {
 #pragma unroll
-                for (int jj = 0; jj < 8; ++jj) ob[kVCodes + v_code_byte(s, 64 * u + 8 * y + jj)] = (uint8_t)bytes[jj];
+                for (int jj = 0; jj < 8; ++jj)
+                    ob[kVCodes + v_code_byte(s, 64 * u + 8 * y + jj)] = (uint8_t)(w[jj >> 2] >> (8 * (jj & 3)));
             }
             if (live && (cb & 7) == 0)
                 *reinterpret_cast<uint32_t*>(ob + kVSm + s * 8 + u * 4) = (uint32_t)s16 | ((uint32_t)m16 << 16);
