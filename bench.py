@@ -57,6 +57,8 @@ def parse():
                     help="requests per GPU (0 = the workload's batch); smaller values are for profiling")
     ap.add_argument("--path", default="mma", choices=["mma", "simt"],
                     help="decode kernel: warp-level MMA (default) or the SIMT baseline")
+    ap.add_argument("--unfused", action="store_true",
+                    help="run each step as kv_quant_append + oscar_decode_attention instead of oscar_decode_step")
     return ap.parse_args()
 
 
@@ -88,11 +90,15 @@ def peaks():
 
 
 def kernel_source_hash():
-    """Hash of the sources that decide the INT2 attention kernel's memory traffic, with comments
-    and blank space removed so that editing a comment keeps the recorded counters valid."""
+    """Hash of the sources that decide the INT2 attention kernel's memory traffic: the kernel file,
+    its copy helpers and the page layout / parameter structs of internal.h (the host-side launcher
+    declarations at its end are left out), with comments and blank space removed so that editing a
+    comment keeps the recorded counters valid."""
     h = hashlib.sha256()
-    for name in ("decode_mma.cu", "internal.h"):
+    for name in ("decode_mma.cu", "ptx_async.h", "internal.h"):
         text = open(os.path.join(ROOT, "int2_rotated_paged_gb300", "csrc", name)).read()
+        if name == "internal.h":
+            text = text[:text.index("cudaError_t launch_")]
         text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
         text = re.sub(r"//[^\n]*", " ", text)
         h.update(" ".join(text.split()).encode())
@@ -328,9 +334,18 @@ def run_ours(args, cfg, rank, world, dist):
     out = torch.empty(B, hq, 128, device=dev)
     torch.cuda.synchronize()
 
+    ones = [1] * B
+
+    def step_call(k, v, q):
+        # one decode step through the public API: the fused call, or its two halves
+        if args.unfused:
+            cache.append(k, v, ones, rk)
+            cache.attend(q, rk, out)
+        else:
+            cache.step(k, v, q, rk, out)
+
     def step(s):
-        cache.append(ks[s], vs[s], [1] * B, rk)
-        cache.attend(qs[s], rk, out)
+        step_call(ks[s], vs[s], qs[s])
 
     # inputs smaller than twice L2 (129 MB): a 256 MB buffer is rewritten between timed steps
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if l2_flush_needed(cfg, lens0) else None
@@ -353,17 +368,21 @@ def run_ours(args, cfg, rank, world, dist):
     # byte counts of the timed steps, worked out before the loop so the host stays ahead of the GPU
     bytes_steps = sum(decode_bytes([lens_at[b] + i + 1 for b in range(B)], hkv, hq) for i in range(args.steps))
     kbytes = sum(int2_kernel_bytes([lens_at[b] + i + 1 for b in range(B)], hkv, hq) for i in range(args.steps))
-    ones = [1] * B
     t0.record(stream)
     for i in range(args.steps):
         s = args.warmup + i
         if flush is not None:
             flush.fill_(i & 255)      # evicts the previous step's pages from L2; outside the step's events
         stp[i][0].record(stream)
-        cache.append(ks[s], vs[s], ones, rk)
-        dec[i][0].record(stream)
-        cache.attend(qs[s], rk, out)
-        dec[i][1].record(stream)
+        if args.unfused:
+            cache.append(ks[s], vs[s], ones, rk)
+            dec[i][0].record(stream)
+            cache.attend(qs[s], rk, out)
+            dec[i][1].record(stream)
+        else:
+            dec[i][0].record(stream)
+            cache.step(ks[s], vs[s], qs[s], rk, out)
+            dec[i][1].record(stream)
         stp[i][1].record(stream)
     t1.record(stream)
     torch.cuda.synchronize()
@@ -419,8 +438,7 @@ def run_ours(args, cfg, rank, world, dist):
                 w0 = time.perf_counter()
             h0 = time.perf_counter()
             d_in.copy_(h_in[s], non_blocking=True)
-            cache.append(dk, dv, [1] * B, rk)
-            cache.attend(dq, rk, out)
+            step_call(dk, dv, dq)
             host_out.copy_(out, non_blocking=True)
             if s >= args.warmup:
                 enqueue += time.perf_counter() - h0
@@ -447,6 +465,14 @@ def run_ours(args, cfg, rank, world, dist):
                          f"(request, KV head) pairs at full context on {threads} threads, "
                          f"{sum(times):.1f} s wall ({sum(times) * threads:.0f} thread-s)"}
     kname = dict(mma="decode_mma", simt="split_simt")[args.path]
+    if args.unfused or args.path != "mma":
+        call_what = (f"oscar_decode_attention: prep (q rotation + BF16 sink/window attention) + {kname} + combine"
+                     if args.path == "mma" else
+                     f"oscar_decode_attention: rotate_q + {kname} (INT2 and BF16 splits) + combine")
+        call_what += "; the step adds kv_quant_append before it"
+    else:
+        call_what = (f"oscar_decode_step (the whole step): prep with the append of one token per request "
+                     f"(window insert, leaving key rotated and quantised) + {kname} + combine")
     workload = workload_config(cfg, lens0)
     line = {
         "metric": "decode_attention_hbm_gbs", "value": value, "unit": "GB/s", "n_gpus": world,
@@ -457,10 +483,9 @@ def run_ours(args, cfg, rank, world, dist):
                      "peak_kind": peak_kind, "traffic": profiled_traffic(workload["workload"], k_bytes),
                      "kernel": kname, "bytes_per_launch": k_bytes, "ms_per_launch": k_t * 1e3,
                      "timing": "CUDA events recorded by the library on the launching stream around each launch",
-                     "call": {"what": (f"oscar_decode_attention: prep (q rotation + BF16 sink/window attention) + {kname} + combine" if args.path == "mma" else f"oscar_decode_attention: rotate_q + {kname} (INT2 and BF16 splits) + combine"),
-                              "bytes": dec_bytes, "ms": dec_t * 1e3, "gbs": dec_bytes / dec_t / 1e9}},
+                     "call": {"what": call_what, "bytes": dec_bytes, "ms": dec_t * 1e3, "gbs": dec_bytes / dec_t / 1e9}},
         "append": {"prefill_tokens_per_s": tok_append / t_append, "prefill_tokens": tok_append,
-                   "step_ms_excl_decode": (per_step - dec_t) * 1e3},
+                   "step_ms_outside_int2_kernel": (per_step - k_t) * 1e3},
         "clocks": clk,
         "gpu_launches": launches,
         "e2e": e2e,

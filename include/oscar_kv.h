@@ -184,6 +184,21 @@ int oscar_decode_attention(oscar_cache *c, const void *q, int32_t q_dtype, const
                            void *out, int32_t out_dtype, void *workspace, size_t workspace_bytes,
                            void *stream);
 
+/* oscar_decode_step: one decode step of every request, the write path and the read path in one
+ * call.  It appends one token per request (k, v: device, bf16, [batch, num_kv_heads, 128], as for
+ * kv_quant_append with new_tokens[b] = 1 for every b) and then runs oscar_decode_attention with q
+ * (all arguments as there).  The result, the cache contents and the errors are the same as those
+ * of the two calls in a row, bit for bit; on the warp-MMA path the append runs inside the first
+ * attention kernel (the leaving key is rotated with the same R_K loads as the queries) instead of
+ * in launches of its own.  On the SIMT path it makes the two calls.  Argument, capacity and
+ * alignment errors are found before anything is enqueued and leave the cache unchanged.
+ * Source: axbrief.com OSCAR page, section "attention-statistics rotation + Triton kernels" (the
+ * rotated, quantised write path and the fused read path); joining them into one step is this
+ * library's scheduling, not something the page describes. */
+int oscar_decode_step(oscar_cache *c, const void *k, const void *v, const void *q, int32_t q_dtype,
+                      const float *rk, void *out, int32_t out_dtype, void *workspace,
+                      size_t workspace_bytes, void *stream);
+
 /* Which decode kernel oscar_decode_attention runs (process-wide; default OSCAR_PATH_WARP_MMA):
  * OSCAR_PATH_WARP_MMA: every warp streams its own contiguous run of INT2 pages through a
  *                      bulk-async-copy ring and runs scores and P.V on warp-level tensor-core

@@ -35,7 +35,7 @@ EXPORTS = [
     "kv_page_table_free_pages", "kv_quant_append", "oscar_decode_workspace_bytes",
     "oscar_decode_attention", "oscar_build_rk_workspace_bytes", "oscar_build_rk", "oscar_read_int2",
     "oscar_read_bf16", "oscar_strerror", "oscar_last_cuda_error", "oscar_launch_count",
-    "oscar_set_decode_path", "oscar_decode_status", "oscar_decode_attention_noalloc",
+    "oscar_set_decode_path", "oscar_decode_status", "oscar_decode_attention_noalloc", "oscar_decode_step",
     "oscar_kernel_timing", "oscar_kernel_timing_read",
 ]
 OSCAR_ESCRATCH = -8
@@ -100,6 +100,7 @@ def lib() -> ctypes.CDLL:
         "oscar_set_decode_path": (ctypes.c_int, [I32]),
         "oscar_decode_status": (ctypes.c_int, [P, SZ, P, P]),
         "oscar_decode_attention_noalloc": (ctypes.c_int, [P, P, I32, P, P, I32, P]),
+        "oscar_decode_step": (ctypes.c_int, [P, P, P, P, I32, P, P, I32, P, SZ, P]),
         "oscar_kernel_timing": (ctypes.c_int, [P, I32]),
         "oscar_kernel_timing_read": (ctypes.c_int, [P, P, I32, P]),
     }
@@ -197,6 +198,14 @@ def oscar_decode_attention(cache, q, q_dtype: int, rk, out, out_dtype: int, work
     nbytes = workspace.numel() * workspace.element_size()
     _check("oscar_decode_attention", lib().oscar_decode_attention(
         cache, _ptr(q), q_dtype, _ptr(rk), _ptr(out), out_dtype, _ptr(workspace), nbytes, _stream(stream)))
+
+
+def oscar_decode_step(cache, k, v, q, q_dtype: int, rk, out, out_dtype: int, workspace, stream=None):
+    """Append one token per request (k, v: [batch, Hkv, 128] bf16) and attend with q, in one call."""
+    nbytes = workspace.numel() * workspace.element_size()
+    _check("oscar_decode_step", lib().oscar_decode_step(
+        cache, _ptr(k), _ptr(v), _ptr(q), q_dtype, _ptr(rk), _ptr(out), out_dtype, _ptr(workspace), nbytes,
+        _stream(stream)))
 
 
 def oscar_decode_attention_noalloc(cache, q, q_dtype: int, rk, out, out_dtype: int, stream=None):
@@ -307,6 +316,12 @@ class Cache:
         qd = DTYPE_BF16 if str(q.dtype) == "torch.bfloat16" else DTYPE_F32
         od = DTYPE_BF16 if str(out.dtype) == "torch.bfloat16" else DTYPE_F32
         oscar_decode_attention(self.handle, q, qd, rk, out, od, self.workspace, stream)
+
+    def step(self, k, v, q, rk, out, stream=None):
+        """One decode step: append one token per request and attend (oscar_decode_step)."""
+        qd = DTYPE_BF16 if str(q.dtype) == "torch.bfloat16" else DTYPE_F32
+        od = DTYPE_BF16 if str(out.dtype) == "torch.bfloat16" else DTYPE_F32
+        oscar_decode_step(self.handle, k, v, q, qd, rk, out, od, self.workspace, stream)
 
     def status(self, stream=None):
         """Raise if the last decode on this cache's workspace hit a bounded in-kernel wait."""

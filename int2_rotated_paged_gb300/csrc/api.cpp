@@ -252,8 +252,11 @@ int32_t kv_page_table_free_pages(const oscar_cache* c) {
 
 // ------------------------------------------------------------------ write path
 
-int kv_quant_append(oscar_cache* c, const void* k, const void* v, const int32_t* new_tokens,
-                    const float* rk, void* stream) {
+// Host part of an append: argument and capacity checks, page reservation, page-table upload and
+// the kernel parameters.  *any = false when no token is appended.  c->len is left to the caller.
+static int prepare_append(oscar_cache* c, const void* k, const void* v, const int32_t* new_tokens,
+                          const float* rk, cudaStream_t s, AppendParams& p, bool* any) {
+    *any = false;
     if (!c || !new_tokens) return OSCAR_EINVAL;
     const oscar_cache_desc& d = c->d;
     int64_t rows = 0;
@@ -272,14 +275,12 @@ int kv_quant_append(oscar_cache* c, const void* k, const void* v, const int32_t*
     if (!aligned16(k) || !aligned16(v) || !aligned16(rk)) return OSCAR_EALIGN;
     if (need_pages > (int64_t)c->free_list.size()) return OSCAR_ENOPAGES;
 
-    cudaStream_t s = S(stream);
     for (int32_t b = 0; b < d.batch; ++b) {
         int rc = take_pages(c, b, c->len[b] + new_tokens[b]);
         if (rc != OSCAR_OK) return rc;   // cannot happen after the capacity check above
     }
     int rc = sync(c, s);
     if (rc != OSCAR_OK) return rc;
-    AppendParams p;
     std::memset(&p, 0, sizeof(p));
     p.batch = d.batch;
     p.hkv = d.num_kv_heads;
@@ -309,9 +310,19 @@ int kv_quant_append(oscar_cache* c, const void* k, const void* v, const int32_t*
         off += new_tokens[b];
     }
     p.n_jobs = jobs;
-    cudaError_t e = launch_append(p, s);
+    *any = true;
+    return OSCAR_OK;
+}
+
+int kv_quant_append(oscar_cache* c, const void* k, const void* v, const int32_t* new_tokens,
+                    const float* rk, void* stream) {
+    AppendParams p;
+    bool any = false;
+    int rc = prepare_append(c, k, v, new_tokens, rk, S(stream), p, &any);
+    if (rc != OSCAR_OK || !any) return rc;
+    cudaError_t e = launch_append(p, S(stream));
     if (e != cudaSuccess) return cuda_fail(e);
-    for (int32_t b = 0; b < d.batch; ++b) c->len[b] += new_tokens[b];
+    for (int32_t b = 0; b < c->d.batch; ++b) c->len[b] += new_tokens[b];
     return OSCAR_OK;
 }
 
@@ -396,18 +407,22 @@ int oscar_decode_status(const void* workspace, size_t workspace_bytes, const osc
     return err ? OSCAR_ETIMEOUT : OSCAR_OK;
 }
 
-int oscar_decode_attention(oscar_cache* c, const void* q, int32_t q_dtype, const float* rk,
-                           void* out, int32_t out_dtype, void* workspace, size_t workspace_bytes,
-                           void* stream) {
+static int check_decode_args(const oscar_cache* c, const void* q, int32_t q_dtype, const float* rk,
+                             const void* out, int32_t out_dtype, const void* workspace, size_t workspace_bytes) {
     if (!c || !q || !rk || !out) return OSCAR_EINVAL;
     if ((q_dtype != OSCAR_DTYPE_F32 && q_dtype != OSCAR_DTYPE_BF16) ||
         (out_dtype != OSCAR_DTYPE_F32 && out_dtype != OSCAR_DTYPE_BF16))
         return OSCAR_EINVAL;
     if (!workspace || workspace_bytes < oscar_decode_workspace_bytes(c)) return OSCAR_EWORKSPACE;
     if (!aligned16(q) || !aligned16(rk) || !aligned16(out) || !aligned16(workspace)) return OSCAR_EALIGN;
-    int rc = sync(c, S(stream));
+    return OSCAR_OK;
+}
+
+// Kernel parameters of a decode call over the cache's current lengths (page table uploaded first).
+static int prepare_decode(oscar_cache* c, const void* q, int32_t q_dtype, const float* rk, void* out,
+                          int32_t out_dtype, void* workspace, cudaStream_t s, DecodeParams& p) {
+    int rc = sync(c, s);
     if (rc != OSCAR_OK) return rc;
-    DecodeParams p;
     std::memset(&p, 0, sizeof(p));
     p.batch = c->d.batch;
     p.hkv = c->d.num_kv_heads;
@@ -444,12 +459,52 @@ int oscar_decode_attention(oscar_cache* c, const void* q, int32_t q_dtype, const
         rc = mma_warp_count(c->g, pages, &p.n_warps);
         if (rc != OSCAR_OK) return rc;
     }
-    cudaEvent_t* timing = nullptr;
-    if (c->timing_used * 2 + 1 < (int32_t)c->timing_ev.size()) {
-        timing = &c->timing_ev[2 * c->timing_used];
-        ++c->timing_used;
+    return OSCAR_OK;
+}
+
+static cudaEvent_t* next_timing(oscar_cache* c) {
+    if (c->timing_used * 2 + 1 >= (int32_t)c->timing_ev.size()) return nullptr;
+    cudaEvent_t* t = &c->timing_ev[2 * c->timing_used];
+    ++c->timing_used;
+    return t;
+}
+
+int oscar_decode_attention(oscar_cache* c, const void* q, int32_t q_dtype, const float* rk,
+                           void* out, int32_t out_dtype, void* workspace, size_t workspace_bytes,
+                           void* stream) {
+    int rc = check_decode_args(c, q, q_dtype, rk, out, out_dtype, workspace, workspace_bytes);
+    if (rc != OSCAR_OK) return rc;
+    DecodeParams p;
+    rc = prepare_decode(c, q, q_dtype, rk, out, out_dtype, workspace, S(stream), p);
+    if (rc != OSCAR_OK) return rc;
+    cudaError_t e = launch_decode(p, S(stream), next_timing(c));
+    return e == cudaSuccess ? OSCAR_OK : cuda_fail(e);
+}
+
+int oscar_decode_step(oscar_cache* c, const void* k, const void* v, const void* q, int32_t q_dtype,
+                      const float* rk, void* out, int32_t out_dtype, void* workspace, size_t workspace_bytes,
+                      void* stream) {
+    int rc = check_decode_args(c, q, q_dtype, rk, out, out_dtype, workspace, workspace_bytes);
+    if (rc != OSCAR_OK) return rc;
+    const std::vector<int32_t> ones(c->d.batch, 1);
+    if (g_decode_path != OSCAR_PATH_WARP_MMA) {
+        rc = kv_quant_append(c, k, v, ones.data(), rk, stream);
+        if (rc != OSCAR_OK) return rc;
+        return oscar_decode_attention(c, q, q_dtype, rk, out, out_dtype, workspace, workspace_bytes, stream);
     }
-    cudaError_t e = launch_decode(p, S(stream), timing);
+    // the lengths after the append must fit the page-offset arithmetic before anything changes
+    int64_t pages = 0;
+    for (int32_t b = 0; b < c->d.batch; ++b) pages += (int64_t)int2_pages((int32_t)c->len[b] + 1) * c->d.num_kv_heads;
+    if (pages > INT32_MAX / 4) return OSCAR_ERANGE;
+    AppendParams a;
+    bool any = false;
+    rc = prepare_append(c, k, v, ones.data(), rk, S(stream), a, &any);
+    if (rc != OSCAR_OK) return rc;
+    for (int32_t b = 0; b < c->d.batch; ++b) c->len[b] += 1;
+    DecodeParams p;
+    rc = prepare_decode(c, q, q_dtype, rk, out, out_dtype, workspace, S(stream), p);
+    if (rc != OSCAR_OK) return rc;
+    cudaError_t e = launch_decode_step(p, a, S(stream), next_timing(c));
     return e == cudaSuccess ? OSCAR_OK : cuda_fail(e);
 }
 

@@ -23,81 +23,18 @@
 #include <cuda_fp16.h>
 
 #include "internal.h"
+#include "token_quant.h"
 
 namespace oscar {
 namespace {
 
-__device__ __forceinline__ float bf16_bits_to_f32(uint16_t b) {
-    return __uint_as_float(((uint32_t)b) << 16);
-}
+using namespace tq;
 
 __device__ __forceinline__ int find_request(const AppendParams& p, int job) {
     int b = 0;
     for (int i = 1; i < p.batch; ++i)
         if (p.req[i].e1 > p.req[i].e0 && p.req[i].job0 <= job) b = i;
     return b;
-}
-
-// Source row (bf16[128]) of position `pos` of request b, KV head h, tensor kv (0 = K, 1 = V).
-__device__ __forceinline__ const uint16_t* token_src(const AppendParams& p, int b, int h, int kv,
-                                                     int pos) {
-    const AppendReq& r = p.req[b];
-    if (pos < r.len0) {   // still in the BF16 window (it leaves it in this call)
-        size_t base = (((size_t)b * p.hkv + h) * 2 + kv) * kSlots + bf16_slot(pos);
-        return p.bf16 + base * kD;
-    }
-    const uint16_t* t = kv == 0 ? p.k : p.v;
-    return t + ((size_t)(r.tok_off + (pos - r.len0)) * p.hkv + h) * kD;
-}
-
-struct GroupStat {
-    float mn, mx;
-};
-
-struct Quant {
-    int code;
-    uint16_t s16, m16;
-};
-
-__device__ __forceinline__ Quant quantise(float y, GroupStat g, float clip) {
-    const float lo = __fmul_rn(clip, g.mn);
-    const float hi = __fmul_rn(clip, g.mx);
-    const float s_exact = __fdiv_rn(__fsub_rn(hi, lo), 3.0f);
-    Quant q;
-    q.s16 = __half_as_ushort(__float2half_rn(s_exact));
-    q.m16 = __half_as_ushort(__float2half_rn(lo));
-    const float s = __half2float(__ushort_as_half(q.s16));
-    const float m = __half2float(__ushort_as_half(q.m16));
-    const float xc = fminf(fmaxf(y, lo), hi);
-    int code = 0;
-    if (s != 0.0f) {
-        const float t = rintf(__fdiv_rn(__fsub_rn(xc, m), s));
-        code = t < 0.0f ? 0 : (t > 3.0f ? 3 : (int)t);
-    }
-    q.code = code;
-    return q;
-}
-
-// Min and max over the 64 channels of each group (threads 0..63 and 64..127).
-__device__ __forceinline__ GroupStat group_minmax(float y, float* red) {
-    float mn = y, mx = y;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    }
-    const int w = threadIdx.x >> 5;
-    if ((threadIdx.x & 31) == 0) {
-        red[2 * w] = mn;
-        red[2 * w + 1] = mx;
-    }
-    __syncthreads();
-    const int w0 = w & ~1;
-    GroupStat g;
-    g.mn = fminf(red[2 * w0], red[2 * w0 + 2]);
-    g.mx = fmaxf(red[2 * w0 + 1], red[2 * w0 + 3]);
-    __syncthreads();
-    return g;
 }
 
 constexpr int kFew = 8;   // tokens per (page, KV head) up to which quant_few is used
@@ -114,7 +51,6 @@ __global__ void __launch_bounds__(128) quant_few(const __grid_constant__ AppendP
     const int job = blockIdx.x;
     const int h = blockIdx.y;
     const int c = threadIdx.x;
-    const int lane = c & 31;
     const int b = find_request(p, job);
     const AppendReq& r = p.req[b];
     const int pg = r.page0 + (job - r.job0);
@@ -156,40 +92,9 @@ __global__ void __launch_bounds__(128) quant_few(const __grid_constant__ AppendP
             }
         }
         for (int t = 0; t < n; ++t) {
-            const int slot = (p0 + t - kSink) % kPage;
-            // ---- K (rotated) and V (unrotated): per-token asymmetric INT2 in two 64-channel groups
-            const float yk = acc[t];
-            const Quant qk = quantise(yk, group_minmax(yk, red), p.clip_k);
+            // K (rotated) and V (unrotated): per-token asymmetric INT2 in two 64-channel groups
             const float yv = bf16_bits_to_f32(token_src(p, b, h, 1, p0 + t)[c]);
-            const Quant qv = quantise(yv, group_minmax(yv, red), p.clip_v);
-            if ((c & 63) == 0) {
-                *reinterpret_cast<uint32_t*>(blk + kKSm + slot * 8 + (c >> 6) * 4) =
-                    (uint32_t)qk.s16 | ((uint32_t)qk.m16 << 16);
-                *reinterpret_cast<uint32_t*>(blk + kVSm + slot * 8 + (c >> 6) * 4) =
-                    (uint32_t)qv.s16 | ((uint32_t)qv.m16 << 16);
-            }
-            // ---- pack: every code byte holds the codes of four channels c0 + 16 r (r = 0..3) of
-            // this token, two from lanes l and l ^ 16 of one warp and two from the next warp
-            uint32_t pk = (uint32_t)qk.code << k_code_shift(c);
-            uint32_t pv = (uint32_t)qv.code << v_code_shift(c);
-            pk |= __shfl_xor_sync(0xffffffffu, pk, 16);
-            pv |= __shfl_xor_sync(0xffffffffu, pv, 16);
-            if (lane < 16) {
-                part[0][c >> 5][lane] = (uint8_t)pk;
-                part[1][c >> 5][lane] = (uint8_t)pv;
-            }
-            __syncthreads();
-            if (c < 32) {
-                // key byte c of the token row: channels 64u + 16r + 8y + 2x + e
-                const int x = c >> 3, u = (c >> 2) & 1, e = (c >> 1) & 1, y = c & 1;
-                const int l = 8 * y + 2 * x + e;
-                blk[kKCodes + slot * 32 + c] = part[0][2 * u][l] | part[0][2 * u + 1][l];
-            } else if (c < 64) {
-                // value byte of channels 64q + 16r + 8y + g
-                const int j = c - 32, q = j >> 4, g = (j >> 1) & 7, y = j & 1;
-                const int l = 8 * y + g;
-                blk[kVCodes + v_code_byte(slot, 64 * q + 8 * y + g)] = part[1][2 * q][l] | part[1][2 * q + 1][l];
-            }
+            store_token(blk, (p0 + t - kSink) % kPage, acc[t], yv, p.clip_k, p.clip_v, red, part);
         }
     }
 }

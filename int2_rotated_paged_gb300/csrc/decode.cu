@@ -369,6 +369,21 @@ cudaError_t launch_split(const DecodeParams& p, int max_ns, cudaStream_t s) {
 
 }  // namespace
 
+cudaError_t launch_decode_step(const DecodeParams& p, const AppendParams& a, cudaStream_t s, cudaEvent_t* timing) {
+    static_assert(sizeof(DecodeParams) + sizeof(AppendParams) <= 32000, "kernel parameters of prep_step");
+    if (p.path != 2) return cudaErrorInvalidValue;
+    cudaError_t e = launch_prep_step(p, a, s);
+    if (e != cudaSuccess) return e;
+    count_launches(1);
+    if (timing && (e = cudaEventRecord(timing[0], s)) != cudaSuccess) return e;
+    e = launch_decode_mma(p, s);
+    if (e != cudaSuccess) return e;
+    if (timing && (e = cudaEventRecord(timing[1], s)) != cudaSuccess) return e;
+    combine_mma<<<dim3(p.hkv, p.batch), 32 * p.g, 0, s>>>(p);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t s, cudaEvent_t* timing) {
     cudaError_t e;
     if (p.path == 2) {

@@ -114,6 +114,11 @@ cudaError_t launch_append(const AppendParams& p, cudaStream_t s);
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t s, cudaEvent_t* timing = nullptr);
 cudaError_t launch_decode_mma(const DecodeParams& p, cudaStream_t s);
 cudaError_t launch_prep(const DecodeParams& p, cudaStream_t s);
+cudaError_t launch_prep_step(const DecodeParams& p, const AppendParams& a, cudaStream_t s);
+// fused decode step (warp-MMA path): prep with the append of one token per request, then the INT2
+// attention and the combine
+cudaError_t launch_decode_step(const DecodeParams& p, const AppendParams& a, cudaStream_t s,
+                               cudaEvent_t* timing = nullptr);
 int mma_warps_per_cta(int g);   // warps per CTA of the warp-MMA kernel for G query heads per KV head
 cudaError_t launch_build_rk(const float* q, int64_t n, int hkv, float* rk, void* ws, cudaStream_t s);
 size_t build_rk_ws_bytes(int hkv);

@@ -14,6 +14,7 @@
 #include <cuda_bf16.h>
 
 #include "internal.h"
+#include "token_quant.h"
 
 namespace oscar {
 namespace {
@@ -51,8 +52,11 @@ __device__ __forceinline__ bool slot_live(int s, int n_sink, int n_win) {
     return s < n_sink || (s >= kSink && s < kSink + n_win);
 }
 
-template <int G>
-__global__ void __launch_bounds__(32 * prep_warps(G)) prep(const __grid_constant__ DecodeParams p) {
+// STEP: the CTA first appends request b's new token for KV head h (the fused decode step, one new
+// token per request): the token leaving the window is read, the new one written into its BF16 slot,
+// and the leaving key is rotated in the same loop as the queries and quantised into its INT2 slot.
+template <int G, bool STEP>
+__device__ __forceinline__ void prep_body(const DecodeParams& p, const AppendParams* ap) {
     constexpr int MT = (G + 7) / 8;                  // head tiles (rows g and g + 8 of each)
     constexpr int kPrepWarps = prep_warps(G);
     constexpr int NT = 32 * kPrepWarps;
@@ -65,6 +69,26 @@ __global__ void __launch_bounds__(32 * prep_warps(G)) prep(const __grid_constant
     const int warp = c >> 5, lane = c & 31, g = lane >> 2, tig = lane & 3;
     if (b == 0 && h == 0 && c == 0 && p.err) *p.err = 0;
     const size_t qbase = ((size_t)b * p.hkv + h) * G * kD;
+
+    __shared__ float xk[STEP ? kD : 1];              // key leaving the window (fp32)
+    __shared__ float red[2 * kPrepWarps];
+    __shared__ uint8_t tpart[2][4][16];              // packing scratch of the leaving token
+    const bool evict = STEP && ap->req[b].e1 > ap->req[b].e0;   // the same for the whole CTA
+    float yv = 0.f;
+    if constexpr (STEP) {
+        const AppendReq& r = ap->req[b];
+        if (evict && c < kD) {
+            xk[c] = tq::bf16_bits_to_f32(tq::token_src(*ap, b, h, 0, r.e0)[c]);
+            yv = tq::bf16_bits_to_f32(tq::token_src(*ap, b, h, 1, r.e0)[c]);
+        }
+        __syncthreads();   // read before the new token takes the slot it leaves
+        for (int i = c; i < 2 * kD; i += NT) {
+            const int kv = i / kD, ch = i % kD;
+            const uint16_t* src = (kv == 0 ? ap->k : ap->v) + ((size_t)r.tok_off * p.hkv + h) * kD;
+            ap->bf16[((((size_t)b * p.hkv + h) * 2 + kv) * kSlots + bf16_slot(r.len0)) * kD + ch] = src[ch];
+        }
+        if (h == 0 && c == 0) ap->seq_lens[b] = r.len0 + r.n_new;
+    }
     for (int i = c; i < G * kD; i += NT) qs[i / kD][i % kD] = load_query(p, qbase + (size_t)i);
     __syncthreads();
 
@@ -76,6 +100,8 @@ __global__ void __launch_bounds__(32 * prep_warps(G)) prep(const __grid_constant
         float acc[(G + HS - 1) / HS];
 #pragma unroll
         for (int i = 0; i < (G + HS - 1) / HS; ++i) acc[i] = 0.f;
+        // the leaving key takes the same R_K loads: k~_col = serial fmaf chain over ascending j from +0
+        float acck = 0.f;
         const float* R = p.rk + (size_t)h * kD * kD + col;
         for (int j0 = 0; j0 < kD; j0 += 32) {
             float r[32];
@@ -86,10 +112,23 @@ __global__ void __launch_bounds__(32 * prep_warps(G)) prep(const __grid_constant
 #pragma unroll
                 for (int i = 0; i < (G + HS - 1) / HS; ++i)
                     if (h0 + HS * i < G) acc[i] = fmaf(qs[h0 + HS * i][j0 + j], r[j], acc[i]);
+            if (evict) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) acck = __fmaf_rn(xk[j0 + j], r[j], acck);
+            }
         }
 #pragma unroll
         for (int i = 0; i < (G + HS - 1) / HS; ++i)
             if (h0 + HS * i < G) p.qrot[qbase + (size_t)(h0 + HS * i) * kD + col] = acc[i];
+        if (evict) {
+            // clip, quantise and pack the leaving token into its INT2 slot (threads c < 128 hold
+            // channel c; thread c >= 128 of an 8-warp CTA only takes part in the barriers)
+            const AppendReq& r = ap->req[b];
+            const int pg = (r.e0 - kSink) / kPage;
+            const int phys = ap->page_table[(size_t)b * ap->max_pps + pg];
+            uint8_t* blk = ap->pool + ((size_t)phys * p.hkv + h) * kPageHeadBytes;
+            tq::store_token(blk, (r.e0 - kSink) % kPage, c < kD ? acck : 0.f, yv, ap->clip_k, ap->clip_v, red, tpart);
+        }
     }
 
     // ---- BF16 sink + window
@@ -230,7 +269,36 @@ __global__ void __launch_bounds__(32 * prep_warps(G)) prep(const __grid_constant
     }
 }
 
+template <int G>
+__global__ void __launch_bounds__(32 * prep_warps(G)) prep(const __grid_constant__ DecodeParams p) {
+    prep_body<G, false>(p, nullptr);
+}
+
+template <int G>
+__global__ void __launch_bounds__(32 * prep_warps(G)) prep_step(const __grid_constant__ DecodeParams p,
+                                                                 const __grid_constant__ AppendParams a) {
+    prep_body<G, true>(p, &a);
+}
+
 }  // namespace
+
+cudaError_t launch_prep_step(const DecodeParams& p, const AppendParams& a, cudaStream_t s) {
+    const dim3 grid(p.hkv, p.batch);
+    switch (p.g) {
+        case 1: prep_step<1><<<grid, 32 * prep_warps(1), 0, s>>>(p, a); break;
+        case 2: prep_step<2><<<grid, 32 * prep_warps(2), 0, s>>>(p, a); break;
+        case 3: prep_step<3><<<grid, 32 * prep_warps(3), 0, s>>>(p, a); break;
+        case 4: prep_step<4><<<grid, 32 * prep_warps(4), 0, s>>>(p, a); break;
+        case 5: prep_step<5><<<grid, 32 * prep_warps(5), 0, s>>>(p, a); break;
+        case 6: prep_step<6><<<grid, 32 * prep_warps(6), 0, s>>>(p, a); break;
+        case 7: prep_step<7><<<grid, 32 * prep_warps(7), 0, s>>>(p, a); break;
+        case 8: prep_step<8><<<grid, 32 * prep_warps(8), 0, s>>>(p, a); break;
+        case 12: prep_step<12><<<grid, 32 * prep_warps(12), 0, s>>>(p, a); break;
+        case 16: prep_step<16><<<grid, 32 * prep_warps(16), 0, s>>>(p, a); break;
+        default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
 
 cudaError_t launch_prep(const DecodeParams& p, cudaStream_t s) {
     const dim3 grid(p.hkv, p.batch);

@@ -147,6 +147,17 @@ def test_append_argument_errors_before_any_launch(K):
     assert L.oscar_build_rk(FAKE[0], 0, 8, FAKE[1], FAKE[2], 1 << 30, None) == K.OSCAR_EINVAL
     assert L.oscar_build_rk(FAKE[0], 10, 8, FAKE[1], FAKE[2], 8, None) == K.OSCAR_EWORKSPACE
     assert K.strerror(K.OSCAR_ENOPAGES) == "out of INT2 pages"
+    # fused decode step: the decode checks, then the append checks, all before anything changes
+    big_ws = ctypes.c_size_t(1 << 40)
+    assert L.oscar_decode_step(c, FAKE[0], FAKE[1], FAKE[2], 0, FAKE[3], FAKE[0], 0, FAKE[1], 16,
+                               None) == K.OSCAR_EWORKSPACE
+    assert L.oscar_decode_step(c, FAKE[0], FAKE[1], FAKE[2], 7, FAKE[3], FAKE[0], 0, FAKE[1], big_ws,
+                               None) == K.OSCAR_EINVAL
+    assert L.oscar_decode_step(c, FAKE[0] + 2, FAKE[1], FAKE[2], 0, FAKE[3], FAKE[0], 0, FAKE[1], big_ws,
+                               None) == K.OSCAR_EALIGN
+    assert L.oscar_decode_step(c, None, FAKE[1], FAKE[2], 0, FAKE[3], FAKE[0], 0, FAKE[1], big_ws,
+                               None) == K.OSCAR_EINVAL
+    assert L.oscar_cache_length(c, 0) == 0 and L.kv_page_table_free_pages(c) == 4
     L.oscar_cache_destroy(c)
 
 
