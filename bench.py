@@ -90,15 +90,17 @@ def peaks():
 
 
 def kernel_source_hash():
-    """Hash of the sources that decide the INT2 attention kernel's memory traffic: the kernel file,
-    its copy helpers and the page layout / parameter structs of internal.h (the host-side launcher
-    declarations at its end are left out), with comments and blank space removed so that editing a
-    comment keeps the recorded counters valid."""
+    """Hash of the sources that decide the INT2 attention kernel's memory traffic: the kernel's
+    device code, its copy helpers and the page layout / parameter structs of internal.h (host-side
+    launchers and their declarations are left out), with comments and blank space removed so that
+    editing a comment keeps the recorded counters valid."""
     h = hashlib.sha256()
     for name in ("decode_mma.cu", "ptx_async.h", "internal.h"):
         text = open(os.path.join(ROOT, "int2_rotated_paged_gb300", "csrc", name)).read()
         if name == "internal.h":
             text = text[:text.index("cudaError_t launch_")]
+        if name == "decode_mma.cu":                # the device code, not the host launchers after it
+            text = text[:text.index("cudaError_t launch_mma_g")]
         text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
         text = re.sub(r"//[^\n]*", " ", text)
         h.update(" ".join(text.split()).encode())

@@ -544,8 +544,12 @@ template <int G>
 cudaError_t launch_mma_g(const DecodeParams& p, cudaStream_t s) {
     constexpr int W = warps_for(G);
     const int smem = (int)sizeof(MmaSmem<W>);
-    cudaError_t e = cudaFuncSetAttribute(decode_mma<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
+    static bool attr_set = false;   // once per instantiation (the library drives one device)
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(decode_mma<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
     decode_mma<G><<<p.n_warps / W, 32 * W, smem, s>>>(p);
     return cudaGetLastError();
 }
