@@ -251,11 +251,14 @@ __global__ void __launch_bounds__(32 * warps_for(G), 1) decode_mma(const __grid_
         const int n_live = min(kPage, int2_tokens(p.len[it.b]) - it.j * kPage);
 
         // ---- per-token scales of the page (tokens lane and lane + 32), staged in shared memory;
-        // the warp barrier before the stage refill orders the previous page's reads before these writes
+        // the warp barrier before the stage refill orders the previous page's reads before these writes.
+        // Slots past the request's end are staged as 0 (their bytes may be anything); a full page
+        // takes a copy of the loop without that test
+        auto stage = [&](const bool full) {
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
             const int t = lane + 32 * hh;
-            const bool live = t < n_live;
+            const bool live = full || t < n_live;
             const uint2 ksm = *reinterpret_cast<const uint2*>(pg + kKSm + t * 8);
             const uint2 vsm = *reinterpret_cast<const uint2*>(pg + kVSm + t * 8);
             const float val[8] = {
@@ -274,6 +277,9 @@ __global__ void __launch_bounds__(32 * warps_for(G), 1) decode_mma(const __grid_
                 row[j * 128 + 2 + (t & 1)] = val[2 * j + 1];
             }
         }
+        };
+        if (n_live == kPage) stage(true);
+        else stage(false);
         __syncwarp();
 
         // scores and logits of one chunk, relative to the current reference max
