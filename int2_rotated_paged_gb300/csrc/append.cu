@@ -12,7 +12,9 @@
 //   2. insert_bf16: copies the new tokens that stay in BF16 into the sink / window
 //      slots and publishes the new lengths (axbrief.com OSCAR page, section "OSCAR
 //      release": BF16 sink + recent window).
-// Stream order makes kernel 1 read the window before kernel 2 overwrites it.
+// Stream order makes kernel 1 read the window before kernel 2 overwrites it.  A decode step made
+// through oscar_decode_step does the same work for its one token per request inside prep_step
+// (prep.cu) with the per-token quantisation of token_quant.h, which quant_few uses as well.
 //
 // Bit-exact contract (shared with nothing but the written specification): the key
 // rotation is the serial chain acc = fma(x_j, R[j][c], acc), j = 0..127, acc0 = +0;

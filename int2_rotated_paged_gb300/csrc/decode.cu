@@ -15,6 +15,10 @@
 //                 pages (or, for the last split of a request, over the BF16 tokens) for
 //                 the G query heads of the KV head; writes (max, sum, unnormalised out).
 //   combine       out = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s per (request, head).
+//   combine_mma   the same merge for the warp-MMA path (prep.cu, decode_mma.cu): the BF16
+//                 partial and the partials of the warps that streamed the request's pages.
+// launch_decode runs either path; launch_decode_step runs the fused decode step
+// (prep_step -> decode_mma -> combine_mma).
 // All softmax arithmetic is in base 2 (logits pre-scaled by log2(e) / sqrt(128)).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>

@@ -1,4 +1,7 @@
-// prep.cu -- first kernel of a warp-MMA decode call, one CTA per (KV head, request):
+// prep.cu -- first kernel of a warp-MMA decode call, one CTA per (KV head, request).  Its
+// prep_step form (oscar_decode_step) first appends the request's new token for the KV head: the
+// token leaving the window is read, the new one written into the slot it leaves, and the leaving
+// key, rotated in the same R_K loop as the queries, is quantised into its INT2 slot.  Then:
 //   1. q~ = q . R_K for the G query heads of the KV head (fp32), the queries of the INT2 pages
 //      (axbrief.com OSCAR page, section "attention-statistics rotation + Triton kernels": scores
 //      against rotated keys; rotating q once equals inverse-rotating every key, R_K orthogonal);
