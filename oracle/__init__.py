@@ -66,10 +66,15 @@ def _L():
         lib.or_build_rk.argtypes = [P, ctypes.c_long, P, P, P]
         lib.or_rotate_f32.argtypes = [P, P, P]
         lib.or_quant_vec.argtypes = [P, ctypes.c_float, P, P]
+        lib.or_quant_vec_g.argtypes = [P, ctypes.c_float, ctypes.c_int, P, P]
         lib.or_quant_tokens.argtypes = [P, ctypes.c_long, P, ctypes.c_float, P, P, P]
+        lib.or_quant_tokens_g.argtypes = [P, ctypes.c_long, P, ctypes.c_float, ctypes.c_int, P, P, P]
         lib.or_dequant_tokens.argtypes = [P, P, ctypes.c_long, P]
+        lib.or_dequant_tokens_g.argtypes = [P, P, ctypes.c_long, ctypes.c_int, P]
         lib.or_attention.argtypes = [ctypes.c_int, P, P, ctypes.c_long, P, P, P, P, ctypes.c_long,
                                      P, P, P, P]
+        lib.or_attention_g.argtypes = [ctypes.c_int, P, P, ctypes.c_long, ctypes.c_int, ctypes.c_int,
+                                       P, P, P, P, ctypes.c_long, P, P, P, P]
         _lib = lib
     return _lib
 
@@ -141,51 +146,65 @@ def rotate_f32(x: np.ndarray, r: np.ndarray) -> np.ndarray:
     return y
 
 
-def quant_vec(y: np.ndarray, clip: float):
+def _group_ok(group: int) -> int:
+    if group <= 0 or D % group:
+        raise ValueError(f"group size {group} does not divide {D}")
+    return int(group)
+
+
+def quant_vec(y: np.ndarray, clip: float, group: int = GROUP):
+    """One 128-channel vector -> (codes [32] u8, sm [2 * 128 / group] u16: s, m per group)."""
     y = _c(y, np.float32)
+    group = _group_ok(group)
     codes = np.empty(D // 4, np.uint8)
-    sm = np.empty(4, np.uint16)
-    _L().or_quant_vec(_p(y), float(clip), _p(codes), _p(sm))
+    sm = np.empty(2 * D // group, np.uint16)
+    _L().or_quant_vec_g(_p(y), float(clip), group, _p(codes), _p(sm))
     return codes, sm
 
 
-def quant_tokens(x16: np.ndarray, r: Optional[np.ndarray], clip: float, want_y: bool = False):
-    """bf16 bit patterns [n, 128] -> (codes [n, 32] u8, sm [n, 4] u16[, rotated fp32 [n, 128]])."""
+def quant_tokens(x16: np.ndarray, r: Optional[np.ndarray], clip: float, want_y: bool = False,
+                 group: int = GROUP):
+    """bf16 bit patterns [n, 128] -> (codes [n, 32] u8, sm [n, 2 * 128 / group] u16[, rotated fp32
+    [n, 128]])."""
     x16 = _c(x16, np.uint16).reshape(-1, D)
+    group = _group_ok(group)
     n = x16.shape[0]
     codes = np.empty((n, D // 4), np.uint8)
-    sm = np.empty((n, 4), np.uint16)
+    sm = np.empty((n, 2 * D // group), np.uint16)
     y = np.empty((n, D), np.float32) if want_y else None
     rr = None if r is None else _c(r, np.float32)
-    _L().or_quant_tokens(_p(x16), n, _p(rr), float(clip), _p(codes), _p(sm), _p(y))
+    _L().or_quant_tokens_g(_p(x16), n, _p(rr), float(clip), group, _p(codes), _p(sm), _p(y))
     return (codes, sm, y) if want_y else (codes, sm)
 
 
-def dequant_tokens(codes: np.ndarray, sm: np.ndarray) -> np.ndarray:
+def dequant_tokens(codes: np.ndarray, sm: np.ndarray, group: int = GROUP) -> np.ndarray:
+    group = _group_ok(group)
     codes = _c(codes, np.uint8).reshape(-1, D // 4)
-    sm = _c(sm, np.uint16).reshape(-1, 4)
+    sm = _c(sm, np.uint16).reshape(-1, 2 * D // group)
     out = np.empty((codes.shape[0], D), np.float64)
-    _L().or_dequant_tokens(_p(codes), _p(sm), codes.shape[0], _p(out))
+    _L().or_dequant_tokens_g(_p(codes), _p(sm), codes.shape[0], group, _p(out))
     return out
 
 
 # ------------------------------------------------------------------ read path
 
-def attention(q: np.ndarray, r: Optional[np.ndarray], k_codes, k_sm, v_codes, v_sm, k16, v16):
+def attention(q: np.ndarray, r: Optional[np.ndarray], k_codes, k_sm, v_codes, v_sm, k16, v16,
+              group_k: int = GROUP, group_v: int = GROUP):
     """Decode attention of G heads over one KV head (fp64).  Returns (out [G,128], lse [G])."""
     q = _c(q, np.float32).reshape(-1, D)
     g = q.shape[0]
+    group_k, group_v = _group_ok(group_k), _group_ok(group_v)
     kc = _c(k_codes, np.uint8).reshape(-1, D // 4)
-    ks = _c(k_sm, np.uint16).reshape(-1, 4)
+    ks = _c(k_sm, np.uint16).reshape(-1, 2 * D // group_k)
     vc = _c(v_codes, np.uint8).reshape(-1, D // 4)
-    vs = _c(v_sm, np.uint16).reshape(-1, 4)
+    vs = _c(v_sm, np.uint16).reshape(-1, 2 * D // group_v)
     k16 = _c(k16, np.uint16).reshape(-1, D)
     v16 = _c(v16, np.uint16).reshape(-1, D)
     out = np.empty((g, D), np.float64)
     lse = np.empty(g, np.float64)
     rr = None if r is None else _c(r, np.float32)
-    _L().or_attention(g, _p(q), _p(rr), kc.shape[0], _p(kc), _p(ks), _p(vc), _p(vs),
-                      k16.shape[0], _p(k16), _p(v16), _p(out), _p(lse))
+    _L().or_attention_g(g, _p(q), _p(rr), kc.shape[0], group_k, group_v, _p(kc), _p(ks), _p(vc), _p(vs),
+                        k16.shape[0], _p(k16), _p(v16), _p(out), _p(lse))
     return out, lse
 
 
@@ -214,18 +233,20 @@ class OracleCache:
     """
 
     def __init__(self, rk: Optional[np.ndarray], clip_k: float = CLIP_K, clip_v: float = CLIP_V,
-                 sink: int = SINK, window: int = WINDOW):
+                 sink: int = SINK, window: int = WINDOW, group_k: int = GROUP, group_v: int = GROUP):
         self.rk = rk
         self.clip_k = clip_k
         self.clip_v = clip_v
         self.sink = sink
         self.window = window
+        self.group_k = _group_ok(group_k)
+        self.group_v = _group_ok(group_v)
         self.k16: List[np.ndarray] = []   # bf16 bits of every position (kept for the bf16 regions)
         self.v16: List[np.ndarray] = []
         self.kc = np.zeros((0, D // 4), np.uint8)
-        self.ks = np.zeros((0, 4), np.uint16)
+        self.ks = np.zeros((0, 2 * D // self.group_k), np.uint16)
         self.vc = np.zeros((0, D // 4), np.uint8)
-        self.vs = np.zeros((0, 4), np.uint16)
+        self.vs = np.zeros((0, 2 * D // self.group_v), np.uint16)
 
     @property
     def length(self) -> int:
@@ -245,8 +266,8 @@ class OracleCache:
                 evict_k.append(self.k16[q])
                 evict_v.append(self.v16[q])
         if evict_k:
-            kc, ks = quant_tokens(np.stack(evict_k), self.rk, self.clip_k)
-            vc, vs = quant_tokens(np.stack(evict_v), None, self.clip_v)
+            kc, ks = quant_tokens(np.stack(evict_k), self.rk, self.clip_k, group=self.group_k)
+            vc, vs = quant_tokens(np.stack(evict_v), None, self.clip_v, group=self.group_v)
             self.kc = np.concatenate([self.kc, kc])
             self.ks = np.concatenate([self.ks, ks])
             self.vc = np.concatenate([self.vc, vc])
@@ -263,4 +284,4 @@ class OracleCache:
 
     def attend(self, q: np.ndarray):
         k16, v16 = self.bf16_tokens()
-        return attention(q, self.rk, self.kc, self.ks, self.vc, self.vs, k16, v16)
+        return attention(q, self.rk, self.kc, self.ks, self.vc, self.vs, k16, v16, self.group_k, self.group_v)

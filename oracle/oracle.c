@@ -262,21 +262,22 @@ void or_rotate_f32(const float *x, const float *r, float *y)
 }
 
 /*
- * Per-token asymmetric INT2 of one 128-channel vector y (fp32), groups of 64:
+ * Per-token asymmetric INT2 of one 128-channel vector y (fp32), groups of `group` channels
+ * (64, the default G_K of the OSCAR page, or 128; any divisor of 128 works):
  *   mn, mx = group min / max;  lo = c*mn, hi = c*mx  (the clip);
  *   s = fp16(( hi - lo) / 3),  m = fp16(lo);
  *   code = min(max(rint((min(max(y, lo), hi) - m) / s), 0), 3), computed with
  *   the fp16-rounded s and m that are stored; s == 0 gives code 0.
  * Packing: channel 4i + j goes to bits 2j..2j+1 of byte i.
- * sm = [s_0, m_0, s_1, m_1] (fp16 bit patterns).
+ * sm = [s_0, m_0, s_1, m_1, ...] (fp16 bit patterns, one pair per group: 2 * 128 / group).
  */
-void or_quant_vec(const float *y, float clip, uint8_t *codes, uint16_t *sm)
+void or_quant_vec_g(const float *y, float clip, int group, uint8_t *codes, uint16_t *sm)
 {
     uint8_t code[D];
-    for (int g = 0; g < D / GROUP; ++g) {
-        const float *yg = y + g * GROUP;
+    for (int g = 0; g < D / group; ++g) {
+        const float *yg = y + g * group;
         float mn = yg[0], mx = yg[0];
-        for (int c = 1; c < GROUP; ++c) {
+        for (int c = 1; c < group; ++c) {
             mn = fminf(mn, yg[c]);
             mx = fmaxf(mx, yg[c]);
         }
@@ -287,7 +288,7 @@ void or_quant_vec(const float *y, float clip, uint8_t *codes, uint16_t *sm)
         uint16_t m16 = or_f32_to_f16(lo);
         float s = or_f16_to_f32(s16);
         float m = or_f16_to_f32(m16);
-        for (int c = 0; c < GROUP; ++c) {
+        for (int c = 0; c < group; ++c) {
             float xc = fminf(fmaxf(yg[c], lo), hi);
             int q = 0;
             if (s != 0.0f) {
@@ -295,7 +296,7 @@ void or_quant_vec(const float *y, float clip, uint8_t *codes, uint16_t *sm)
                 float r = rintf(t);
                 q = r < 0.0f ? 0 : (r > 3.0f ? 3 : (int)r);
             }
-            code[g * GROUP + c] = (uint8_t)q;
+            code[g * group + c] = (uint8_t)q;
         }
         sm[2 * g] = s16;
         sm[2 * g + 1] = m16;
@@ -305,10 +306,15 @@ void or_quant_vec(const float *y, float clip, uint8_t *codes, uint16_t *sm)
                              (code[4 * i + 3] << 6));
 }
 
-/* n tokens of bf16 input (n x 128 bit patterns) -> codes (n x 32) + sm (n x 4).
+void or_quant_vec(const float *y, float clip, uint8_t *codes, uint16_t *sm)
+{
+    or_quant_vec_g(y, clip, GROUP, codes, sm);
+}
+
+/* n tokens of bf16 input (n x 128 bit patterns) -> codes (n x 32) + sm (n x 2 * 128 / group).
  * r == NULL: no rotation (values).  Also returns the fp32 rotated vectors if y_out != NULL. */
-void or_quant_tokens(const uint16_t *x16, long n, const float *r, float clip, uint8_t *codes,
-                     uint16_t *sm, float *y_out)
+void or_quant_tokens_g(const uint16_t *x16, long n, const float *r, float clip, int group, uint8_t *codes,
+                       uint16_t *sm, float *y_out)
 {
     float x[D], y[D];
     for (long t = 0; t < n; ++t) {
@@ -320,21 +326,33 @@ void or_quant_tokens(const uint16_t *x16, long n, const float *r, float clip, ui
             memcpy(y, x, sizeof(y));
         if (y_out)
             memcpy(y_out + t * D, y, sizeof(y));
-        or_quant_vec(y, clip, codes + t * (D / 4), sm + t * 4);
+        or_quant_vec_g(y, clip, group, codes + t * (D / 4), sm + t * (2 * D / group));
     }
 }
 
-/* x^ = m + code * s in fp64 (exact), n tokens. */
-void or_dequant_tokens(const uint8_t *codes, const uint16_t *sm, long n, double *out)
+void or_quant_tokens(const uint16_t *x16, long n, const float *r, float clip, uint8_t *codes,
+                     uint16_t *sm, float *y_out)
 {
+    or_quant_tokens_g(x16, n, r, clip, GROUP, codes, sm, y_out);
+}
+
+/* x^ = m + code * s in fp64 (exact), n tokens, groups of `group` channels. */
+void or_dequant_tokens_g(const uint8_t *codes, const uint16_t *sm, long n, int group, double *out)
+{
+    const int per = 2 * D / group;
     for (long t = 0; t < n; ++t)
         for (int c = 0; c < D; ++c) {
-            int g = c / GROUP;
+            int g = c / group;
             int code = (codes[t * (D / 4) + c / 4] >> (2 * (c % 4))) & 3;
-            double s = or_f16_to_f32(sm[t * 4 + 2 * g]);
-            double m = or_f16_to_f32(sm[t * 4 + 2 * g + 1]);
+            double s = or_f16_to_f32(sm[t * per + 2 * g]);
+            double m = or_f16_to_f32(sm[t * per + 2 * g + 1]);
             out[t * D + c] = m + code * s;
         }
+}
+
+void or_dequant_tokens(const uint8_t *codes, const uint16_t *sm, long n, double *out)
+{
+    or_dequant_tokens_g(codes, sm, n, GROUP, out);
 }
 
 /* ---------------------------------------------------------------- read path */
@@ -348,17 +366,17 @@ void or_dequant_tokens(const uint8_t *codes, const uint16_t *sm, long n, double 
  * because R_K is orthogonal.  r == NULL means R_K = I.
  * out: G x 128; lse: G (natural log of sum exp(logit)), may be NULL.
  */
-void or_attention(int g_heads, const float *q, const float *r, long n_int2,
-                  const uint8_t *k_codes, const uint16_t *k_sm, const uint8_t *v_codes,
-                  const uint16_t *v_sm, long n_bf16, const uint16_t *k16, const uint16_t *v16,
-                  double *out, double *lse)
+void or_attention_g(int g_heads, const float *q, const float *r, long n_int2, int group_k, int group_v,
+                    const uint8_t *k_codes, const uint16_t *k_sm, const uint8_t *v_codes,
+                    const uint16_t *v_sm, long n_bf16, const uint16_t *k16, const uint16_t *v16,
+                    double *out, double *lse)
 {
     long n = n_int2 + n_bf16;
     double *logit = (double *)malloc(sizeof(double) * (n > 0 ? n : 1));
     double *kh = (double *)malloc(sizeof(double) * D * (n_int2 > 0 ? n_int2 : 1));
     double *vh = (double *)malloc(sizeof(double) * D * (n_int2 > 0 ? n_int2 : 1));
-    or_dequant_tokens(k_codes, k_sm, n_int2, kh);
-    or_dequant_tokens(v_codes, v_sm, n_int2, vh);
+    or_dequant_tokens_g(k_codes, k_sm, n_int2, group_k, kh);
+    or_dequant_tokens_g(v_codes, v_sm, n_int2, group_v, vh);
     double scale = 1.0 / sqrt((double)D);
     for (int hh = 0; hh < g_heads; ++hh) {
         const float *qh = q + hh * D;
@@ -408,4 +426,12 @@ void or_attention(int g_heads, const float *q, const float *r, long n_int2,
     free(logit);
     free(kh);
     free(vh);
+}
+
+void or_attention(int g_heads, const float *q, const float *r, long n_int2,
+                  const uint8_t *k_codes, const uint16_t *k_sm, const uint8_t *v_codes,
+                  const uint16_t *v_sm, long n_bf16, const uint16_t *k16, const uint16_t *v16,
+                  double *out, double *lse)
+{
+    or_attention_g(g_heads, q, r, n_int2, GROUP, GROUP, k_codes, k_sm, v_codes, v_sm, n_bf16, k16, v16, out, lse);
 }
