@@ -257,6 +257,10 @@ int oscar_decode_attention_noalloc(oscar_cache *c, const void *q, int32_t q_dtyp
  * eigenvector signed so its largest-magnitude entry is positive) comes from a parallel
  * cyclic Jacobi eigen-solver in fp64, H_Had[i][j] = (-1)^popcount(i & j) / sqrt(128),
  * P_br[i][j] = [j == bitrev7(i)].  workspace >= oscar_build_rk_workspace_bytes(heads).
+ * Given rows of S V instead (the attention outputs of calibration queries: score-weighted
+ * values, S the softmax scores), the same computation builds the value rotation
+ * R_V = U_S * H_Had * P_br, because C_S = (1/N) V^T S^T S V is their covariance.  The library
+ * stores values as given, so R_V is folded into the value and output projections offline.
  * Source: axbrief.com OSCAR page, section "attention-statistics rotation + Triton
  * kernels"; techllm.github.io page, section "OSCAR" (Hadamard + bit reversal). */
 size_t oscar_build_rk_workspace_bytes(int32_t num_kv_heads);

@@ -136,6 +136,38 @@ def build_rk(q: np.ndarray):
     return r32, r64, ev
 
 
+def score_weighted_values(q: np.ndarray, k: np.ndarray, v: np.ndarray) -> np.ndarray:
+    """Rows of S V (fp64) for calibration queries q [N, 128] against keys k [T, 128] and values
+    v [T, 128]: S = row-wise softmax(q k^T / sqrt(128)).  These are the samples whose covariance
+    is the score-weighted value covariance C_S of the OSCAR page (axbrief.com, section
+    "attention-statistics rotation + Triton kernels")."""
+    q64, k64, v64 = (np.asarray(a, np.float64) for a in (q, k, v))
+    logit = q64 @ k64.T / np.sqrt(D)
+    s = np.exp(logit - logit.max(axis=1, keepdims=True))
+    s /= s.sum(axis=1, keepdims=True)
+    return s @ v64
+
+
+def value_covariance(q: np.ndarray, k: np.ndarray, v: np.ndarray) -> np.ndarray:
+    """C_S = (1/N) V^T S^T S V as the page writes it (fp64), S as in score_weighted_values."""
+    q64, k64, v64 = (np.asarray(a, np.float64) for a in (q, k, v))
+    logit = q64 @ k64.T / np.sqrt(D)
+    s = np.exp(logit - logit.max(axis=1, keepdims=True))
+    s /= s.sum(axis=1, keepdims=True)
+    return v64.T @ (s.T @ s) @ v64 / q64.shape[0]
+
+
+def build_rv(q: np.ndarray, k: np.ndarray, v: np.ndarray):
+    """R_V = U_S H P_br from calibration queries, keys and values (same page and section): U_S the
+    eigenvectors of C_S by the oracle's Jacobi solver (descending, same sign rule as R_K).  Returns
+    (fp32 R_V, fp64 R_V, eigenvalues)."""
+    ev, u, _ = jacobi_eigh(value_covariance(q, k, v))
+    pbr = np.zeros((D, D))
+    pbr[np.arange(D), [bitrev7(i) for i in range(D)]] = 1.0
+    r64 = u @ hadamard128() @ pbr
+    return r64.astype(np.float32), r64, ev
+
+
 # ------------------------------------------------------------------ write path
 
 def rotate_f32(x: np.ndarray, r: np.ndarray) -> np.ndarray:
