@@ -166,6 +166,28 @@ def test_release_and_reuse_pages():
     assert rel_l2(out[0, cfg.group:2 * cfg.group], ref) <= REL_L2
 
 
+def test_build_rv_on_gpu_from_score_weighted_values():
+    # the value rotation: rows of S V (attention outputs of calibration queries) as the samples
+    hkv, n, t = 2, 2048, 600
+    ys = []
+    for h in range(hkv):
+        rng = np.random.default_rng(100 + h)
+        qc = rng.standard_normal((n, 128)) * np.linspace(2.0, 0.2, 128)
+        kc = rng.standard_normal((t, 128))
+        vc = rng.standard_normal((t, 128)) * np.exp(0.5 * rng.standard_normal(128))
+        ys.append(oracle.score_weighted_values(qc, kc, vc).astype(np.float32))
+    y = torch.tensor(np.stack(ys)).cuda().contiguous()
+    rv = torch.empty(hkv, 128, 128, device="cuda")
+    ws = torch.empty(K.oscar_build_rk_workspace_bytes(hkv), dtype=torch.uint8, device="cuda")
+    K.oscar_build_rk(y, n, hkv, rv, ws)
+    torch.cuda.synchronize()
+    got = rv.cpu().numpy().astype(np.float64)
+    for h in range(hkv):
+        _, ref64, _ = oracle.build_rk(ys[h])          # the oracle's builder on the same samples
+        assert np.abs(got[h] - ref64).max() < 1e-6
+        assert np.abs(got[h] @ got[h].T - np.eye(128)).max() < 1e-6
+
+
 def test_build_rk_on_gpu_matches_oracle():
     hkv, n = 4, 4096
     q = torch.stack([synth.calibration_queries(77, h, n) for h in range(hkv)]).cuda().contiguous()
