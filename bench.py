@@ -80,6 +80,22 @@ def int2_kernel_bytes(lens, hkv, hq):
     return sum(hkv * max(0, L - 320) * 80 for L in lens) + len(lens) * hq * 128 * 4
 
 
+# What each decode path computes in (the line's "dtype" names the tensor-core operand / accumulator
+# types of the default path).
+PRECISION = {
+    "mma": {"kv": "INT2 codes with fp16 scale/min per 64-channel group (exact as MMA operands)",
+            "scores": "mma.sync fp16 x fp16 -> fp32; q as fp16 high + low parts (~22 bits) under a "
+                      "power-of-two scale per (request, KV head)",
+            "pv": "mma.sync fp16 x fp16 -> fp32; P' = p * s_V rounded once to fp16",
+            "softmax": "fp32 (packed f32x2), base-2, lazily raised reference max",
+            "bf16_part": "bf16 keys x bf16 high + low query parts (~16 bits) -> fp32; P.V fp32",
+            "combine": "fp32"},
+    "simt": {"kv": "INT2 codes with fp16 scale/min per 64-channel group",
+             "scores": "fp32", "pv": "fp32", "softmax": "fp32", "bf16_part": "fp32", "combine": "fp32"},
+}
+NOMINAL_HBM_GBS = 8000.0   # the GB300 HBM3e figure the workload's target is stated against
+
+
 def peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -268,7 +284,7 @@ def run_reference(args, cfg, rank, world):
               f"(the oracle's cost is linear in the context)")
     line = {
         "impl": "reference", "metric": "decode_attention_hbm_gbs", "value": value, "unit": "GB/s",
-        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": per * 1e3,
+        "n_gpus": world, "world_size": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": per * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": workload_config(cfg, lens),
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": sample},
@@ -486,12 +502,15 @@ def run_ours(args, cfg, rank, world, dist):
                      f"(window insert, leaving key rotated and quantised) + {kname} + combine")
     workload = workload_config(cfg, lens0)
     line = {
-        "metric": "decode_attention_hbm_gbs", "value": value, "unit": "GB/s", "n_gpus": world,
+        "metric": "decode_attention_hbm_gbs", "value": value, "unit": "GB/s", "n_gpus": world, "world_size": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_step * 1e3, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None, "dtype": "fp16-mma/fp32-acc", "data": "synthetic",
+        "precision": PRECISION[args.path],
         "config": workload,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "peak_kind": peak_kind, "traffic": profiled_traffic(workload["workload"], k_bytes),
+                     "peak_kind": peak_kind,
+                     "nominal": {"peak": NOMINAL_HBM_GBS, "frac": achieved / NOMINAL_HBM_GBS},
+                     "traffic": profiled_traffic(workload["workload"], k_bytes),
                      "kernel": kname, "bytes_per_launch": k_bytes, "ms_per_launch": k_t * 1e3,
                      "timing": "CUDA events recorded by the library on the launching stream around each launch",
                      "call": {"what": call_what, "bytes": dec_bytes, "ms": dec_t * 1e3, "gbs": dec_bytes / dec_t / 1e9}},
@@ -506,14 +525,30 @@ def run_ours(args, cfg, rank, world, dist):
     print(json.dumps(line), flush=True)
 
 
+def relaunch_under_torchrun(args) -> int:
+    """`bench.py --gpus N` (N > 1) started without torchrun: start N ranks on this node with
+    torch.distributed.run (rendezvous on 127.0.0.1) and return their exit status."""
+    import socket
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={args.gpus}",
+           "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.abspath(__file__), *sys.argv[1:]]
+    return subprocess.run(cmd).returncode
+
+
 def main():
     args = parse()
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        sys.exit(relaunch_under_torchrun(args))
     import synth
     cfg = synth.config(args.config)
     if args.batch:
         cfg = synth.scaled(cfg, cfg.ctx, batch=args.batch)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
+    if world != args.gpus:
+        sys.exit(f"--gpus {args.gpus} but WORLD_SIZE {world}: launch one rank per GPU")
     dist = None
     if world > 1:
         import torch

@@ -161,6 +161,10 @@ int32_t kv_page_table_free_pages(const oscar_cache *c);
  * and stored in its INT2 page.  Tokens leaving the window are quantised from their
  * BF16 window copy, so appending L tokens at once or one by one stores the same bytes.
  * Pages are reserved as needed (OSCAR_ENOPAGES leaves the cache unchanged).
+ * Range: the clipped group minimum and (hi - lo) / 3 must be representable in fp16
+ * (|c * min|, |c * max| up to about 65504); larger values give undefined codes and scales.
+ * A group whose scale rounds to 0 in fp16 (a constant group, or a range below 2^-25) stores
+ * s = 0 and codes 0, so every element dequantises to m.
  * Source: axbrief.com OSCAR page, section "attention-statistics rotation + Triton
  * kernels" (rotation, c_K, c_V, G_K = 64, per-token asymmetric INT2, V unrotated). */
 int kv_quant_append(oscar_cache *c, const void *k, const void *v, const int32_t *new_tokens,
@@ -177,6 +181,13 @@ int kv_quant_append(oscar_cache *c, const void *k, const void *v, const int32_t 
  * copy reaches global memory.  Requests with length 0 get zeros.
  * workspace (device, >= oscar_decode_workspace_bytes(c) bytes, 16-byte aligned) holds
  * the rotated queries and the split-K partial results; it needs no initialisation.
+ * Numeric range: any finite query and any stored scale.  The tensor-core kernel scales each
+ * (request, KV head)'s queries by a power of two before splitting them into fp16 high and low
+ * parts, and keeps every P' = p * s_V below 2^15 by lowering its reference maximum as larger value
+ * scales appear, so neither operand overflows fp16.  Its one precision limit: inside one
+ * (request, KV head), tokens whose value scale is more than about 2^21 times smaller than the
+ * largest value scale streamed before them by the same warp get fewer significant bits in P'
+ * (fp16 subnormals); their share of the output is that much smaller too.
  * Source: axbrief.com OSCAR page, section "attention-statistics rotation + Triton
  * kernels" (fused read path). */
 size_t oscar_decode_workspace_bytes(const oscar_cache *c);
@@ -225,6 +236,14 @@ int oscar_kernel_timing_read(oscar_cache *c, float *ms, int32_t max_n, int32_t *
  * (OSCAR_ETIMEOUT; its output is then undefined). */
 int oscar_decode_status(const void *workspace, size_t workspace_bytes, const oscar_cache *c,
                         void *stream);
+/* Limit of the bounded waits inside the decode kernels (process-wide): a wait for a page copy
+ * gives up after one test and then `iters` tests that may each sleep up to 1 ms (default 2000,
+ * about 2 s), sets the error word that oscar_decode_status / oscar_decode_status_noalloc read and
+ * ends that warp's work.  Copies already in flight are always waited for (about 2 s at most)
+ * before a warp exits.  iters = 0 makes a wait give up at its first failed test, which lets a
+ * test exercise the timeout path without a fault; iters < 0 restores the default.  Not a
+ * counterpart of anything on the OSCAR pages.  Errors: OSCAR_EINVAL (iters > 1000000). */
+int oscar_set_wait_limit(int32_t iters);
 
 /* oscar_decode_attention_noalloc: oscar_decode_attention without a workspace argument, for
  * callers that cannot allocate device memory at the time they run attention: code executing
@@ -243,11 +262,19 @@ int oscar_decode_status(const void *workspace, size_t workspace_bytes, const osc
  * the last call's contents: calls that may run at the same time on the GPU (other streams,
  * other threads, two caches) race on it and must be serialised by the caller.  Nothing in the
  * array has to start at zero: the one word that must (the flag a bounded in-kernel wait sets
- * when it gives up) is cleared by each call before its kernels read it.  That flag lives in the
- * fixed array, so oscar_decode_status cannot read it for this variant.  q, rk, out and the
- * dtypes are as for oscar_decode_attention. */
+ * when it gives up) is cleared by each call before its kernels read it.  That flag sits at a
+ * fixed place in the array; oscar_decode_status_noalloc reads it.  Like the other decode calls,
+ * this one first uploads any page-table entries and lengths that changed on the host since the
+ * last upload (cudaMemcpyAsync from the handle's host memory); a caller that wants the call to
+ * issue no host-to-device copy calls kv_page_table_sync beforehand.  q, rk, out and the dtypes
+ * are as for oscar_decode_attention. */
 int oscar_decode_attention_noalloc(oscar_cache *c, const void *q, int32_t q_dtype, const float *rk,
                                    void *out, int32_t out_dtype, void *stream);
+/* Synchronise `stream` and report whether the last oscar_decode_attention_noalloc call on the
+ * current device completed normally (OSCAR_OK) or one of its bounded in-kernel waits gave up
+ * (OSCAR_ETIMEOUT; its output is then undefined).  Allocates nothing.  No counterpart on the OSCAR
+ * pages. */
+int oscar_decode_status_noalloc(void *stream);
 
 /* ---------------------------------------------------------------- calibration
  * oscar_build_rk: R_K = U_Q * H_Had * P_br for num_kv_heads heads from n query samples

@@ -36,7 +36,7 @@ EXPORTS = [
     "oscar_decode_attention", "oscar_build_rk_workspace_bytes", "oscar_build_rk", "oscar_read_int2",
     "oscar_read_bf16", "oscar_strerror", "oscar_last_cuda_error", "oscar_launch_count",
     "oscar_set_decode_path", "oscar_decode_status", "oscar_decode_attention_noalloc", "oscar_decode_step",
-    "oscar_kernel_timing", "oscar_kernel_timing_read",
+    "oscar_kernel_timing", "oscar_kernel_timing_read", "oscar_set_wait_limit", "oscar_decode_status_noalloc",
 ]
 OSCAR_ESCRATCH = -8
 OSCAR_ETIMEOUT = -7
@@ -103,6 +103,8 @@ def lib() -> ctypes.CDLL:
         "oscar_decode_step": (ctypes.c_int, [P, P, P, P, I32, P, P, I32, P, SZ, P]),
         "oscar_kernel_timing": (ctypes.c_int, [P, I32]),
         "oscar_kernel_timing_read": (ctypes.c_int, [P, P, I32, P]),
+        "oscar_set_wait_limit": (ctypes.c_int, [I32]),
+        "oscar_decode_status_noalloc": (ctypes.c_int, [P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -257,6 +259,16 @@ def oscar_set_decode_path(path: int):
 def oscar_decode_status(cache, workspace, stream=None):
     nbytes = workspace.numel() * workspace.element_size()
     _check("oscar_decode_status", lib().oscar_decode_status(_ptr(workspace), nbytes, cache, _stream(stream)))
+
+
+def oscar_set_wait_limit(iters: int):
+    """Bounded in-kernel waits give up after `iters` tests of up to 1 ms (< 0: the default)."""
+    _check("oscar_set_wait_limit", lib().oscar_set_wait_limit(iters))
+
+
+def oscar_decode_status_noalloc(stream=None):
+    """Raise OscarError(OSCAR_ETIMEOUT) if the last fixed-scratch decode hit a bounded wait."""
+    _check("oscar_decode_status_noalloc", lib().oscar_decode_status_noalloc(_stream(stream)))
 
 
 def oscar_kernel_timing(cache, capacity: int):

@@ -330,6 +330,8 @@ int kv_quant_append(oscar_cache* c, const void* k, const void* v, const int32_t*
 
 static const int kMaxSplits = 64;   // SIMT path: INT2 splits + 1 BF16 split per (request, KV head)
 static std::atomic<int> g_decode_path{OSCAR_PATH_WARP_MMA};
+static constexpr int kDefaultWaitIters = 2000;   // about 2 s
+static std::atomic<int> g_wait_iters{kDefaultWaitIters};
 
 static int pick_pps(const oscar_cache* c) {
     int64_t total = 0;
@@ -395,6 +397,16 @@ int oscar_set_decode_path(int32_t path) {
     return OSCAR_OK;
 }
 
+int oscar_set_wait_limit(int32_t iters) {
+    if (iters < 0) {
+        g_wait_iters = kDefaultWaitIters;
+        return OSCAR_OK;
+    }
+    if (iters > 1000000) return OSCAR_EINVAL;
+    g_wait_iters = iters;
+    return OSCAR_OK;
+}
+
 int oscar_decode_status(const void* workspace, size_t workspace_bytes, const oscar_cache* c, void* stream) {
     if (!c || !workspace) return OSCAR_EINVAL;
     const WsLayout w = ws_layout(c);
@@ -446,6 +458,7 @@ static int prepare_decode(oscar_cache* c, const void* q, int32_t q_dtype, const 
     p.part_bf16 = (float*)(ws + w.bf16);
     p.err = (int32_t*)(ws + w.err);
     p.path = g_decode_path;
+    p.wait_iters = g_wait_iters;
     int64_t pages = 0;
     for (int32_t b = 0; b < c->d.batch; ++b) {
         p.len[b] = (int32_t)c->len[b];
@@ -681,6 +694,7 @@ int noalloc_decode_params(oscar_cache* c, const void* q, int32_t q_dtype, const 
     p.page_table = c->pt;
     p.max_pps = c->d.max_pages_per_seq;
     p.path = OSCAR_PATH_WARP_MMA;
+    p.wait_iters = g_wait_iters;
     int64_t pages = 0;
     for (int32_t b = 0; b < c->d.batch; ++b) {
         p.len[b] = (int32_t)c->len[b];
@@ -696,11 +710,11 @@ int noalloc_decode_params(oscar_cache* c, const void* q, int32_t q_dtype, const 
     }
     const size_t per_part = (size_t)c->g * (2 + kD) * sizeof(float);
     const size_t bh = (size_t)c->d.batch * c->d.num_kv_heads;
-    const size_t o_qrot = 0;
+    const size_t o_err = kNoallocErrOffset;   // fixed, so that oscar_decode_status_noalloc finds it
+    const size_t o_qrot = 256;
     const size_t o_mma = o_qrot + (((size_t)c->d.batch * c->d.num_q_heads * kD * sizeof(float) + 255) & ~(size_t)255);
     const size_t o_bf16 = o_mma + (bh + (size_t)p.n_warps) * per_part;
-    const size_t o_err = o_bf16 + bh * per_part;
-    if (o_err + 16 > scratch_bytes) return OSCAR_ESCRATCH;
+    if (o_bf16 + bh * per_part > scratch_bytes) return OSCAR_ESCRATCH;
     uint8_t* ws = (uint8_t*)scratch;
     p.qrot = (float*)(ws + o_qrot);
     p.part_mma = (float*)(ws + o_mma);

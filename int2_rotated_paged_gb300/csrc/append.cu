@@ -328,14 +328,17 @@ cudaError_t launch_append(const AppendParams& p, cudaStream_t s) {
     const bool few = most <= kFew;
     const size_t smem_tiled = (size_t)(kD * kD + kD * kPage) * sizeof(float) + (size_t)kPage * kD * sizeof(uint16_t);
     const size_t smem_few = (size_t)(kD * kD + kFew * kD + 8) * sizeof(float);
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(quant_pages, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)smem_tiled);
+    static bool attr_set[kMaxDevices] = {};   // once per device
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    if (!attr_set[dev]) {
+        e = cudaFuncSetAttribute(quant_pages, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_tiled);
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(quant_few, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_few);
         if (e != cudaSuccess) return e;
-        attr_set = true;
+        attr_set[dev] = true;
     }
     int n = 0;
     if (p.n_jobs > 0) {

@@ -53,7 +53,8 @@ using namespace ptx;
 // registers) for two head tiles, whose query fragments and accumulators need twice the registers
 __host__ __device__ constexpr int warps_for(int G) { return G <= 8 ? 12 : 8; }
 constexpr int kStagesPerWarp = 3;
-constexpr float kTauM = 8.0f;
+constexpr float kTauSlack = 8.0f;   // a raise of the reference max leaves the largest logit this far below tau
+constexpr float kTauMax = 40.0f;    // tau of a segment before any non-zero value scale is seen
 constexpr float kQScaleM = 1.4426950408889634f * 0.08838834764831845f;   // log2(e) / sqrt(128)
 constexpr float kTwo18 = 262144.0f;
 
@@ -99,13 +100,16 @@ struct PageIt {
     }
 };
 
-__device__ __forceinline__ bool wait_full(uint32_t bar, uint32_t parity, int* err) {
+// Wait for a stage's bulk copy: one test, then up to `iters` tests that may each sleep up to 1 ms.
+// Gives up (error word set) after that.
+__device__ __forceinline__ bool wait_full(uint32_t bar, uint32_t parity, int* err, int iters) {
     if (mbar_try(bar, parity)) return true;
-    for (int t = 0; t < 2000; ++t)
+    for (int t = 0; t < iters; ++t)
         if (mbar_try_sleep(bar, parity, 1000000)) return true;
     atomicOr(err, 1);
     return false;
 }
+constexpr int kDrainIters = 2000;   // copies in flight at a warp's exit: up to about 2 s
 
 __device__ __forceinline__ float ex2(float x) {
     float y;
@@ -187,6 +191,12 @@ __global__ void __launch_bounds__(32 * warps_for(G), 1) decode_mma(const __grid_
     float mref[MT];
     float2 lsum[MT], mv[MT][2];     // per token parity e, summed when the partial is written
     bool fresh = true;
+    float qscale = 1.f, kscale = kTwo18;   // power-of-two query scale of the segment and 2^18 / it
+    // Reference-max slack tau (log2 units): probabilities stay at most 2^tau, and tau is lowered so
+    // that 2^tau times the largest value scale seen in the segment stays below 2^15, so that
+    // P' = p * s_V cannot overflow fp16; ptau = 2^tau.  A raise of the reference puts the largest
+    // logit at tau - 8, so the dominant probabilities sit 2^8 below the limit.
+    float tau = kTauMax, ptau = __uint_as_float((uint32_t)(127 + (int)kTauMax) << 23);
     float o[8][MT][4];              // output^T accumulators: channel tile cm, head tile nh
     PageIt it;
     it.init(p, P0);
@@ -196,6 +206,33 @@ __global__ void __launch_bounds__(32 * warps_for(G), 1) decode_mma(const __grid_
     for (int i = 0; i < n; ++i) {
         const int s = i % kStagesPerWarp;
         if (seg_start) {
+            // power-of-two query scale of this (request, KV head): the largest |q~| of its G heads,
+            // times log2(e) / sqrt(128) * 2^6, lands in [2^13, 2^14), so the fp16 high parts cannot
+            // overflow and keep 11 significant bits whatever the query's magnitude.  It is exact and
+            // taken out again through the key-scale factor and the minimum sums (qs).
+            float amax = 0.f;
+#pragma unroll
+            for (int k = 0; k < MT; ++k) {
+                const int hd = g + 8 * k;
+                const float* qr = p.qrot + (((size_t)it.b * p.hkv + it.h) * G + (hd < G ? hd : 0)) * kD;
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    const float2 q0 = *reinterpret_cast<const float2*>(qr + 16 * ks + 2 * tig);
+                    const float2 q1 = *reinterpret_cast<const float2*>(qr + 16 * ks + 2 * tig + 8);
+                    if (hd < G) amax = fmaxf(amax, fmaxf(fmaxf(fabsf(q0.x), fabsf(q0.y)), fmaxf(fabsf(q1.x), fabsf(q1.y))));
+                }
+            }
+#pragma unroll
+            for (int o2 = 1; o2 < 32; o2 <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o2));
+            {
+                // floor(log2(amax * log2(e) / sqrt(128) * 64)) from the exponent field; the exponent
+                // of the scale is clamped so that 2^e stays a normal fp32 number
+                const int ex = (int)((__float_as_uint(amax * (kQScaleM * 64.f)) >> 23) & 0xff) - 127;
+                const int e = max(-120, min(120, 13 - ex));
+                qscale = __uint_as_float((uint32_t)(127 + e) << 23);
+                kscale = __uint_as_float((uint32_t)(127 + 18 - e) << 23);    // 2^18 / qscale
+            }
+            const float qinv = __uint_as_float((uint32_t)(127 + 127 - ((__float_as_uint(qscale) >> 23) & 0xff)) << 23);
             // query fragments of this (request, KV head): k-step ks holds channels 16 ks + 2 tig + e
             // (+ 8 for registers 2, 3), scaled by 2^(6 - 2 (ks mod 4)) against the key codes' 4^r
 #pragma unroll
@@ -206,7 +243,7 @@ __global__ void __launch_bounds__(32 * warps_for(G), 1) decode_mma(const __grid_
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
                     const float pw = (float)(64 >> (2 * (ks & 3)));      // 2^(6 - 2r), exact
-                    const float sc = kQScaleM * pw, inv = 1.0f / pw;
+                    const float sc = kQScaleM * pw * qscale, inv = qinv / pw;
                     const float2 q0 = *reinterpret_cast<const float2*>(qr + 16 * ks + 2 * tig);
                     const float2 q1 = *reinterpret_cast<const float2*>(qr + 16 * ks + 2 * tig + 8);
                     const float qv[2][2] = {{q0.x, q0.y}, {q1.x, q1.y}};
@@ -243,8 +280,10 @@ __global__ void __launch_bounds__(32 * warps_for(G), 1) decode_mma(const __grid_
                 for (int k = 0; k < MT; ++k) o[c][k][0] = o[c][k][1] = o[c][k][2] = o[c][k][3] = 0.f;
             seg_start = false;
             fresh = true;
+            tau = kTauMax;
+            ptau = __uint_as_float((uint32_t)(127 + (int)kTauMax) << 23);
         }
-        const bool got = wait_full(smem_u32(&sm->full[warp][s]), (i / kStagesPerWarp) & 1, p.err);
+        const bool got = wait_full(smem_u32(&sm->full[warp][s]), (i / kStagesPerWarp) & 1, p.err, p.wait_iters);
         if (!__all_sync(0xffffffffu, got)) break;      // error word set; stop issuing, drain below
         consumed = i + 1;
         const uint8_t* pg = sm->stage[warp][s];
@@ -255,26 +294,44 @@ __global__ void __launch_bounds__(32 * warps_for(G), 1) decode_mma(const __grid_
         // Slots past the request's end are staged as 0 (their bytes may be anything); a full page
         // takes a copy of the loop without that test
         auto stage = [&](const bool full) {
+        float val[2][8];
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
             const int t = lane + 32 * hh;
             const bool live = full || t < n_live;
             const uint2 ksm = *reinterpret_cast<const uint2*>(pg + kKSm + t * 8);
             const uint2 vsm = *reinterpret_cast<const uint2*>(pg + kVSm + t * 8);
-            const float val[8] = {
-                live ? kTwo18 * __half2float(__ushort_as_half(ksm.x & 0xffff)) : 0.f,
-                live ? __half2float(__ushort_as_half(ksm.x >> 16)) : 0.f,
-                live ? kTwo18 * __half2float(__ushort_as_half(ksm.y & 0xffff)) : 0.f,
-                live ? __half2float(__ushort_as_half(ksm.y >> 16)) : 0.f,
-                live ? __half2float(__ushort_as_half(vsm.x & 0xffff)) : 0.f,
-                live ? __half2float(__ushort_as_half(vsm.x >> 16)) : 0.f,
-                live ? __half2float(__ushort_as_half(vsm.y & 0xffff)) : 0.f,
-                live ? __half2float(__ushort_as_half(vsm.y >> 16)) : 0.f};
+            val[hh][0] = live ? kscale * __half2float(__ushort_as_half(ksm.x & 0xffff)) : 0.f;
+            val[hh][1] = live ? __half2float(__ushort_as_half(ksm.x >> 16)) : 0.f;
+            val[hh][2] = live ? kscale * __half2float(__ushort_as_half(ksm.y & 0xffff)) : 0.f;
+            val[hh][3] = live ? __half2float(__ushort_as_half(ksm.y >> 16)) : 0.f;
+            val[hh][4] = live ? __half2float(__ushort_as_half(vsm.x & 0xffff)) : 0.f;
+            val[hh][5] = live ? __half2float(__ushort_as_half(vsm.x >> 16)) : 0.f;
+            val[hh][6] = live ? __half2float(__ushort_as_half(vsm.y & 0xffff)) : 0.f;
+            val[hh][7] = live ? __half2float(__ushort_as_half(vsm.y >> 16)) : 0.f;
+        }
+        // value scales against the slack: 2^tau * s_V must stay below 2^15 (thread-local test; the
+        // warp-wide maximum and the new tau only on the rare path: the first page with non-zero
+        // value scales of a segment, or a page whose scales are larger than any before)
+        const float vmax = fmaxf(fmaxf(val[0][4], val[0][6]), fmaxf(val[1][4], val[1][6]));
+        if (__any_sync(0xffffffffu, vmax * ptau >= 32768.f)) {
+            float w = vmax;
+#pragma unroll
+            for (int o2 = 1; o2 < 32; o2 <<= 1) w = fmaxf(w, __shfl_xor_sync(0xffffffffu, w, o2));
+            // w * 2^tau in [2^14, 2^15): tau = 14 - floor(log2 w) (w > 0 and normal: an fp16 value)
+            const int ew = (int)((__float_as_uint(w) >> 23) & 0xff) - 127;
+            const int tnew = 14 - ew;
+            tau = (float)tnew;
+            ptau = __uint_as_float((uint32_t)(127 + tnew) << 23);
+        }
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            const int t = lane + 32 * hh;
             float* row = reinterpret_cast<float*>(&sm->tsc[warp][0][t >> 1]);
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                row[j * 128 + (t & 1)] = val[2 * j];
-                row[j * 128 + 2 + (t & 1)] = val[2 * j + 1];
+                row[j * 128 + (t & 1)] = val[hh][2 * j];
+                row[j * 128 + 2 + (t & 1)] = val[hh][2 * j + 1];
             }
         }
         };
@@ -357,7 +414,7 @@ __global__ void __launch_bounds__(32 * warps_for(G), 1) decode_mma(const __grid_
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) cm = fmaxf(cm, fmaxf(lg[k][nt].x, lg[k][nt].y));
                 cml[k] = cm;
-                hot = hot || cm > kTauM;
+                hot = hot || cm > tau;
             }
             if (__any_sync(0xffffffffu, hot)) {
                 float fown[MT], cmx[MT];
@@ -368,10 +425,12 @@ __global__ void __launch_bounds__(32 * warps_for(G), 1) decode_mma(const __grid_
                     cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, 2));
                     fown[k] = 1.f;
                     cmx[k] = 0.f;
-                    if (fresh || cm > kTauM) {
-                        fown[k] = fresh ? 0.f : ex2(-cm);
-                        mref[k] += cm;
-                        cmx[k] = cm;
+                    if (fresh || cm > tau) {
+                        // the reference rises so that the largest logit sits at tau - 8
+                        const float d = cm - (tau - kTauSlack);
+                        fown[k] = fresh ? 0.f : ex2(-d);
+                        mref[k] += d;
+                        cmx[k] = d;
                         const float2 f2 = make_float2(fown[k], fown[k]);
                         lsum[k] = __fmul2_rn(lsum[k], f2);
                         mv[k][0] = __fmul2_rn(mv[k][0], f2);
@@ -441,10 +500,11 @@ __global__ void __launch_bounds__(32 * warps_for(G), 1) decode_mma(const __grid_
                         vw[q][0][1] = w2.y;
                     }
                 }
+                // k-step outer: the MMAs into one accumulator are 8 apart
 #pragma unroll
-                for (int q = 0; q < 2; ++q)
+                for (int kk = 0; kk < KK; ++kk)
 #pragma unroll
-                    for (int kk = 0; kk < KK; ++kk) {
+                    for (int q = 0; q < 2; ++q) {
                         const uint32_t w0 = vw[q][kk][0], w1 = vw[q][kk][1];
                         const uint32_t s0 = w0 >> 8, s1 = w1 >> 8;
 #define OSCAR_PV_STEP(R)                                                                                 \
@@ -543,18 +603,23 @@ __global__ void __launch_bounds__(32 * warps_for(G), 1) decode_mma(const __grid_
     }
     // copies still in flight must land before the warp may exit (only after a timeout)
     if (lane == 0)
-        for (int q = consumed; q < issued; ++q) wait_full(smem_u32(&sm->full[warp][q % kStagesPerWarp]), (q / kStagesPerWarp) & 1, p.err);
+        for (int q = consumed; q < issued; ++q)
+            wait_full(smem_u32(&sm->full[warp][q % kStagesPerWarp]), (q / kStagesPerWarp) & 1, p.err, kDrainIters);
 }
 
 template <int G>
 cudaError_t launch_mma_g(const DecodeParams& p, cudaStream_t s) {
     constexpr int W = warps_for(G);
     const int smem = (int)sizeof(MmaSmem<W>);
-    static bool attr_set = false;   // once per instantiation (the library drives one device)
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(decode_mma<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    static bool attr_set[kMaxDevices] = {};   // once per instantiation and device
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    if (!attr_set[dev]) {
+        e = cudaFuncSetAttribute(decode_mma<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
-        attr_set = true;
+        attr_set[dev] = true;
     }
     decode_mma<G><<<p.n_warps / W, 32 * W, smem, s>>>(p);
     return cudaGetLastError();

@@ -18,6 +18,7 @@ constexpr int kWindow = 256;       // BF16 recent-window tokens
 constexpr int kSlots = kSink + kWindow;
 constexpr int kMaxBatch = 256;     // requests per call (kernel-parameter tables)
 constexpr int kMaxG = 16;          // query heads per KV head
+constexpr int kMaxDevices = 64;    // devices whose per-device launch settings are cached
 
 // Byte layout of one (physical page, KV head) block.
 constexpr int kKCodes = 0;                      // [64 tokens][32 B] key codes (k_code_byte / k_code_shift)
@@ -89,6 +90,7 @@ struct DecodeParams {
     float* part_mma;       // warp-MMA path: [batch * hkv + n_warps][g][2 + 128], slot (b * hkv + h) + warp
     float* part_bf16;      // [batch * hkv][g][2 + 128]: the BF16 sink / window split
     int32_t* err;          // nonzero after a bounded wait gave up
+    int32_t wait_iters;    // a bounded wait gives up after this many tests of up to 1 ms each
     // warp-MMA path
     int32_t total_pages;   // INT2 pages over all (request, KV head)
     int32_t n_warps;       // warps of the warp-MMA kernel
@@ -124,6 +126,9 @@ cudaError_t launch_build_rk(const float* q, int64_t n, int hkv, float* rk, void*
 size_t build_rk_ws_bytes(int hkv);
 
 void count_launches(int n);
+
+// Byte offset of the error word inside the fixed scratch of oscar_decode_attention_noalloc.
+constexpr size_t kNoallocErrOffset = 0;
 
 // Parameters of a warp-MMA decode using one fixed scratch buffer (see noalloc.cu).
 int noalloc_decode_params(oscar_cache* c, const void* q, int32_t q_dtype, const float* rk, void* out,

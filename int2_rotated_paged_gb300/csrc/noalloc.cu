@@ -8,21 +8,20 @@
 namespace {
 
 constexpr size_t kFixedScratchBytes = (size_t)16 << 20;   // 16 MiB, held by every GPU that loads us
-constexpr int kMaxDevices = 64;
 
 // The device array.  In host code its name is only a stand-in for the device address, which
 // cudaGetSymbolAddress resolves per device below.
 static __device__ __align__(256) unsigned char g_fixed_scratch[kFixedScratchBytes];
 
 std::mutex g_mu;
-void* g_addr[kMaxDevices] = {nullptr};
+void* g_addr[oscar::kMaxDevices] = {nullptr};
 
 // Device address of the array on the current device (looked up once per device).
 int fixed_scratch(void** out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return OSCAR_ECUDA;
-    if (dev < 0 || dev >= kMaxDevices) return OSCAR_EINVAL;
+    if (dev < 0 || dev >= oscar::kMaxDevices) return OSCAR_EINVAL;
     std::lock_guard<std::mutex> lk(g_mu);
     if (!g_addr[dev]) {
         void* p = nullptr;
@@ -47,4 +46,18 @@ extern "C" int oscar_decode_attention_noalloc(oscar_cache* c, const void* q, int
     if (rc != OSCAR_OK) return rc;
     cudaError_t e = oscar::launch_decode(p, (cudaStream_t)stream);
     return e == cudaSuccess ? OSCAR_OK : OSCAR_ECUDA;
+}
+
+// The error word sits at a fixed offset of the array, so it can be read without knowing the
+// layout the last call used.  Reading it allocates nothing: the copy goes to a host variable.
+extern "C" int oscar_decode_status_noalloc(void* stream) {
+    void* scratch = nullptr;
+    int rc = fixed_scratch(&scratch);
+    if (rc != OSCAR_OK) return rc;
+    int32_t err = 0;
+    cudaError_t e = cudaMemcpyAsync(&err, (const unsigned char*)scratch + oscar::kNoallocErrOffset, sizeof(err),
+                                    cudaMemcpyDeviceToHost, (cudaStream_t)stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize((cudaStream_t)stream);
+    if (e != cudaSuccess) return OSCAR_ECUDA;
+    return err ? OSCAR_ETIMEOUT : OSCAR_OK;
 }

@@ -183,9 +183,22 @@ def test_build_rv_on_gpu_from_score_weighted_values():
     torch.cuda.synchronize()
     got = rv.cpu().numpy().astype(np.float64)
     for h in range(hkv):
-        _, ref64, _ = oracle.build_rk(ys[h])          # the oracle's builder on the same samples
-        assert np.abs(got[h] - ref64).max() < 1e-6
+        _, ref64, ev = oracle.build_rk(ys[h])         # the oracle's builder on the same samples
         assert np.abs(got[h] @ got[h].T - np.eye(128)).max() < 1e-6
+        # invariants that hold whatever the eigen-gaps: R_V = U_S H P_br with H P_br known, so
+        # U_S = R_V (H P_br)^T must diagonalise C_S with the oracle's eigenvalues, descending
+        c = ys[h].astype(np.float64).T @ ys[h].astype(np.float64) / n
+        hp = oracle.build_rk(np.eye(128, dtype=np.float32))[1]      # C = I/N: R = H P_br exactly
+        u = got[h] @ hp.T
+        lam = np.diag(u.T @ c @ u)
+        off = u.T @ c @ u - np.diag(lam)
+        assert np.abs(off).max() <= 1e-6 * np.abs(ev).max()
+        assert np.abs(lam - ev).max() <= 1e-6 * np.abs(ev).max()
+        # element-wise agreement with the oracle's vectors, where the eigen-gaps make them unique
+        gap = np.minimum(np.r_[np.inf, -np.diff(ev)], np.r_[-np.diff(ev), np.inf])
+        unique = gap > 1e-4 * np.abs(ev).max()
+        u_ref = ref64 @ hp.T
+        assert np.abs(u[:, unique] - u_ref[:, unique]).max() < 1e-5
 
 
 def test_build_rk_on_gpu_matches_oracle():

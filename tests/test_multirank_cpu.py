@@ -51,3 +51,25 @@ def test_reference_arm_under_torchrun_prints_one_line():
     rec = json.loads(lines[0])
     assert rec["impl"] == "reference" and rec["n_gpus"] == 2 and rec["value"] > 0
     assert rec["e2e"]["h2d_bytes_per_step"] == 0 and rec["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_gpus_flag_without_torchrun_starts_that_many_ranks():
+    # `bench.py --gpus 2` outside torchrun relaunches itself with two ranks; both arms report the
+    # world size they ran with
+    cmd = [sys.executable, "bench.py", "--impl", "reference", "--gpus", "2", "--config", "tiny", "--steps", "1",
+           "--warmup", "1", "--ref-pairs", "1"]
+    env = dict(os.environ, OMP_NUM_THREADS="1")
+    env.pop("WORLD_SIZE", None)
+    r = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=300, env=env)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    rec = json.loads(lines[0])
+    assert rec["n_gpus"] == 2 and rec["world_size"] == 2
+
+
+def test_gpus_flag_must_match_world_size():
+    cmd = [sys.executable, "bench.py", "--impl", "reference", "--gpus", "3", "--config", "tiny"]
+    env = dict(os.environ, WORLD_SIZE="1", RANK="0")
+    r = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=120, env=env)
+    assert r.returncode != 0 and "WORLD_SIZE" in r.stderr

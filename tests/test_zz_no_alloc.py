@@ -5,8 +5,11 @@ engine's plugin hook that forbids allocation, in a real-time loop that must not 
 allocator, or next to another runtime that has already reserved all device memory.  For them
 the library offers a variant that takes no workspace and uses one fixed scratch array built
 into the library.  These tests check, through the C ABI, that it returns what the regular
-entry point returns (same tolerance as the other parity tests) on two calls in a row, and that
-a call too large for the fixed scratch is refused before anything is enqueued.
+entry point returns (same tolerance as the other parity tests) on two calls in a row, that a
+warm call changes neither torch's allocator nor the device's free memory, that a bounded
+in-kernel wait that runs out is reported by oscar_decode_status_noalloc (and the next call is
+correct again), and that a call too large for the fixed scratch is refused before anything is
+enqueued.
 """
 import numpy as np
 import pytest
@@ -45,6 +48,53 @@ def test_noalloc_matches_regular_entry_point_twice():
         r, g = ref.cpu().numpy(), got.cpu().numpy()
         assert np.isfinite(g).all()
         assert rel_l2(g, r) <= REL_L2 and np.abs(g - r).max() <= MAX_ABS
+
+
+def test_noalloc_allocates_nothing():
+    cfg = synth.scaled(synth.config("qwen3_4b"), [3000, 1200], batch=2)
+    rk = torch.tensor(oracle_rk(cfg.seed, cfg.num_kv_heads, 1024), device="cuda")
+    cache = make_cache(cfg, max(cfg.ctx) + 2)
+    append_initial(cache, cfg, cfg.ctx, rk)
+    q = decode_query(cfg, 0)
+    out = torch.empty_like(q)
+    K.oscar_decode_attention_noalloc(cache.handle, q, K.DTYPE_F32, rk, out, K.DTYPE_F32)   # warm
+    torch.cuda.synchronize()
+    alloc0 = torch.cuda.memory_allocated()
+    free0, _ = torch.cuda.mem_get_info()
+    for _ in range(3):
+        K.oscar_decode_attention_noalloc(cache.handle, q, K.DTYPE_F32, rk, out, K.DTYPE_F32)
+    torch.cuda.synchronize()                 # raises if the calls left a CUDA error behind
+    K.oscar_decode_status_noalloc()
+    assert torch.cuda.memory_allocated() == alloc0
+    free1, _ = torch.cuda.mem_get_info()
+    assert free1 == free0
+
+
+def test_noalloc_reports_a_wait_that_ran_out():
+    # a wait limit of zero makes the page-copy waits give up at their first failed test: the call
+    # must report OSCAR_ETIMEOUT through the status query, and the next call, with the default
+    # limit, must be correct again
+    cfg = synth.scaled(synth.config("qwen3_8b"), [32768] * 8, batch=8)
+    rk = torch.tensor(oracle_rk(cfg.seed, cfg.num_kv_heads, 1024), device="cuda")
+    cache = make_cache(cfg, max(cfg.ctx) + 2)
+    append_initial(cache, cfg, cfg.ctx, rk, chunks=[16384, 16384])
+    q = decode_query(cfg, 0)
+    ref = torch.empty_like(q)
+    cache.attend(q, rk, ref)
+    got = torch.empty_like(q)
+    K.oscar_set_wait_limit(0)
+    try:
+        K.oscar_decode_attention_noalloc(cache.handle, q, K.DTYPE_F32, rk, got, K.DTYPE_F32)
+        with pytest.raises(K.OscarError) as e:
+            K.oscar_decode_status_noalloc()
+        assert e.value.code == K.OSCAR_ETIMEOUT
+    finally:
+        K.oscar_set_wait_limit(-1)
+    torch.cuda.synchronize()
+    K.oscar_decode_attention_noalloc(cache.handle, q, K.DTYPE_F32, rk, got, K.DTYPE_F32)
+    K.oscar_decode_status_noalloc()
+    r, g = ref.cpu().numpy(), got.cpu().numpy()
+    assert rel_l2(g, r) <= REL_L2 and np.abs(g - r).max() <= MAX_ABS
 
 
 def test_noalloc_refuses_calls_beyond_its_scratch():
