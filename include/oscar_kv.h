@@ -244,6 +244,14 @@ int oscar_decode_status(const void *workspace, size_t workspace_bytes, const osc
  * test exercise the timeout path without a fault; iters < 0 restores the default.  Not a
  * counterpart of anything on the OSCAR pages.  Errors: OSCAR_EINVAL (iters > 1000000). */
 int oscar_set_wait_limit(int32_t iters);
+/* Timeout-path check (process-wide, default off): with on != 0, the first kernel of every
+ * warp-MMA decode call also makes one bounded wait on a shared-memory barrier that nothing
+ * arrives at.  It runs out after the wait limit above, sets the same error word a page copy that
+ * never lands would set (so oscar_decode_status / oscar_decode_status_noalloc report
+ * OSCAR_ETIMEOUT), and the call otherwise completes normally.  It lets a test exercise the
+ * timeout reporting without any fault; it is not for production use.  No counterpart on the
+ * OSCAR pages.  Always returns OSCAR_OK. */
+int oscar_set_wait_probe(int32_t on);
 
 /* oscar_decode_attention_noalloc: oscar_decode_attention without a workspace argument, for
  * callers that cannot allocate device memory at the time they run attention: code executing

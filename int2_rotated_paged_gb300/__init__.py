@@ -37,6 +37,7 @@ EXPORTS = [
     "oscar_read_bf16", "oscar_strerror", "oscar_last_cuda_error", "oscar_launch_count",
     "oscar_set_decode_path", "oscar_decode_status", "oscar_decode_attention_noalloc", "oscar_decode_step",
     "oscar_kernel_timing", "oscar_kernel_timing_read", "oscar_set_wait_limit", "oscar_decode_status_noalloc",
+    "oscar_set_wait_probe",
 ]
 OSCAR_ESCRATCH = -8
 OSCAR_ETIMEOUT = -7
@@ -104,6 +105,7 @@ def lib() -> ctypes.CDLL:
         "oscar_kernel_timing": (ctypes.c_int, [P, I32]),
         "oscar_kernel_timing_read": (ctypes.c_int, [P, P, I32, P]),
         "oscar_set_wait_limit": (ctypes.c_int, [I32]),
+        "oscar_set_wait_probe": (ctypes.c_int, [I32]),
         "oscar_decode_status_noalloc": (ctypes.c_int, [P]),
     }
     for name, (res, args) in sig.items():
@@ -264,6 +266,11 @@ def oscar_decode_status(cache, workspace, stream=None):
 def oscar_set_wait_limit(iters: int):
     """Bounded in-kernel waits give up after `iters` tests of up to 1 ms (< 0: the default)."""
     _check("oscar_set_wait_limit", lib().oscar_set_wait_limit(iters))
+
+
+def oscar_set_wait_probe(on: bool):
+    """Timeout-path check: decode calls also wait, bounded, on a barrier nothing arrives at."""
+    _check("oscar_set_wait_probe", lib().oscar_set_wait_probe(1 if on else 0))
 
 
 def oscar_decode_status_noalloc(stream=None):

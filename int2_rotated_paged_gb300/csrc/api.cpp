@@ -332,6 +332,7 @@ static const int kMaxSplits = 64;   // SIMT path: INT2 splits + 1 BF16 split per
 static std::atomic<int> g_decode_path{OSCAR_PATH_WARP_MMA};
 static constexpr int kDefaultWaitIters = 2000;   // about 2 s
 static std::atomic<int> g_wait_iters{kDefaultWaitIters};
+static std::atomic<int> g_wait_probe{0};
 
 static int pick_pps(const oscar_cache* c) {
     int64_t total = 0;
@@ -407,6 +408,11 @@ int oscar_set_wait_limit(int32_t iters) {
     return OSCAR_OK;
 }
 
+int oscar_set_wait_probe(int32_t on) {
+    g_wait_probe = on ? 1 : 0;
+    return OSCAR_OK;
+}
+
 int oscar_decode_status(const void* workspace, size_t workspace_bytes, const oscar_cache* c, void* stream) {
     if (!c || !workspace) return OSCAR_EINVAL;
     const WsLayout w = ws_layout(c);
@@ -459,6 +465,7 @@ static int prepare_decode(oscar_cache* c, const void* q, int32_t q_dtype, const 
     p.err = (int32_t*)(ws + w.err);
     p.path = g_decode_path;
     p.wait_iters = g_wait_iters;
+    p.wait_probe = g_wait_probe;
     int64_t pages = 0;
     for (int32_t b = 0; b < c->d.batch; ++b) {
         p.len[b] = (int32_t)c->len[b];
@@ -695,6 +702,7 @@ int noalloc_decode_params(oscar_cache* c, const void* q, int32_t q_dtype, const 
     p.max_pps = c->d.max_pages_per_seq;
     p.path = OSCAR_PATH_WARP_MMA;
     p.wait_iters = g_wait_iters;
+    p.wait_probe = g_wait_probe;
     int64_t pages = 0;
     for (int32_t b = 0; b < c->d.batch; ++b) {
         p.len[b] = (int32_t)c->len[b];

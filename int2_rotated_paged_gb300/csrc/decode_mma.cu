@@ -20,11 +20,14 @@
 //            in one 8-byte load, and each B register is one AND of a code word (or of the word
 //            shifted right by 8) with 0x00030003 << 2r: two fp16 subnormals code * 4^r * 2^-24,
 //            exact.  The 4^r of k-step ks (r = ks mod 4) is taken out of the query side
-//            (A = q~ * 2^(6 - 2r)).  One accumulator per 64-channel group because each group
-//            has its own scale: logit = 2^18 s_g S_g + m_g sum_{c in g} q~_c (log2 units);
+//            (A = q~ * 2^(6 - 2r)), and the query of each (request, KV head) is scaled by a power
+//            of two so that its largest high part sits in [2^13, 2^14).  One accumulator per
+//            64-channel group because each group has its own scale:
+//            logit = 2^18 s_g S_g / qscale + m_g sum_{c in g} q~_c (log2 units);
 //   softmax  online, per head, with a lazily raised reference max (output rescaled only when a
-//            logit passes the reference by 2^8, tested per thread first, so the row-group max
-//            reduction runs only on that rare path); logits are formed relative to the reference
+//            logit passes the reference by 2^tau, tested per thread first, so the row-group max
+//            reduction runs only on that rare path; tau is chosen per segment from the largest
+//            value scale so that P' stays inside fp16); logits are formed relative to the reference
 //            and all the per-token arithmetic runs on packed fp32 pairs (f32x2 FMA / MUL / ADD:
 //            the two tokens 2 tig, 2 tig + 1 of a score column pair), which halves the FP32
 //            instructions and, unlike scalar FFMA, overlaps the MMAs almost fully;
@@ -53,7 +56,12 @@ using namespace ptx;
 // registers) for two head tiles, whose query fragments and accumulators need twice the registers
 __host__ __device__ constexpr int warps_for(int G) { return G <= 8 ? 12 : 8; }
 constexpr int kStagesPerWarp = 3;
-constexpr float kTauSlack = 8.0f;   // a raise of the reference max leaves the largest logit this far below tau
+// A raise of the reference max leaves the largest logit this far below tau.  The half step keeps
+// the largest probabilities off exact powers of two: with p = 2^k (1 - e) for a nearly flat
+// attention, fp16(p * s_V) would round back to the fp16 value 2^k s_V for every token, a bias
+// that the output's cancellation between sum P' code and sum p m_V magnifies; at 2^(k + 1/2) the
+// rounding errors are spread evenly and average out.
+constexpr float kTauSlack = 7.5f;
 constexpr float kTauMax = 40.0f;    // tau of a segment before any non-zero value scale is seen
 constexpr float kQScaleM = 1.4426950408889634f * 0.08838834764831845f;   // log2(e) / sqrt(128)
 constexpr float kTwo18 = 262144.0f;
@@ -195,7 +203,7 @@ __global__ void __launch_bounds__(32 * warps_for(G), 1) decode_mma(const __grid_
     // Reference-max slack tau (log2 units): probabilities stay at most 2^tau, and tau is lowered so
     // that 2^tau times the largest value scale seen in the segment stays below 2^15, so that
     // P' = p * s_V cannot overflow fp16; ptau = 2^tau.  A raise of the reference puts the largest
-    // logit at tau - 8, so the dominant probabilities sit 2^8 below the limit.
+    // logit at tau - 7.5, so the dominant probabilities sit about 2^7.5 below the limit.
     float tau = kTauMax, ptau = __uint_as_float((uint32_t)(127 + (int)kTauMax) << 23);
     float o[8][MT][4];              // output^T accumulators: channel tile cm, head tile nh
     PageIt it;
@@ -426,7 +434,7 @@ __global__ void __launch_bounds__(32 * warps_for(G), 1) decode_mma(const __grid_
                     fown[k] = 1.f;
                     cmx[k] = 0.f;
                     if (fresh || cm > tau) {
-                        // the reference rises so that the largest logit sits at tau - 8
+                        // the reference rises so that the largest logit sits at tau - 7.5
                         const float d = cm - (tau - kTauSlack);
                         fown[k] = fresh ? 0.f : ex2(-d);
                         mref[k] += d;

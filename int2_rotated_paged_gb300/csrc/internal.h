@@ -91,6 +91,7 @@ struct DecodeParams {
     float* part_bf16;      // [batch * hkv][g][2 + 128]: the BF16 sink / window split
     int32_t* err;          // nonzero after a bounded wait gave up
     int32_t wait_iters;    // a bounded wait gives up after this many tests of up to 1 ms each
+    int32_t wait_probe;    // nonzero: the first kernel also waits on a barrier nothing arrives at
     // warp-MMA path
     int32_t total_pages;   // INT2 pages over all (request, KV head)
     int32_t n_warps;       // warps of the warp-MMA kernel

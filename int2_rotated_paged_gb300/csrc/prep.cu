@@ -17,6 +17,7 @@
 #include <cuda_bf16.h>
 
 #include "internal.h"
+#include "ptx_async.h"
 #include "token_quant.h"
 
 namespace oscar {
@@ -70,7 +71,20 @@ __device__ __forceinline__ void prep_body(const DecodeParams& p, const AppendPar
     __shared__ float ow[kPrepWarps][G][kD];
     const int h = blockIdx.x, b = blockIdx.y, c = threadIdx.x;
     const int warp = c >> 5, lane = c & 31, g = lane >> 2, tig = lane & 3;
-    if (b == 0 && h == 0 && c == 0 && p.err) *p.err = 0;
+    if (b == 0 && h == 0 && c == 0 && p.err) {
+        *p.err = 0;
+        if (p.wait_probe) {
+            // timeout-path check: a bounded wait on a barrier that nothing arrives at runs out and
+            // sets the error word, exactly as a page copy that never lands would
+            __shared__ uint64_t probe;
+            const uint32_t bar = ptx::smem_u32(&probe);
+            ptx::mbar_init(bar, 1);
+            ptx::fence_mbar_init();
+            bool done = ptx::mbar_try(bar, 0);
+            for (int t = 0; t < p.wait_iters && !done; ++t) done = ptx::mbar_try_sleep(bar, 0, 1000000);
+            if (!done) atomicOr(p.err, 1);
+        }
+    }
     const size_t qbase = ((size_t)b * p.hkv + h) * G * kD;
 
     __shared__ float xk[STEP ? kD : 1];              // key leaving the window (fp32)

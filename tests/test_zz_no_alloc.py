@@ -71,24 +71,26 @@ def test_noalloc_allocates_nothing():
 
 
 def test_noalloc_reports_a_wait_that_ran_out():
-    # a wait limit of zero makes the page-copy waits give up at their first failed test: the call
-    # must report OSCAR_ETIMEOUT through the status query, and the next call, with the default
-    # limit, must be correct again
-    cfg = synth.scaled(synth.config("qwen3_8b"), [32768] * 8, batch=8)
+    # the probe makes the call's first kernel wait on a barrier nothing arrives at, with a short
+    # limit (5 tests of up to 1 ms): the wait runs out, the call must report OSCAR_ETIMEOUT through
+    # the status query, and the next call, without the probe, must be correct again
+    cfg = synth.scaled(synth.config("qwen3_4b"), [2500, 900], batch=2)
     rk = torch.tensor(oracle_rk(cfg.seed, cfg.num_kv_heads, 1024), device="cuda")
     cache = make_cache(cfg, max(cfg.ctx) + 2)
-    append_initial(cache, cfg, cfg.ctx, rk, chunks=[16384, 16384])
+    append_initial(cache, cfg, cfg.ctx, rk)
     q = decode_query(cfg, 0)
     ref = torch.empty_like(q)
     cache.attend(q, rk, ref)
     got = torch.empty_like(q)
-    K.oscar_set_wait_limit(0)
+    K.oscar_set_wait_limit(5)
+    K.oscar_set_wait_probe(True)
     try:
         K.oscar_decode_attention_noalloc(cache.handle, q, K.DTYPE_F32, rk, got, K.DTYPE_F32)
         with pytest.raises(K.OscarError) as e:
             K.oscar_decode_status_noalloc()
         assert e.value.code == K.OSCAR_ETIMEOUT
     finally:
+        K.oscar_set_wait_probe(False)
         K.oscar_set_wait_limit(-1)
     torch.cuda.synchronize()
     K.oscar_decode_attention_noalloc(cache.handle, q, K.DTYPE_F32, rk, got, K.DTYPE_F32)
