@@ -63,12 +63,15 @@ extern "C" {
 /* Fixed geometry of this implementation. */
 #define OSCAR_HEAD_DIM 128
 #define OSCAR_PAGE_TOKENS 64   /* INT2 tokens per page */
-#define OSCAR_GROUP 64         /* channels per quantisation group */
+#define OSCAR_GROUP 64         /* default channels per quantisation group (64 or 128 per tensor) */
 #define OSCAR_MAX_GQA 16       /* largest num_q_heads / num_kv_heads */
-/* Bytes of one (page, KV head) block: K codes 2048 (32 per token), K scale/min 64x8,
- * V codes 2048, V scale/min 64x8.  Inside the two code regions the 2-bit codes are stored in
- * the order the decode kernel's tensor-core fragments read them (not the logical order);
- * oscar_read_int2 returns them in the logical order. */
+/* Bytes of one (page, KV head) block with 64-channel groups for keys and values: K codes 2048
+ * (32 per token), K scale/min 64x8, V codes 2048, V scale/min 64x8.  A tensor quantised in
+ * 128-channel groups keeps one scale/min pair per token (64x4 bytes): 4864 bytes with keys in
+ * groups of 64 and values in groups of 128, 4608 with both in groups of 128
+ * (oscar_page_head_bytes).  Inside the two code regions the 2-bit codes are stored in the order
+ * the decode kernel's tensor-core fragments read them (not the logical order); oscar_read_int2
+ * returns them in the logical order. */
 #define OSCAR_PAGE_HEAD_BYTES 5120
 
 typedef struct {
@@ -77,25 +80,34 @@ typedef struct {
     int32_t num_q_heads;       /* num_kv_heads * G, G in {1..8, 12, 16} */
     int32_t head_dim;          /* must be 128 */
     int32_t page_size;         /* must be 64 */
-    int32_t group_size;        /* must be 64 */
+    int32_t group_size;        /* key quantisation group: 64 or 128 channels */
     int32_t sink;              /* BF16 sink tokens, must be 64 */
     int32_t window;            /* BF16 recent-window tokens, must be 256 */
     int32_t max_pages_total;   /* physical INT2 pages in the pool, >= 1 */
     int32_t max_pages_per_seq; /* INT2 pages one request may hold, >= 1 */
     float clip_k;              /* key clip factor, 0 < c <= 1 (default 0.96) */
     float clip_v;              /* value clip factor, 0 < c <= 1 (default 0.92) */
+    int32_t group_size_v;      /* value quantisation group: 64 or 128 channels; 0 = group_size */
 } oscar_cache_desc;
 
 typedef struct oscar_cache oscar_cache; /* opaque host handle */
 
-/* Fill *d with the defaults (head_dim 128, page 64, group 64, sink 64, window 256,
- * clip 0.96 / 0.92); the caller then sets batch, heads and the page counts. */
+/* Fill *d with the defaults (head_dim 128, page 64, groups of 64 for keys and values, sink 64,
+ * window 256, clip 0.96 / 0.92); the caller then sets batch, heads and the page counts.
+ * The group sizes select the page format.  Groups of 64 are the OSCAR pages' G_K = 64 (axbrief.com
+ * OSCAR page, section "attention-statistics rotation + Triton kernels"); keys in groups of 64 with
+ * values in groups of 128 (2.375 bits per stored value) and both in groups of 128 (2.25 bits, 2.28
+ * with the BF16 sink and window of a 128K context) are the configurations behind the 2.38 and 2.28
+ * effective bits the same page reports (section "Naive INT2 0 vs OSCAR 71.86"). */
 void oscar_default_desc(oscar_cache_desc *d);
+/* Bytes of one (page, KV head) block of the pool for the descriptor's group sizes (5120, 4864 or
+ * 4608), or 0 if *d is invalid. */
+size_t oscar_page_head_bytes(const oscar_cache_desc *d);
 
 /* Device buffer sizes (bytes) the caller must allocate for a cache described by *d;
  * 0 if *d is invalid.
- *   pool:       max_pages_total * num_kv_heads * OSCAR_PAGE_HEAD_BYTES; physical page p,
- *               KV head h starts at byte (p * num_kv_heads + h) * OSCAR_PAGE_HEAD_BYTES.
+ *   pool:       max_pages_total * num_kv_heads * oscar_page_head_bytes(d); physical page p,
+ *               KV head h starts at byte (p * num_kv_heads + h) * oscar_page_head_bytes(d).
  *   bf16:       batch * num_kv_heads * 2 * (sink + window) * 128 bf16 values, laid out
  *               [b][h][K|V][slot][128]; slot = pos for pos < sink, else
  *               sink + (pos - sink) % window.
@@ -306,8 +318,8 @@ int oscar_build_rk(const float *q, int64_t n, int32_t num_kv_heads, float *rk, v
  * Copy n INT2 tokens of request b, KV head h, starting at position pos0 (each position
  * must lie in the INT2 history) into host buffers, in the per-token logical format:
  * codes [n][32] bytes (channel 4i+j in bits 2j..2j+1 of byte i) and scale/min
- * [n][4] fp16 bit patterns (s0, m0, s1, m1), for K and V.  Any host pointer may be
- * NULL.  Synchronises `stream`. */
+ * [n][2 * 128 / group] fp16 bit patterns (s0, m0, s1, m1 for groups of 64; s, m for groups of
+ * 128), for K and V.  Any host pointer may be NULL.  Synchronises `stream`. */
 int oscar_read_int2(const oscar_cache *c, int32_t b, int32_t h, int64_t pos0, int64_t n,
                     uint8_t *k_codes, uint16_t *k_sm, uint8_t *v_codes, uint16_t *v_sm,
                     void *stream);

@@ -37,7 +37,7 @@ EXPORTS = [
     "oscar_read_bf16", "oscar_strerror", "oscar_last_cuda_error", "oscar_launch_count",
     "oscar_set_decode_path", "oscar_decode_status", "oscar_decode_attention_noalloc", "oscar_decode_step",
     "oscar_kernel_timing", "oscar_kernel_timing_read", "oscar_set_wait_limit", "oscar_decode_status_noalloc",
-    "oscar_set_wait_probe",
+    "oscar_set_wait_probe", "oscar_page_head_bytes",
 ]
 OSCAR_ESCRATCH = -8
 OSCAR_ETIMEOUT = -7
@@ -56,7 +56,8 @@ class CacheDesc(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "batch", "num_kv_heads", "num_q_heads", "head_dim", "page_size", "group_size", "sink",
         "window", "max_pages_total", "max_pages_per_seq")] + [("clip_k", ctypes.c_float),
-                                                              ("clip_v", ctypes.c_float)]
+                                                              ("clip_v", ctypes.c_float),
+                                                              ("group_size_v", ctypes.c_int32)]
 
 
 _lib = None
@@ -76,6 +77,7 @@ def lib() -> ctypes.CDLL:
     sig = {
         "oscar_default_desc": (None, [DP]),
         "oscar_pool_bytes": (SZ, [DP]),
+        "oscar_page_head_bytes": (SZ, [DP]),
         "oscar_bf16_bytes": (SZ, [DP]),
         "oscar_page_table_bytes": (SZ, [DP]),
         "oscar_seq_lens_bytes": (SZ, [DP]),
@@ -228,13 +230,14 @@ def oscar_build_rk(q, n: int, num_kv_heads: int, rk, workspace, stream=None):
                                                   nbytes, _stream(stream)))
 
 
-def oscar_read_int2(cache, b: int, h: int, pos0: int, n: int, stream=None):
-    """(k_codes [n,32] u8, k_sm [n,4] u16, v_codes, v_sm) as numpy arrays, logical per-token format."""
+def oscar_read_int2(cache, b: int, h: int, pos0: int, n: int, stream=None, group_k: int = 64, group_v: int = 64):
+    """(k_codes [n,32] u8, k_sm [n, 2*128/group_k] u16, v_codes, v_sm [n, 2*128/group_v]) as numpy
+    arrays, logical per-token format (the group sizes must be the cache's)."""
     import numpy as np
     kc = np.zeros((n, 32), np.uint8)
-    ks = np.zeros((n, 4), np.uint16)
+    ks = np.zeros((n, 256 // group_k), np.uint16)
     vc = np.zeros((n, 32), np.uint8)
-    vs = np.zeros((n, 4), np.uint16)
+    vs = np.zeros((n, 256 // group_v), np.uint16)
     p = lambda a: a.ctypes.data_as(ctypes.c_void_p)
     _check("oscar_read_int2", lib().oscar_read_int2(cache, b, h, pos0, n, p(kc), p(ks), p(vc), p(vs),
                                                     _stream(stream)))
@@ -301,13 +304,15 @@ class Cache:
 
     def __init__(self, batch: int, num_q_heads: int, num_kv_heads: int, max_pages_total: int,
                  max_pages_per_seq: int, page_order: Optional[Sequence[int]] = None,
-                 clip_k: float = 0.96, clip_v: float = 0.92, device="cuda"):
+                 clip_k: float = 0.96, clip_v: float = 0.92, device="cuda", group_k: int = 64, group_v: int = 64):
         import torch
         d = default_desc()
         d.batch, d.num_q_heads, d.num_kv_heads = batch, num_q_heads, num_kv_heads
         d.max_pages_total, d.max_pages_per_seq = max_pages_total, max_pages_per_seq
         d.clip_k, d.clip_v = clip_k, clip_v
+        d.group_size, d.group_size_v = group_k, group_v
         self.desc = d
+        self.group_k, self.group_v = group_k, group_v
         L = lib()
         sizes = [L.oscar_pool_bytes(ctypes.byref(d)), L.oscar_bf16_bytes(ctypes.byref(d)),
                  L.oscar_page_table_bytes(ctypes.byref(d)), L.oscar_seq_lens_bytes(ctypes.byref(d))]
@@ -348,3 +353,10 @@ class Cache:
 
     def length(self, b: int) -> int:
         return oscar_cache_length(self.handle, b)
+
+    def read_int2(self, b: int, h: int, pos0: int, n: int):
+        """INT2 codes and scale/min of n tokens in the logical per-token format (oscar_read_int2)."""
+        return oscar_read_int2(self.handle, b, h, pos0, n, group_k=self.group_k, group_v=self.group_v)
+
+    def page_head_bytes(self) -> int:
+        return int(lib().oscar_page_head_bytes(ctypes.byref(self.desc)))

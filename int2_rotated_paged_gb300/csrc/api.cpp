@@ -23,6 +23,7 @@ struct oscar_cache {
     bool clear_device;                        // the device table / lengths need zeroing
     bool lens_dirty;
     int32_t g;
+    PageFmt fmt;                              // byte layout of a (page, KV head) block
     // optional per-launch timing of the decode kernel: event pairs, filled in launch order
     std::vector<cudaEvent_t> timing_ev;
     int32_t timing_used = 0;
@@ -53,7 +54,9 @@ bool desc_ok(const oscar_cache_desc* d) {
     if (d->num_q_heads % d->num_kv_heads) return false;
     const int g = d->num_q_heads / d->num_kv_heads;
     if (g > kMaxG || (g > 8 && g != 12 && g != 16)) return false;
-    if (d->head_dim != kD || d->page_size != kPage || d->group_size != kGroup) return false;
+    if (d->head_dim != kD || d->page_size != kPage) return false;
+    if (d->group_size != 64 && d->group_size != 128) return false;
+    if (d->group_size_v != 0 && d->group_size_v != 64 && d->group_size_v != 128) return false;
     if (d->sink != kSink || d->window != kWindow) return false;
     if (d->max_pages_total < 1 || d->max_pages_per_seq < 1) return false;
     if (!(d->clip_k > 0.f && d->clip_k <= 1.f && d->clip_v > 0.f && d->clip_v <= 1.f)) return false;
@@ -61,6 +64,10 @@ bool desc_ok(const oscar_cache_desc* d) {
 }
 
 cudaStream_t S(void* s) { return (cudaStream_t)s; }
+
+PageFmt fmt_of(const oscar_cache_desc* d) {
+    return page_fmt(d->group_size, d->group_size_v ? d->group_size_v : d->group_size);
+}
 
 // Pages the INT2 history of a request needs once it holds `len` tokens.
 int64_t pages_for(int64_t len) {
@@ -127,6 +134,7 @@ void oscar_default_desc(oscar_cache_desc* d) {
     d->head_dim = kD;
     d->page_size = kPage;
     d->group_size = kGroup;
+    d->group_size_v = kGroup;
     d->sink = kSink;
     d->window = kWindow;
     d->max_pages_total = 1;
@@ -135,9 +143,13 @@ void oscar_default_desc(oscar_cache_desc* d) {
     d->clip_v = 0.92f;
 }
 
+size_t oscar_page_head_bytes(const oscar_cache_desc* d) {
+    if (!desc_ok(d)) return 0;
+    return (size_t)fmt_of(d).bytes;
+}
 size_t oscar_pool_bytes(const oscar_cache_desc* d) {
     if (!desc_ok(d)) return 0;
-    return (size_t)d->max_pages_total * d->num_kv_heads * kPageHeadBytes;
+    return (size_t)d->max_pages_total * d->num_kv_heads * fmt_of(d).bytes;
 }
 size_t oscar_bf16_bytes(const oscar_cache_desc* d) {
     if (!desc_ok(d)) return 0;
@@ -161,6 +173,8 @@ int oscar_cache_create(const oscar_cache_desc* d, void* pool, void* bf16, int32_
         return OSCAR_EALIGN;
     oscar_cache* c = new oscar_cache();
     c->d = *d;
+    if (!c->d.group_size_v) c->d.group_size_v = c->d.group_size;
+    c->fmt = fmt_of(&c->d);
     c->pool = (uint8_t*)pool;
     c->bf16 = (uint16_t*)bf16;
     c->pt = page_table;
@@ -282,6 +296,7 @@ static int prepare_append(oscar_cache* c, const void* k, const void* v, const in
     int rc = sync(c, s);
     if (rc != OSCAR_OK) return rc;
     std::memset(&p, 0, sizeof(p));
+    p.fmt = c->fmt;
     p.batch = d.batch;
     p.hkv = d.num_kv_heads;
     p.clip_k = d.clip_k;
@@ -360,13 +375,13 @@ static int sm_count() {
     return cached[dev];
 }
 
-// Warps of the warp-MMA kernel: one CTA per SM (fewer when there are few pages).
-static int mma_warp_count(int32_t g, int64_t pages, int32_t* n_warps) {
+// Page-streaming units (warp pairs) of the warp-MMA kernel: one CTA per SM (fewer when there are few pages).
+static int mma_unit_count(int32_t g, int64_t pages, int32_t* n_units) {
     const int sms = sm_count();
     if (sms <= 0) return cuda_fail(cudaGetLastError());
-    const int per = mma_warps_per_cta(g);
-    const int64_t ctas = std::min<int64_t>(std::min(sms, kMaxMmaWarps / per), (pages + per - 1) / per);
-    *n_warps = (int32_t)(ctas * per);
+    const int per = mma_units_per_cta(g);
+    const int64_t ctas = std::min<int64_t>(std::min(sms, kMaxMmaUnits / per), (pages + per - 1) / per);
+    *n_units = (int32_t)(ctas * per);
     return OSCAR_OK;
 }
 
@@ -381,7 +396,7 @@ static WsLayout ws_layout(const oscar_cache* c) {
     w.qrot = 0;
     w.simt = w.qrot + (size_t)c->d.batch * c->d.num_q_heads * kD * sizeof(float);
     w.mma = w.simt + bh * kMaxSplits * per;
-    w.bf16 = w.mma + (bh + kMaxMmaWarps) * per;   // one slot per (request, KV head) run of a warp
+    w.bf16 = w.mma + (bh + kMaxMmaUnits) * per;   // one slot per (request, KV head) run of a unit
     w.err = w.bf16 + bh * per;
     w.total = w.err + 16;
     return w;
@@ -442,6 +457,7 @@ static int prepare_decode(oscar_cache* c, const void* q, int32_t q_dtype, const 
     int rc = sync(c, s);
     if (rc != OSCAR_OK) return rc;
     std::memset(&p, 0, sizeof(p));
+    p.fmt = c->fmt;
     p.batch = c->d.batch;
     p.hkv = c->d.num_kv_heads;
     p.g = c->g;
@@ -476,7 +492,7 @@ static int prepare_decode(oscar_cache* c, const void* q, int32_t q_dtype, const 
     if (pages > INT32_MAX / 4) return OSCAR_ERANGE;
     p.total_pages = (int32_t)pages;
     if (p.path == OSCAR_PATH_WARP_MMA && pages > 0) {
-        rc = mma_warp_count(c->g, pages, &p.n_warps);
+        rc = mma_unit_count(c->g, pages, &p.n_units);
         if (rc != OSCAR_OK) return rc;
     }
     return OSCAR_OK;
@@ -581,7 +597,8 @@ int oscar_read_int2(const oscar_cache* c, int32_t b, int32_t h, int64_t pos0, in
     int64_t l = c->len[b];
     if (n == 0) return OSCAR_OK;
     if (pos0 < kSink || pos0 + n > l - kWindow) return OSCAR_ERANGE;
-    std::vector<uint8_t> blk(kPageHeadBytes);
+    const PageFmt f = c->fmt;
+    std::vector<uint8_t> blk(f.bytes);
     int64_t cur_page = -1;
     for (int64_t i = 0; i < n; ++i) {
         int64_t pos = pos0 + i;
@@ -589,15 +606,15 @@ int oscar_read_int2(const oscar_cache* c, int32_t b, int32_t h, int64_t pos0, in
         int t = (int)((pos - kSink) % kPage);
         if (pg != cur_page) {
             int32_t phys = c->rows[b][pg];
-            const uint8_t* src = c->pool + ((size_t)phys * c->d.num_kv_heads + h) * kPageHeadBytes;
-            cudaError_t e = cudaMemcpyAsync(blk.data(), src, kPageHeadBytes, cudaMemcpyDeviceToHost,
+            const uint8_t* src = c->pool + ((size_t)phys * c->d.num_kv_heads + h) * f.bytes;
+            cudaError_t e = cudaMemcpyAsync(blk.data(), src, f.bytes, cudaMemcpyDeviceToHost,
                                             S(stream));
             if (e == cudaSuccess) e = cudaStreamSynchronize(S(stream));
             if (e != cudaSuccess) return cuda_fail(e);
             cur_page = pg;
         }
-        if (k_sm) std::memcpy(k_sm + i * 4, blk.data() + kKSm + t * 8, 8);
-        if (v_sm) std::memcpy(v_sm + i * 4, blk.data() + kVSm + t * 8, 8);
+        if (k_sm) std::memcpy(k_sm + i * (f.k_stride / 2), blk.data() + f.k_sm + t * f.k_stride, f.k_stride);
+        if (v_sm) std::memcpy(v_sm + i * (f.v_stride / 2), blk.data() + f.v_sm + t * f.v_stride, f.v_stride);
         // codes: from the page order back to the logical order (channel 4i + j in bits 2j of byte i)
         if (k_codes) {
             uint8_t* dst = k_codes + i * 32;
@@ -611,7 +628,7 @@ int oscar_read_int2(const oscar_cache* c, int32_t b, int32_t h, int64_t pos0, in
             uint8_t* dst = v_codes + i * 32;
             std::memset(dst, 0, 32);
             for (int ch = 0; ch < kD; ++ch) {
-                int code = (blk[kVCodes + v_code_byte(t, ch)] >> v_code_shift(ch)) & 3;
+                int code = (blk[f.v_codes + v_code_byte(t, ch)] >> v_code_shift(ch)) & 3;
                 dst[ch / 4] |= (uint8_t)(code << (2 * (ch % 4)));
             }
         }
@@ -686,6 +703,7 @@ int noalloc_decode_params(oscar_cache* c, const void* q, int32_t q_dtype, const 
     if (!aligned16(q) || !aligned16(rk) || !aligned16(out)) return OSCAR_EALIGN;
     DecodeParams& p = *pp;
     std::memset(&p, 0, sizeof(p));
+    p.fmt = c->fmt;
     p.batch = c->d.batch;
     p.hkv = c->d.num_kv_heads;
     p.g = c->g;
@@ -713,7 +731,7 @@ int noalloc_decode_params(oscar_cache* c, const void* q, int32_t q_dtype, const 
     if (pages > INT32_MAX / 4) return OSCAR_ERANGE;
     p.total_pages = (int32_t)pages;
     if (pages > 0) {
-        const int rc = mma_warp_count(c->g, pages, &p.n_warps);
+        const int rc = mma_unit_count(c->g, pages, &p.n_units);
         if (rc != OSCAR_OK) return rc;
     }
     const size_t per_part = (size_t)c->g * (2 + kD) * sizeof(float);
@@ -721,7 +739,7 @@ int noalloc_decode_params(oscar_cache* c, const void* q, int32_t q_dtype, const 
     const size_t o_err = kNoallocErrOffset;   // fixed, so that oscar_decode_status_noalloc finds it
     const size_t o_qrot = 256;
     const size_t o_mma = o_qrot + (((size_t)c->d.batch * c->d.num_q_heads * kD * sizeof(float) + 255) & ~(size_t)255);
-    const size_t o_bf16 = o_mma + (bh + (size_t)p.n_warps) * per_part;
+    const size_t o_bf16 = o_mma + (bh + (size_t)p.n_units) * per_part;
     if (o_bf16 + bh * per_part > scratch_bytes) return OSCAR_ESCRATCH;
     uint8_t* ws = (uint8_t*)scratch;
     p.qrot = (float*)(ws + o_qrot);

@@ -59,7 +59,7 @@ __global__ void __launch_bounds__(128) quant_few(const __grid_constant__ AppendP
     const int pbeg = max(r.e0, kSink + pg * kPage);
     const int pend = min(r.e1, kSink + (pg + 1) * kPage);
     const int phys = p.page_table[(size_t)b * p.max_pps + pg];
-    uint8_t* blk = p.pool + ((size_t)phys * p.hkv + h) * kPageHeadBytes;
+    uint8_t* blk = p.pool + ((size_t)phys * p.hkv + h) * p.fmt.bytes;
 
     {   // stage R_K of this head with asynchronous 16-byte copies, all of a thread's 32 in flight
         // at once (waited for before the first __syncthreads below)
@@ -96,7 +96,7 @@ __global__ void __launch_bounds__(128) quant_few(const __grid_constant__ AppendP
         for (int t = 0; t < n; ++t) {
             // K (rotated) and V (unrotated): per-token asymmetric INT2 in two 64-channel groups
             const float yv = bf16_bits_to_f32(token_src(p, b, h, 1, p0 + t)[c]);
-            store_token(blk, (p0 + t - kSink) % kPage, acc[t], yv, p.clip_k, p.clip_v, red, part);
+            store_token(blk, p.fmt, (p0 + t - kSink) % kPage, acc[t], yv, p.clip_k, p.clip_v, red, part);
         }
     }
 }
@@ -108,12 +108,17 @@ __device__ __forceinline__ uint32_t or_over_r(uint32_t v) {
     return v;
 }
 
-// min / max over the 8 lanes of a 64-channel group (channel blocks differing in bits 0..2)
-__device__ __forceinline__ GroupStat group_minmax8(float mn, float mx) {
+// min / max over the lanes of a group: 8 lanes for 64 channels (channel blocks differing in bits
+// 0..2), 16 lanes for 128 channels (bits 0..3)
+__device__ __forceinline__ GroupStat group_minmax_lanes(float mn, float mx, int group) {
 #pragma unroll
     for (int o = 1; o < 8; o <<= 1) {
         mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    }
+    if (group == kD) {
+        mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, 8));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
     }
     GroupStat g;
     g.mn = mn;
@@ -122,6 +127,11 @@ __device__ __forceinline__ GroupStat group_minmax8(float mn, float mx) {
 }
 
 constexpr int kQPThreads = 256;   // threads of quant_pages
+
+// Position of float4 f (channels 4f .. 4f + 3) inside a staged R_K row: bit 0 flipped when bit 3 is
+// set.  Thread cb reads float4s 2 cb and 2 cb + 1; unswizzled, the 16 lanes of a token would fall
+// on only 4 of the 8 bank groups of a 128-byte row (4-way conflicts), swizzled they cover all 8.
+__device__ __forceinline__ int rk_swz(int f) { return f ^ ((f >> 3) & 1); }
 constexpr int kSPT = kPage * 16 / kQPThreads;   // page slots per thread (16 lanes per slot)
 
 // One CTA per (touched INT2 page, KV head), 128 threads.  Thread t owns the 8 page slots
@@ -149,17 +159,20 @@ __global__ void __launch_bounds__(kQPThreads) quant_pages(const __grid_constant_
     const int pend = min(r.e1, page_pos + kPage);
     const int sbeg = pbeg - page_pos, send = pend - page_pos;
     const int phys = p.page_table[(size_t)b * p.max_pps + pg];
-    uint8_t* blk = p.pool + ((size_t)phys * p.hkv + h) * kPageHeadBytes;
+    uint8_t* blk = p.pool + ((size_t)phys * p.hkv + h) * p.fmt.bytes;
 
     {   // stage R_K of this head (asynchronous 16-byte copies, all in flight while the key inputs
-        // of the page's live slots are loaded) and those key inputs
+        // of the page's live slots are loaded) and those key inputs.  Row j keeps its 32 float4s
+        // with the index swizzled (rk_swz), so that the rotation's row loads hit every bank
         const float4* src = reinterpret_cast<const float4*>(p.rk + (size_t)h * kD * kD);
         const uint32_t dst = (uint32_t)__cvta_generic_to_shared(R);
 #pragma unroll
-        for (int i = 0; i < kD * kD / 4 / kQPThreads; ++i)
-            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst + 16u * (t + kQPThreads * i)),
-                         "l"(src + t + kQPThreads * i)
+        for (int i = 0; i < kD * kD / 4 / kQPThreads; ++i) {
+            const int idx = t + kQPThreads * i, row = idx >> 5, f = idx & 31;
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst + 16u * (32 * row + rk_swz(f))),
+                         "l"(src + idx)
                          : "memory");
+        }
         // value rows of the live slots, also asynchronous (read by the quantisation below)
         const uint32_t vdst = (uint32_t)__cvta_generic_to_shared(vt);
 #pragma unroll
@@ -187,24 +200,35 @@ __global__ void __launch_bounds__(kQPThreads) quant_pages(const __grid_constant_
     }
     __syncthreads();
 
-    // ---- keys: k~[s][c] = sum_j x[s][j] R[j][c], serial fused multiply-add in ascending j
+    // ---- keys: k~[s][c] = sum_j x[s][j] R[j][c], serial fused multiply-add in ascending j.  Two
+    // channels' chains share one packed f32x2 FMA; each lane of it rounds exactly as a scalar fmaf
+    float2 acc2[kSPT][4];
+#pragma unroll
+    for (int i = 0; i < kSPT; ++i)
+#pragma unroll
+        for (int m = 0; m < 4; ++m) acc2[i][m] = make_float2(0.0f, 0.0f);
+    const int f0 = rk_swz(2 * cb), f1 = rk_swz(2 * cb + 1);
+#pragma unroll 2
+    for (int j = 0; j < kD; ++j) {
+        const float4 x0 = *reinterpret_cast<const float4*>(xt + j * kPage + kSPT * tb);
+        const float4 r0 = reinterpret_cast<const float4*>(R + j * kD)[f0];
+        const float4 r1 = reinterpret_cast<const float4*>(R + j * kD)[f1];
+        const float xv[kSPT] = {x0.x, x0.y, x0.z, x0.w};
+        const float2 rv[4] = {make_float2(r0.x, r0.y), make_float2(r0.z, r0.w), make_float2(r1.x, r1.y),
+                              make_float2(r1.z, r1.w)};
+#pragma unroll
+        for (int i = 0; i < kSPT; ++i)
+#pragma unroll
+            for (int m = 0; m < 4; ++m) acc2[i][m] = __ffma2_rn(make_float2(xv[i], xv[i]), rv[m], acc2[i][m]);
+    }
     float acc[kSPT][8];
 #pragma unroll
     for (int i = 0; i < kSPT; ++i)
 #pragma unroll
-        for (int jj = 0; jj < 8; ++jj) acc[i][jj] = 0.0f;
-#pragma unroll 2
-    for (int j = 0; j < kD; ++j) {
-        const float4 x0 = *reinterpret_cast<const float4*>(xt + j * kPage + kSPT * tb);
-        const float4 r0 = *reinterpret_cast<const float4*>(R + j * kD + 8 * cb);
-        const float4 r1 = *reinterpret_cast<const float4*>(R + j * kD + 8 * cb + 4);
-        const float xv[kSPT] = {x0.x, x0.y, x0.z, x0.w};
-        const float rv[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
-#pragma unroll
-        for (int i = 0; i < kSPT; ++i)
-#pragma unroll
-            for (int jj = 0; jj < 8; ++jj) acc[i][jj] = __fmaf_rn(xv[i], rv[jj], acc[i][jj]);
-    }
+        for (int m = 0; m < 4; ++m) {
+            acc[i][2 * m] = acc2[i][m].x;
+            acc[i][2 * m + 1] = acc2[i][m].y;
+        }
     // a page filled completely by this call is built in shared memory (in the key-input space, free
     // now) and written out with 16-byte stores; a partly filled one is updated byte by byte in place
     const bool whole = sbeg == 0 && send == kPage;
@@ -224,7 +248,7 @@ __global__ void __launch_bounds__(kQPThreads) quant_pages(const __grid_constant_
             float mn = acc[i][0], mx = acc[i][0];
 #pragma unroll
             for (int jj = 1; jj < 8; ++jj) mn = fminf(mn, acc[i][jj]), mx = fmaxf(mx, acc[i][jj]);
-            const GroupStat gs = group_minmax8(mn, mx);
+            const GroupStat gs = group_minmax_lanes(mn, mx, p.fmt.gk);
             // code of channel 8 cb + jj at bits 2 rpos of byte jj & 3 of word jj >> 2; after the OR
             // over the four code positions every byte is complete
             uint32_t w[2] = {0u, 0u};
@@ -247,8 +271,9 @@ __global__ void __launch_bounds__(kQPThreads) quant_pages(const __grid_constant_
                 *reinterpret_cast<uint32_t*>(row) = __byte_perm(lo, hi, 0x5140);
                 *reinterpret_cast<uint32_t*>(row + 8) = __byte_perm(lo, hi, 0x7362);
             }
-            if (live && (cb & 7) == 0)
-                *reinterpret_cast<uint32_t*>(ob + kKSm + s * 8 + u * 4) = (uint32_t)s16 | ((uint32_t)m16 << 16);
+            if (live && (8 * cb) % p.fmt.gk == 0)
+                *reinterpret_cast<uint32_t*>(ob + p.fmt.k_sm + s * p.fmt.k_stride + (8 * cb / p.fmt.gk) * 4) =
+                    (uint32_t)s16 | ((uint32_t)m16 << 16);
         }
         // values (unrotated): this thread's 8 channels of the token, straight from the source row
         {
@@ -268,7 +293,7 @@ __global__ void __launch_bounds__(kQPThreads) quant_pages(const __grid_constant_
             float mn = vx[0], mx = vx[0];
 #pragma unroll
             for (int jj = 1; jj < 8; ++jj) mn = fminf(mn, vx[jj]), mx = fmaxf(mx, vx[jj]);
-            const GroupStat gs = group_minmax8(mn, mx);
+            const GroupStat gs = group_minmax_lanes(mn, mx, p.fmt.gv);
             uint32_t w[2] = {0u, 0u};
             uint16_t s16 = 0, m16 = 0;
 #pragma unroll
@@ -284,15 +309,16 @@ __global__ void __launch_bounds__(kQPThreads) quant_pages(const __grid_constant_
             if (live && rpos == 0) {
 #pragma unroll
                 for (int jj = 0; jj < 8; ++jj)
-                    ob[kVCodes + v_code_byte(s, 64 * u + 8 * y + jj)] = (uint8_t)(w[jj >> 2] >> (8 * (jj & 3)));
+                    ob[p.fmt.v_codes + v_code_byte(s, 64 * u + 8 * y + jj)] = (uint8_t)(w[jj >> 2] >> (8 * (jj & 3)));
             }
-            if (live && (cb & 7) == 0)
-                *reinterpret_cast<uint32_t*>(ob + kVSm + s * 8 + u * 4) = (uint32_t)s16 | ((uint32_t)m16 << 16);
+            if (live && (8 * cb) % p.fmt.gv == 0)
+                *reinterpret_cast<uint32_t*>(ob + p.fmt.v_sm + s * p.fmt.v_stride + (8 * cb / p.fmt.gv) * 4) =
+                    (uint32_t)s16 | ((uint32_t)m16 << 16);
         }
     }
     if (whole) {
         __syncthreads();
-        for (int i = t; i < kPageHeadBytes / 16; i += kQPThreads)
+        for (int i = t; i < p.fmt.bytes / 16; i += kQPThreads)
             reinterpret_cast<uint4*>(blk)[i] = reinterpret_cast<const uint4*>(ob)[i];
     }
 }

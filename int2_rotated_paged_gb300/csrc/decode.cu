@@ -152,7 +152,7 @@ __global__ void __launch_bounds__(128) split_simt(const __grid_constant__ Decode
         const int vgrp = lane >> 4;         // group of this lane's value channels
         for (int pg = s * p.pps + w; pg < pg_end; pg += 4) {
             const int phys = p.page_table[(size_t)b * p.max_pps + pg];
-            const uint8_t* blk = p.pool + ((size_t)phys * p.hkv + h) * kPageHeadBytes;
+            const uint8_t* blk = p.pool + ((size_t)phys * p.hkv + h) * p.fmt.bytes;
             const int nt = min(kPage, n_tok - pg * kPage);
             for (int t4 = 0; t4 < nt; t4 += 4) {
                 float lg[4][G];
@@ -160,13 +160,15 @@ __global__ void __launch_bounds__(128) split_simt(const __grid_constant__ Decode
                 // V: one byte per token holds this lane's 4 value channels (bits 2j)
                 uint32_t vb[4];
 #pragma unroll
-                for (int i = 0; i < 4; ++i) vb[i] = blk[kVCodes + v_code_byte(t4 + i, och(0))];
+                for (int i = 0; i < 4; ++i) vb[i] = blk[p.fmt.v_codes + v_code_byte(t4 + i, och(0))];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const int t = t4 + i;
                     const uint32_t kb = blk[kKCodes + t * 32 + lane];
-                    const uint32_t ksm = *reinterpret_cast<const uint32_t*>(blk + kKSm + t * 8 + kgrp * 4);
-                    const uint32_t vsm = *reinterpret_cast<const uint32_t*>(blk + kVSm + t * 8 + vgrp * 4);
+                    const uint32_t ksm =
+                        *reinterpret_cast<const uint32_t*>(blk + p.fmt.k_sm + t * p.fmt.k_stride + (p.fmt.gk == 64 ? kgrp * 4 : 0));
+                    const uint32_t vsm =
+                        *reinterpret_cast<const uint32_t*>(blk + p.fmt.v_sm + t * p.fmt.v_stride + (p.fmt.gv == 64 ? vgrp * 4 : 0));
                     const float ks = h2f(ksm & 0xffff), km = h2f(ksm >> 16);
                     const float vs = h2f(vsm & 0xffff), vm = h2f(vsm >> 16);
 #pragma unroll
@@ -324,12 +326,12 @@ __global__ void __launch_bounds__(32 * kMaxG) combine_mma(const __grid_constant_
         int w0 = 0, w1 = -1;
         if (pages > 0) {
             const int pf = p.page_off[b] + h * pages;
-            w0 = (int)((((long long)pf + 1) * p.n_warps - 1) / p.total_pages);
-            w1 = (int)((((long long)pf + pages) * p.n_warps - 1) / p.total_pages);
+            w0 = (int)((((long long)pf + 1) * p.n_units - 1) / p.total_pages);
+            w1 = (int)((((long long)pf + pages) * p.n_units - 1) / p.total_pages);
         }
         auto slot = [&](int w) { return p.part_mma + (((size_t)u + w) * p.g + hh) * (2 + kD); };
         auto owns = [&](int w) {
-            return ((long long)w * p.total_pages) / p.n_warps != ((long long)(w + 1) * p.total_pages) / p.n_warps;
+            return ((long long)w * p.total_pages) / p.n_units != ((long long)(w + 1) * p.total_pages) / p.n_units;
         };
         float M = pb[0];
         for (int w = w0; w <= w1; ++w)

@@ -20,12 +20,35 @@ constexpr int kMaxBatch = 256;     // requests per call (kernel-parameter tables
 constexpr int kMaxG = 16;          // query heads per KV head
 constexpr int kMaxDevices = 64;    // devices whose per-device launch settings are cached
 
-// Byte layout of one (physical page, KV head) block.
+// Byte layout of one (physical page, KV head) block with 64-channel groups for keys and values
+// (the largest format; PageFmt below gives the layout for every group-size pair).
 constexpr int kKCodes = 0;                      // [64 tokens][32 B] key codes (k_code_byte / k_code_shift)
 constexpr int kKSm = 2048;                      // [64 tokens][s0 m0 s1 m1] fp16
 constexpr int kVCodes = 2560;                   // 2048 B of value codes (v_code_byte / v_code_shift)
 constexpr int kVSm = 4608;                      // [64 tokens][s0 m0 s1 m1] fp16
 constexpr int kPageHeadBytes = 5120;
+
+// Layout of a (page, KV head) block when keys are quantised in groups of gk channels and values in
+// groups of gv channels (64 or 128 each): key codes, key scale/min (one fp16 pair per group and
+// token), value codes, value scale/min.  The code regions are the same for every format.
+struct PageFmt {
+    int32_t gk, gv;                 // channels per quantisation group: keys, values
+    int32_t k_stride, v_stride;     // scale/min bytes per token: 4 * (128 / group)
+    int32_t k_sm, v_codes, v_sm;    // byte offsets of the key scale/min, value codes, value scale/min
+    int32_t bytes;                  // bytes of the block (a multiple of 16)
+};
+__host__ __device__ inline PageFmt page_fmt(int gk, int gv) {
+    PageFmt f;
+    f.gk = gk;
+    f.gv = gv;
+    f.k_stride = 4 * (kD / gk);
+    f.v_stride = 4 * (kD / gv);
+    f.k_sm = 2048;
+    f.v_codes = f.k_sm + kPage * f.k_stride;
+    f.v_sm = f.v_codes + 2048;
+    f.bytes = f.v_sm + kPage * f.v_stride;
+    return f;
+}
 
 // Where the 2-bit codes sit inside a page.  The order is chosen for the warp-level MMA read
 // path: each thread of a warp finds the codes of its mma.m16n8k16 fragments in one 8-byte
@@ -59,6 +82,7 @@ struct AppendReq {
 };
 
 struct AppendParams {
+    PageFmt fmt;
     int32_t batch, hkv, n_jobs;
     float clip_k, clip_v;
     const uint16_t* k;     // bf16 [rows][hkv][128]
@@ -73,6 +97,7 @@ struct AppendParams {
 };
 
 struct DecodeParams {
+    PageFmt fmt;
     int32_t batch, hkv, g, pps, max_splits;
     const void* q;
     int32_t q_dtype;
@@ -87,14 +112,14 @@ struct DecodeParams {
     float* partial;        // SIMT path: [batch][hkv][max_splits][g][2 + 128]
     int32_t len[kMaxBatch];
     int32_t path;          // OSCAR_PATH_SIMT (1) or OSCAR_PATH_WARP_MMA (2)
-    float* part_mma;       // warp-MMA path: [batch * hkv + n_warps][g][2 + 128], slot (b * hkv + h) + warp
+    float* part_mma;       // warp-MMA path: [batch * hkv + n_units][g][2 + 128], slot (b * hkv + h) + unit
     float* part_bf16;      // [batch * hkv][g][2 + 128]: the BF16 sink / window split
     int32_t* err;          // nonzero after a bounded wait gave up
     int32_t wait_iters;    // a bounded wait gives up after this many tests of up to 1 ms each
     int32_t wait_probe;    // nonzero: the first kernel also waits on a barrier nothing arrives at
     // warp-MMA path
     int32_t total_pages;   // INT2 pages over all (request, KV head)
-    int32_t n_warps;       // warps of the warp-MMA kernel
+    int32_t n_units;       // page-streaming units (warp pairs) of the warp-MMA kernel
     int32_t page_off[kMaxBatch + 1];   // sum over earlier requests of pages * hkv
 };
 
@@ -109,7 +134,7 @@ __host__ __device__ inline int int2_splits(int len, int pps) {
     return (int2_pages(len) + pps - 1) / pps;
 }
 
-constexpr int kMaxMmaWarps = 2048;     // warps of one warp-MMA launch (partial-buffer slots)
+constexpr int kMaxMmaUnits = 2048;     // units of one warp-MMA launch (partial-buffer slots)
 
 // Launchers (each returns the cudaError_t of its launch).
 cudaError_t launch_append(const AppendParams& p, cudaStream_t s);
@@ -122,7 +147,7 @@ cudaError_t launch_prep_step(const DecodeParams& p, const AppendParams& a, cudaS
 // attention and the combine
 cudaError_t launch_decode_step(const DecodeParams& p, const AppendParams& a, cudaStream_t s,
                                cudaEvent_t* timing = nullptr);
-int mma_warps_per_cta(int g);   // warps per CTA of the warp-MMA kernel for G query heads per KV head
+int mma_units_per_cta(int g);   // units (warp pairs) per CTA of the warp-MMA kernel for G heads per KV head
 cudaError_t launch_build_rk(const float* q, int64_t n, int hkv, float* rk, void* ws, cudaStream_t s);
 size_t build_rk_ws_bytes(int hkv);
 

@@ -143,8 +143,9 @@ __device__ __forceinline__ void prep_body(const DecodeParams& p, const AppendPar
             const AppendReq& r = ap->req[b];
             const int pg = (r.e0 - kSink) / kPage;
             const int phys = ap->page_table[(size_t)b * ap->max_pps + pg];
-            uint8_t* blk = ap->pool + ((size_t)phys * p.hkv + h) * kPageHeadBytes;
-            tq::store_token(blk, (r.e0 - kSink) % kPage, c < kD ? acck : 0.f, yv, ap->clip_k, ap->clip_v, red, tpart);
+            uint8_t* blk = ap->pool + ((size_t)phys * p.hkv + h) * ap->fmt.bytes;
+            tq::store_token(blk, ap->fmt, (r.e0 - kSink) % kPage, c < kD ? acck : 0.f, yv, ap->clip_k, ap->clip_v, red,
+                            tpart);
         }
     }
 

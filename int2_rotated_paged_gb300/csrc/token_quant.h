@@ -2,7 +2,8 @@
 // by the write-path kernels and the fused decode step (device code only).
 //
 // The arithmetic is the write path's bit-exact contract (axbrief.com OSCAR page, section
-// "attention-statistics rotation + Triton kernels": per-token asymmetric INT2 in 64-channel groups,
+// "attention-statistics rotation + Triton kernels": per-token asymmetric INT2 in 64-channel groups
+// (128-channel groups as a per-cache option, the variants behind the page's 2.28 / 2.38 bits),
 // c_K = 0.96, c_V = 0.92): clip products, the range subtraction and both divisions are single IEEE
 // fp32 operations (explicit _rn intrinsics), fp16 conversions round to nearest even, codes use rint.
 #pragma once
@@ -58,8 +59,9 @@ __device__ __forceinline__ Quant quantise(float y, GroupStat g, float clip) {
     return q;
 }
 
-// Min and max over the 64 channels of each group (threads 0..63 and 64..127).
-__device__ __forceinline__ GroupStat group_minmax(float y, float* red) {
+// Min and max over the channels of each group: threads 0..63 and 64..127 for 64-channel groups,
+// threads 0..127 for one 128-channel group.
+__device__ __forceinline__ GroupStat group_minmax(float y, float* red, int group) {
     float mn = y, mx = y;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -72,26 +74,33 @@ __device__ __forceinline__ GroupStat group_minmax(float y, float* red) {
         red[2 * w + 1] = mx;
     }
     __syncthreads();
-    const int w0 = w & ~1;
     GroupStat g;
-    g.mn = fminf(red[2 * w0], red[2 * w0 + 2]);
-    g.mx = fmaxf(red[2 * w0 + 1], red[2 * w0 + 3]);
+    if (group == kD) {
+        g.mn = fminf(fminf(red[0], red[2]), fminf(red[4], red[6]));
+        g.mx = fmaxf(fmaxf(red[1], red[3]), fmaxf(red[5], red[7]));
+    } else {
+        const int w0 = (w & 3) & ~1;
+        g.mn = fminf(red[2 * w0], red[2 * w0 + 2]);
+        g.mx = fmaxf(red[2 * w0 + 1], red[2 * w0 + 3]);
+    }
     __syncthreads();
     return g;
 }
 
 // Quantise one token (channel c of the key y_k and value y_v in thread c < 128; any further threads
 // of the block take part in the barriers only) and store its codes and scales into slot `slot` of the
-// page-head block `blk`.  `red` holds 2 floats per warp of the block, `part` 2 x 4 x 16 bytes.
-__device__ __forceinline__ void store_token(uint8_t* blk, int slot, float yk, float yv, float clip_k, float clip_v,
-                                            float* red, uint8_t (*part)[4][16]) {
+// page-head block `blk` (layout f).  `red` holds 2 floats per warp of the block, `part` 2 x 4 x 16 bytes.
+__device__ __forceinline__ void store_token(uint8_t* blk, const PageFmt& f, int slot, float yk, float yv, float clip_k,
+                                            float clip_v, float* red, uint8_t (*part)[4][16]) {
     const int c = threadIdx.x, lane = c & 31;
-    const Quant qk = quantise(yk, group_minmax(yk, red), clip_k);
-    const Quant qv = quantise(yv, group_minmax(yv, red), clip_v);
-    if (c < kD && (c & 63) == 0) {
-        *reinterpret_cast<uint32_t*>(blk + kKSm + slot * 8 + (c >> 6) * 4) = (uint32_t)qk.s16 | ((uint32_t)qk.m16 << 16);
-        *reinterpret_cast<uint32_t*>(blk + kVSm + slot * 8 + (c >> 6) * 4) = (uint32_t)qv.s16 | ((uint32_t)qv.m16 << 16);
-    }
+    const Quant qk = quantise(yk, group_minmax(yk, red, f.gk), clip_k);
+    const Quant qv = quantise(yv, group_minmax(yv, red, f.gv), clip_v);
+    if (c < kD && (c & (f.gk - 1)) == 0)
+        *reinterpret_cast<uint32_t*>(blk + f.k_sm + slot * f.k_stride + (c / f.gk) * 4) =
+            (uint32_t)qk.s16 | ((uint32_t)qk.m16 << 16);
+    if (c < kD && (c & (f.gv - 1)) == 0)
+        *reinterpret_cast<uint32_t*>(blk + f.v_sm + slot * f.v_stride + (c / f.gv) * 4) =
+            (uint32_t)qv.s16 | ((uint32_t)qv.m16 << 16);
     // pack: every code byte holds the codes of four channels c0 + 16 r (r = 0..3) of this token, two
     // from lanes l and l ^ 16 of one warp and two from the next warp
     uint32_t pk = (uint32_t)qk.code << k_code_shift(c & (kD - 1));
@@ -112,7 +121,7 @@ __device__ __forceinline__ void store_token(uint8_t* blk, int slot, float yk, fl
         // value byte of channels 64q + 16r + 8y + g
         const int j = c - 32, q = j >> 4, g = (j >> 1) & 7, y = j & 1;
         const int l = 8 * y + g;
-        blk[kVCodes + v_code_byte(slot, 64 * q + 8 * y + g)] = part[1][2 * q][l] | part[1][2 * q + 1][l];
+        blk[f.v_codes + v_code_byte(slot, 64 * q + 8 * y + g)] = part[1][2 * q][l] | part[1][2 * q + 1][l];
     }
     __syncthreads();   // part and red are free again
 }

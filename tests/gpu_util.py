@@ -21,11 +21,13 @@ def oracle_rk(seed: int, hkv: int, n: int = 4096) -> np.ndarray:
     return np.stack([oracle.build_rk(synth.calibration_queries(seed, h, n).numpy())[0] for h in range(hkv)])
 
 
-def make_cache(cfg: synth.LayerConfig, max_len: int, table: str | None = None) -> K.Cache:
+def make_cache(cfg: synth.LayerConfig, max_len: int, table: str | None = None, group_k: int = 64,
+               group_v: int = 64) -> K.Cache:
     per_seq = pages_needed(max_len) + 1
     total = per_seq * cfg.batch + 3
     order = synth.page_order(cfg.seed, total, table or cfg.table)
-    return K.Cache(cfg.batch, cfg.num_q_heads, cfg.num_kv_heads, total, per_seq, page_order=order)
+    return K.Cache(cfg.batch, cfg.num_q_heads, cfg.num_kv_heads, total, per_seq, page_order=order,
+                   group_k=group_k, group_v=group_v)
 
 
 def append_initial(cache: K.Cache, cfg: synth.LayerConfig, lens, rk_dev, chunks=None):
@@ -47,11 +49,11 @@ def append_initial(cache: K.Cache, cfg: synth.LayerConfig, lens, rk_dev, chunks=
         done = list(lens)
 
 
-def oracle_caches(cfg: synth.LayerConfig, pairs, lens, rk: np.ndarray):
-    """OracleCache per (b, h) in `pairs`, filled with the same tokens (drawn on the CPU copy)."""
+def oracle_caches(cfg: synth.LayerConfig, pairs, lens, rk: np.ndarray, group_k: int = 64, group_v: int = 64):
+    """OracleCache per (b, h) in `pairs`, filled with the same tokens (drawn like the cache's)."""
     out = {}
     for (b, h) in pairs:
-        oc = oracle.OracleCache(rk[h])
+        oc = oracle.OracleCache(rk[h], group_k=group_k, group_v=group_v)
         if lens[b]:
             k16 = synth.bf16_bits(synth.keys(cfg.seed, b, h, 0, lens[b], device="cuda"))
             v16 = synth.bf16_bits(synth.values(cfg.seed, b, h, 0, lens[b], device="cuda"))
@@ -70,7 +72,7 @@ def check_int2_bytes(cache: K.Cache, oc: oracle.OracleCache, b: int, h: int):
     n = oc.kc.shape[0]
     if n == 0:
         return
-    kc, ks, vc, vs = K.oscar_read_int2(cache.handle, b, h, 64, n)
+    kc, ks, vc, vs = cache.read_int2(b, h, 64, n)
     for name, got, ref in (("k codes", kc, oc.kc), ("k scale/min", ks, oc.ks),
                            ("v codes", vc, oc.vc), ("v scale/min", vs, oc.vs)):
         if not np.array_equal(got, ref):

@@ -59,12 +59,14 @@ def test_descriptor_defaults_and_sizes(K):
     assert abs(d.clip_k - 0.96) < 1e-7 and abs(d.clip_v - 0.92) < 1e-7
     L = K.lib()
     assert L.oscar_pool_bytes(ctypes.byref(d)) == 20 * 8 * 5120
+    assert d.group_size_v == 64 and L.oscar_page_head_bytes(ctypes.byref(d)) == 5120
     assert L.oscar_bf16_bytes(ctypes.byref(d)) == 4 * 8 * 2 * 320 * 128 * 2
     assert L.oscar_page_table_bytes(ctypes.byref(d)) == 4 * 8 * 4
     assert L.oscar_seq_lens_bytes(ctypes.byref(d)) == 16
 
 
-@pytest.mark.parametrize("field,value", [("head_dim", 64), ("page_size", 32), ("group_size", 128),
+@pytest.mark.parametrize("field,value", [("head_dim", 64), ("page_size", 32), ("group_size", 32),
+                                         ("group_size", 96), ("group_size_v", 32), ("group_size_v", 256),
                                          ("sink", 0), ("window", 128), ("num_q_heads", 36),
                                          ("num_q_heads", 80), ("batch", 0), ("clip_k", 0.0),
                                          ("clip_v", 1.5), ("max_pages_total", 0)])
@@ -175,3 +177,15 @@ def test_decode_path_and_timing_arguments(K):
     assert L.oscar_kernel_timing_read(c, None, 4, ctypes.byref(got)) == K.OSCAR_EINVAL
     assert L.oscar_kernel_timing_read(c, None, 0, None) == K.OSCAR_EINVAL
     L.oscar_cache_destroy(c)
+
+
+@pytest.mark.parametrize("gk,gv,page", [(64, 64, 5120), (64, 128, 4864), (128, 128, 4608), (128, 64, 4864),
+                                        (128, 0, 4608)])
+def test_page_format_per_group_sizes(K, gk, gv, page):
+    # one fp16 (scale, minimum) pair per group and token: 64 tokens x 4 B x (128 / group) per tensor
+    d = _desc(K, group_size=gk, group_size_v=gv)
+    L = K.lib()
+    assert L.oscar_page_head_bytes(ctypes.byref(d)) == page
+    assert L.oscar_pool_bytes(ctypes.byref(d)) == d.max_pages_total * d.num_kv_heads * page
+    # bits per stored INT2 value: codes (2 bits) plus the scale/min pairs
+    assert page * 8 / (64 * 256) == (2 * 128 + 32 * 128 / gk + 2 * 128 + 32 * 128 / (gv or gk)) / 256

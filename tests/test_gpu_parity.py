@@ -58,13 +58,14 @@ def _check_attention(out, q, ocs, cfg):
     return worst
 
 
-def _run(cfg, lens, pairs=None, steps=2, chunks=None, table=None, check_bytes=True, out_dtype=torch.float32):
+def _run(cfg, lens, pairs=None, steps=2, chunks=None, table=None, check_bytes=True, out_dtype=torch.float32,
+         groups=(64, 64), fused=False):
     rk = oracle_rk(cfg.seed, cfg.num_kv_heads, 1024)
     rk_dev = torch.tensor(rk, device="cuda")
-    cache = make_cache(cfg, max(lens) + steps, table)
+    cache = make_cache(cfg, max(lens) + steps, table, *groups)
     append_initial(cache, cfg, lens, rk_dev, chunks)
     pairs = pairs or [(b, h) for b in range(cfg.batch) for h in range(cfg.num_kv_heads)]
-    ocs = oracle_caches(cfg, pairs, lens, rk)
+    ocs = oracle_caches(cfg, pairs, lens, rk, *groups)
     cur = list(lens)
     for step in range(steps):
         if check_bytes:
@@ -72,7 +73,10 @@ def _run(cfg, lens, pairs=None, steps=2, chunks=None, table=None, check_bytes=Tr
                 check_int2_bytes(cache, oc, b, h)
                 check_bf16_bytes(cache, oc, b, h)
         q = decode_query(cfg, step)
-        out = _attend(cache, q, rk_dev, out_dtype)
+        if fused and step > 0:
+            out = step_out
+        else:
+            out = _attend(cache, q, rk_dev, out_dtype)
         if out_dtype == torch.float32:
             _check_attention(out, q, ocs, cfg)
         else:
@@ -88,7 +92,16 @@ def _run(cfg, lens, pairs=None, steps=2, chunks=None, table=None, check_bytes=Tr
         # one decode token per request, then the next step attends over it too
         n = [1] * cfg.batch
         k, v = synth.kv_block(cfg.seed, n, cur, cfg.num_kv_heads, device="cuda")
-        cache.append(k, v, n, rk_dev)
+        if fused:
+            # the next step's append and attention in one call (oscar_decode_step)
+            qn = decode_query(cfg, step + 1)
+            o = torch.empty(qn.shape, dtype=out_dtype, device="cuda")
+            cache.step(k, v, qn, rk_dev, o)
+            cache.status()
+            torch.cuda.synchronize()
+            step_out = o.float().cpu().numpy()
+        else:
+            cache.append(k, v, n, rk_dev)
         for (b, h), oc in ocs.items():
             oc.append(synth.bf16_bits(k[b, h][None]), synth.bf16_bits(v[b, h][None]))
         cur = [c + 1 for c in cur]
@@ -118,6 +131,16 @@ def test_gqa_group_sizes(hq, hkv):
     base = synth.config("qwen3_4b")
     cfg = synth.LayerConfig("gqa", 2, hq, hkv, [1500, 900], 2, "permuted", "bf16", 4242)
     _run(cfg, cfg.ctx, steps=2)
+
+
+@pytest.mark.parametrize("groups", [(64, 128), (128, 128), (128, 64)])
+@pytest.mark.parametrize("hq,hkv", [(16, 2), (24, 2), (8, 2)])
+def test_group_size_formats(groups, hq, hkv):
+    # keys / values in groups of 64 or 128 channels: codes and scales bit-exact against the oracle's
+    # grouped quantiser, attention against its grouped attention, through bulk appends, chunked
+    # appends and fused decode steps
+    cfg = synth.LayerConfig("groups", 3, hq, hkv, [1700, 383, 960], 4, "permuted", "bf16", 5150)
+    _run(cfg, cfg.ctx, steps=4, chunks=[500, 1, 700, 1000], groups=groups, fused=True)
 
 
 def test_qwen3_4b_shape_sampled_heads():
