@@ -46,7 +46,8 @@ def parse():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--config", default="qwen3_32b")
+    ap.add_argument("--config", default="qwen3_32b",
+                    help="workload: tiny, qwen3_4b, qwen3_8b, qwen3_32b (default), ragged_128k, or all (one line each)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-pairs", type=int, default=max(8, os.cpu_count() or 1),
@@ -542,9 +543,10 @@ def main():
     if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
         sys.exit(relaunch_under_torchrun(args))
     import synth
-    cfg = synth.config(args.config)
+    names = synth.CONFIG_NAMES if args.config == "all" else [args.config]
+    cfgs = [synth.config(nm) for nm in names]
     if args.batch:
-        cfg = synth.scaled(cfg, cfg.ctx, batch=args.batch)
+        cfgs = [synth.scaled(cfg, cfg.ctx, batch=args.batch) for cfg in cfgs]
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if world != args.gpus:
@@ -559,10 +561,11 @@ def main():
         tdist.init_process_group(backend)
         dist = tdist
     try:
-        if args.impl == "reference":
-            run_reference(args, cfg, rank, world)
-        else:
-            run_ours(args, cfg, rank, world, dist)
+        for cfg in cfgs:
+            if args.impl == "reference":
+                run_reference(args, cfg, rank, world)
+            else:
+                run_ours(args, cfg, rank, world, dist)
     finally:
         if dist is not None:
             dist.destroy_process_group()

@@ -314,6 +314,35 @@ size_t oscar_build_rk_workspace_bytes(int32_t num_kv_heads);
 int oscar_build_rk(const float *q, int64_t n, int32_t num_kv_heads, float *rk, void *workspace,
                    size_t workspace_bytes, void *stream);
 
+/* Streaming calibration of R_K (the same C_Q, eigen-solver and assembly as oscar_build_rk, for
+ * more query samples than one call holds, or samples that arrive over time).  The accumulator
+ * (device, oscar_cq_accumulator_bytes(num_kv_heads) bytes, 16-byte aligned, caller-owned) holds
+ * per KV head the fp64 sums of q^T q (128 x 128) and the sample count.  oscar_cq_reset zeroes it;
+ * oscar_cq_accumulate adds n samples per head (q: device, fp32, [num_kv_heads][n][128]; n = 0 is a
+ * no-op); oscar_cq_finalize divides by the count and writes R_K (rk: device, fp32,
+ * [num_kv_heads][128][128]) using workspace >= oscar_build_rk_workspace_bytes(num_kv_heads).  The
+ * accumulator is left unchanged, so more samples can be added and R_K refreshed.  At least one
+ * sample per head must have been added before finalizing (otherwise R_K is undefined).
+ * Source: axbrief.com OSCAR page, section "attention-statistics rotation + Triton kernels"
+ * (C_Q = (1/N) sum_n q_n^T q_n); the splitting into calls is this library's. */
+size_t oscar_cq_accumulator_bytes(int32_t num_kv_heads);
+int oscar_cq_reset(void *acc, int32_t num_kv_heads, void *stream);
+int oscar_cq_accumulate(const float *q, int64_t n, int32_t num_kv_heads, void *acc, void *stream);
+int oscar_cq_finalize(const void *acc, int32_t num_kv_heads, float *rk, void *workspace,
+                      size_t workspace_bytes, void *stream);
+
+/* Calibration samples of the value rotation R_V: the rows of S V, y_i = sum_t s_it v_t with
+ * s_i = softmax(q_i k^T / sqrt(128)), for n calibration queries against t_keys keys and values per
+ * KV head (q: [num_kv_heads][n][128], k, v: [num_kv_heads][t_keys][128], y: [num_kv_heads][n][128];
+ * all device fp32, 16-byte aligned).  Their covariance is the page's score-weighted value
+ * covariance C_S = (1/N) V^T S^T S V, so oscar_build_rk (or the streaming calls above) given y
+ * builds R_V = U_S H_Had P_br.  Logits in fp32, sums of p and p v in fp64.
+ * Errors: OSCAR_ERANGE (n < 1, t_keys < 1 or t_keys > 8192), OSCAR_EINVAL, OSCAR_EALIGN.
+ * Source: axbrief.com OSCAR page, section "attention-statistics rotation + Triton kernels"
+ * (value rotation from the score-weighted value covariance, absorbed into W_V / W_O). */
+int oscar_score_weighted_values(const float *q, int64_t n, const float *k, const float *v,
+                                int32_t t_keys, int32_t num_kv_heads, float *y, void *stream);
+
 /* ---------------------------------------------------------------- readback (synchronous)
  * Copy n INT2 tokens of request b, KV head h, starting at position pos0 (each position
  * must lie in the INT2 history) into host buffers, in the per-token logical format:

@@ -37,7 +37,8 @@ EXPORTS = [
     "oscar_read_bf16", "oscar_strerror", "oscar_last_cuda_error", "oscar_launch_count",
     "oscar_set_decode_path", "oscar_decode_status", "oscar_decode_attention_noalloc", "oscar_decode_step",
     "oscar_kernel_timing", "oscar_kernel_timing_read", "oscar_set_wait_limit", "oscar_decode_status_noalloc",
-    "oscar_set_wait_probe", "oscar_page_head_bytes",
+    "oscar_set_wait_probe", "oscar_page_head_bytes", "oscar_cq_accumulator_bytes", "oscar_cq_reset",
+    "oscar_cq_accumulate", "oscar_cq_finalize", "oscar_score_weighted_values",
 ]
 OSCAR_ESCRATCH = -8
 OSCAR_ETIMEOUT = -7
@@ -108,6 +109,11 @@ def lib() -> ctypes.CDLL:
         "oscar_kernel_timing_read": (ctypes.c_int, [P, P, I32, P]),
         "oscar_set_wait_limit": (ctypes.c_int, [I32]),
         "oscar_set_wait_probe": (ctypes.c_int, [I32]),
+        "oscar_cq_accumulator_bytes": (SZ, [I32]),
+        "oscar_cq_reset": (ctypes.c_int, [P, I32, P]),
+        "oscar_cq_accumulate": (ctypes.c_int, [P, I64, I32, P, P]),
+        "oscar_cq_finalize": (ctypes.c_int, [P, I32, P, P, SZ, P]),
+        "oscar_score_weighted_values": (ctypes.c_int, [P, I64, P, P, I32, I32, P, P]),
         "oscar_decode_status_noalloc": (ctypes.c_int, [P]),
     }
     for name, (res, args) in sig.items():
@@ -228,6 +234,29 @@ def oscar_build_rk(q, n: int, num_kv_heads: int, rk, workspace, stream=None):
     nbytes = workspace.numel() * workspace.element_size()
     _check("oscar_build_rk", lib().oscar_build_rk(_ptr(q), n, num_kv_heads, _ptr(rk), _ptr(workspace),
                                                   nbytes, _stream(stream)))
+
+
+def oscar_cq_accumulator_bytes(num_kv_heads: int) -> int:
+    return int(lib().oscar_cq_accumulator_bytes(num_kv_heads))
+
+
+def oscar_cq_reset(acc, num_kv_heads: int, stream=None):
+    _check("oscar_cq_reset", lib().oscar_cq_reset(_ptr(acc), num_kv_heads, _stream(stream)))
+
+
+def oscar_cq_accumulate(q, n: int, num_kv_heads: int, acc, stream=None):
+    _check("oscar_cq_accumulate", lib().oscar_cq_accumulate(_ptr(q), n, num_kv_heads, _ptr(acc), _stream(stream)))
+
+
+def oscar_cq_finalize(acc, num_kv_heads: int, rk, workspace, stream=None):
+    nbytes = workspace.numel() * workspace.element_size()
+    _check("oscar_cq_finalize", lib().oscar_cq_finalize(_ptr(acc), num_kv_heads, _ptr(rk), _ptr(workspace), nbytes,
+                                                        _stream(stream)))
+
+
+def oscar_score_weighted_values(q, n: int, k, v, t_keys: int, num_kv_heads: int, y, stream=None):
+    _check("oscar_score_weighted_values", lib().oscar_score_weighted_values(
+        _ptr(q), n, _ptr(k), _ptr(v), t_keys, num_kv_heads, _ptr(y), _stream(stream)))
 
 
 def oscar_read_int2(cache, b: int, h: int, pos0: int, n: int, stream=None, group_k: int = 64, group_v: int = 64):

@@ -587,6 +587,44 @@ int oscar_build_rk(const float* q, int64_t n, int32_t num_kv_heads, float* rk, v
     return e == cudaSuccess ? OSCAR_OK : cuda_fail(e);
 }
 
+size_t oscar_cq_accumulator_bytes(int32_t num_kv_heads) {
+    return num_kv_heads > 0 ? cq_acc_bytes(num_kv_heads) : 0;
+}
+
+int oscar_cq_reset(void* acc, int32_t num_kv_heads, void* stream) {
+    if (!acc || num_kv_heads < 1) return OSCAR_EINVAL;
+    if (!aligned16(acc)) return OSCAR_EALIGN;
+    cudaError_t e = cudaMemsetAsync(acc, 0, cq_acc_bytes(num_kv_heads), S(stream));
+    return e == cudaSuccess ? OSCAR_OK : cuda_fail(e);
+}
+
+int oscar_cq_accumulate(const float* q, int64_t n, int32_t num_kv_heads, void* acc, void* stream) {
+    if (!acc || num_kv_heads < 1 || n < 0) return OSCAR_EINVAL;
+    if (n == 0) return OSCAR_OK;
+    if (!q) return OSCAR_EINVAL;
+    if (!aligned16(q) || !aligned16(acc)) return OSCAR_EALIGN;
+    cudaError_t e = launch_cq_accumulate(q, n, num_kv_heads, acc, S(stream));
+    return e == cudaSuccess ? OSCAR_OK : cuda_fail(e);
+}
+
+int oscar_cq_finalize(const void* acc, int32_t num_kv_heads, float* rk, void* workspace, size_t workspace_bytes,
+                      void* stream) {
+    if (!acc || !rk || num_kv_heads < 1) return OSCAR_EINVAL;
+    if (!workspace || workspace_bytes < build_rk_ws_bytes(num_kv_heads)) return OSCAR_EWORKSPACE;
+    if (!aligned16(acc) || !aligned16(rk) || !aligned16(workspace)) return OSCAR_EALIGN;
+    cudaError_t e = launch_cq_finalize(acc, num_kv_heads, rk, workspace, S(stream));
+    return e == cudaSuccess ? OSCAR_OK : cuda_fail(e);
+}
+
+int oscar_score_weighted_values(const float* q, int64_t n, const float* k, const float* v, int32_t t_keys,
+                                int32_t num_kv_heads, float* y, void* stream) {
+    if (!q || !k || !v || !y || num_kv_heads < 1 || num_kv_heads > 65535) return OSCAR_EINVAL;
+    if (n < 1 || n > INT32_MAX || t_keys < 1 || t_keys > sv_max_keys()) return OSCAR_ERANGE;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(y)) return OSCAR_EALIGN;
+    cudaError_t e = launch_score_weighted(q, n, k, v, t_keys, num_kv_heads, y, S(stream));
+    return e == cudaSuccess ? OSCAR_OK : cuda_fail(e);
+}
+
 // ------------------------------------------------------------------ readback
 
 int oscar_read_int2(const oscar_cache* c, int32_t b, int32_t h, int64_t pos0, int64_t n,

@@ -6,7 +6,9 @@
 // page, section "OSCAR": they spread important channels evenly).
 //
 // Three kernels per call, one CTA per KV head for the eigen-solver:
-//   covariance   C = (1/n) Q^T Q in fp64.
+//   covariance   C = (1/n) Q^T Q in fp64 (or, streaming over several calls, cq_accumulate adds
+//                sum_t q_t^T q_t and the sample count into a caller-owned accumulator and
+//                cq_normalise divides once at the end).
 //   jacobi       parallel cyclic Jacobi (round-robin ordering: 64 disjoint rotations per
 //                round, 127 rounds per sweep) on C held in shared memory, accumulating the
 //                eigenvectors in global memory; sweeps until the off-diagonal Frobenius
@@ -14,6 +16,9 @@
 //   assemble     sort eigenpairs by descending eigenvalue, sign each eigenvector so its
 //                largest-magnitude entry is positive, R[r][c] = sum_k U[r][k] H[k][brev(c)],
 //                H[k][i] = (-1)^popcount(k & i) / sqrt(128); rounded to fp32.
+// score_weighted computes the calibration samples of the value rotation: rows of S V, whose
+// covariance is C_S = (1/N) V^T S^T S V (same page and section); R_V is then built from them by
+// the same eigen-solver and assembly.
 #include "internal.h"
 
 namespace oscar {
@@ -30,6 +35,81 @@ __global__ void __launch_bounds__(128) covariance(const float* __restrict__ q, i
     double acc = 0.0;
     for (int64_t t = 0; t < n; ++t) acc = fma((double)qh[t * kN + i], (double)qh[t * kN + j], acc);
     ws[(size_t)h * 2 * kN * kN + (size_t)i * kN + j] = acc / (double)n;
+}
+
+// Streaming form of the covariance: sums[h][i][j] += sum_t q_ti q_tj over this call's samples (fp64,
+// every sample in order, so a run of calls adds the same products a single call would), and
+// counts[h] += n.
+__global__ void __launch_bounds__(128) cq_accumulate(const float* __restrict__ q, int64_t n, double* __restrict__ sums,
+                                                     long long* __restrict__ counts) {
+    const int h = blockIdx.y;
+    const int i = blockIdx.x;
+    const int j = threadIdx.x;
+    const float* qh = q + (size_t)h * n * kN;
+    double acc = 0.0;
+    for (int64_t t = 0; t < n; ++t) acc = fma((double)qh[t * kN + i], (double)qh[t * kN + j], acc);
+    sums[(size_t)h * kN * kN + (size_t)i * kN + j] += acc;
+    if (i == 0 && j == 0) counts[h] += (long long)n;
+}
+
+// C = sums / count into the eigen-solver's workspace (the layout the covariance kernel writes)
+__global__ void __launch_bounds__(128) cq_normalise(const double* __restrict__ sums, const long long* __restrict__ counts,
+                                                    double* __restrict__ ws) {
+    const int h = blockIdx.y;
+    const int i = blockIdx.x;
+    const int j = threadIdx.x;
+    const double c = (double)counts[h];
+    ws[(size_t)h * 2 * kN * kN + (size_t)i * kN + j] = sums[(size_t)h * kN * kN + (size_t)i * kN + j] / c;
+}
+
+// Rows of S V for calibration: y_i = sum_t softmax_t(q_i . k_t / sqrt(128)) v_t for every query i of
+// every head h (one CTA per (query, head), thread = channel).  Logits in fp32 (four warps, one key
+// each, lanes over channels), each probability exp(logit - max) once in fp32, the sums of p and of
+// p v in fp64.
+constexpr int kSvMaxKeys = 8192;
+__global__ void __launch_bounds__(128) score_weighted(const float* __restrict__ q, int64_t n, const float* __restrict__ k,
+                                                      const float* __restrict__ v, int t_keys, float* __restrict__ y) {
+    extern __shared__ float lg[];     // [t_keys]
+    __shared__ float qs[kN];
+    __shared__ float red[4];
+    __shared__ double dred[4];
+    const int h = blockIdx.y;
+    const int64_t i = blockIdx.x;
+    const int c = threadIdx.x, w = c >> 5, lane = c & 31;
+    qs[c] = q[((size_t)h * n + i) * kN + c];
+    __syncthreads();
+    const float* kh = k + (size_t)h * t_keys * kN;
+    const float* vh = v + (size_t)h * t_keys * kN;
+    const float scale = 0.08838834764831845f;   // 1 / sqrt(128)
+    float mx = -INFINITY;
+    for (int t = w; t < t_keys; t += 4) {
+        const float4 kv = *reinterpret_cast<const float4*>(kh + (size_t)t * kN + 4 * lane);
+        float d = qs[4 * lane] * kv.x;
+        d = fmaf(qs[4 * lane + 1], kv.y, d);
+        d = fmaf(qs[4 * lane + 2], kv.z, d);
+        d = fmaf(qs[4 * lane + 3], kv.w, d);
+        for (int o = 16; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
+        d *= scale;
+        if (lane == 0) lg[t] = d;
+        mx = fmaxf(mx, d);
+    }
+    if (lane == 0) red[w] = mx;
+    __syncthreads();
+    mx = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+    // probabilities (unnormalised), each computed once, in place of the logits
+    double lp = 0.0;
+    for (int t = c; t < t_keys; t += kN) {
+        const float pr = expf(lg[t] - mx);
+        lg[t] = pr;
+        lp += (double)pr;
+    }
+    for (int o = 16; o > 0; o >>= 1) lp += __shfl_xor_sync(0xffffffffu, lp, o);
+    if (lane == 0) dred[w] = lp;
+    __syncthreads();
+    const double l = (dred[0] + dred[1]) + (dred[2] + dred[3]);
+    double acc = 0.0;
+    for (int t = 0; t < t_keys; ++t) acc = fma((double)lg[t], (double)vh[(size_t)t * kN + c], acc);
+    y[((size_t)h * n + i) * kN + c] = (float)(acc / l);
 }
 
 __device__ __forceinline__ int rr_player(int slot, int round) {
@@ -172,19 +252,58 @@ __global__ void __launch_bounds__(128) assemble(const double* __restrict__ ws, f
 
 size_t build_rk_ws_bytes(int hkv) { return (size_t)hkv * 2 * kN * kN * sizeof(double); }
 
-cudaError_t launch_build_rk(const float* q, int64_t n, int hkv, float* rk, void* ws, cudaStream_t s) {
-    double* w = (double*)ws;
-    covariance<<<dim3(kN, hkv), 128, 0, s>>>(q, n, w);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
+// eigen-decomposition of the covariances in ws and the R assembly
+static cudaError_t eigen_and_assemble(int hkv, float* rk, double* w, cudaStream_t s) {
     const int smem = kN * kN * sizeof(double);
-    e = cudaFuncSetAttribute(jacobi, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e = cudaFuncSetAttribute(jacobi, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     jacobi<<<hkv, 1024, smem, s>>>(w);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     assemble<<<hkv, 128, 0, s>>>(w, rk);
-    count_launches(3);
+    count_launches(2);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_build_rk(const float* q, int64_t n, int hkv, float* rk, void* ws, cudaStream_t s) {
+    double* w = (double*)ws;
+    covariance<<<dim3(kN, hkv), 128, 0, s>>>(q, n, w);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    count_launches(1);
+    return eigen_and_assemble(hkv, rk, w, s);
+}
+
+size_t cq_acc_bytes(int hkv) { return (size_t)hkv * (kN * kN * sizeof(double) + sizeof(long long)); }
+
+cudaError_t launch_cq_accumulate(const float* q, int64_t n, int hkv, void* acc, cudaStream_t s) {
+    double* sums = (double*)acc;
+    long long* counts = (long long*)(sums + (size_t)hkv * kN * kN);
+    cq_accumulate<<<dim3(kN, hkv), 128, 0, s>>>(q, n, sums, counts);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_cq_finalize(const void* acc, int hkv, float* rk, void* ws, cudaStream_t s) {
+    const double* sums = (const double*)acc;
+    const long long* counts = (const long long*)(sums + (size_t)hkv * kN * kN);
+    double* w = (double*)ws;
+    cq_normalise<<<dim3(kN, hkv), 128, 0, s>>>(sums, counts, w);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    count_launches(1);
+    return eigen_and_assemble(hkv, rk, w, s);
+}
+
+int sv_max_keys() { return kSvMaxKeys; }
+
+cudaError_t launch_score_weighted(const float* q, int64_t n, const float* k, const float* v, int t_keys, int hkv, float* y,
+                                  cudaStream_t s) {
+    const int smem = t_keys * (int)sizeof(float);
+    cudaError_t e = cudaFuncSetAttribute(score_weighted, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    score_weighted<<<dim3((unsigned)n, hkv), 128, smem, s>>>(q, n, k, v, t_keys, y);
+    count_launches(1);
     return cudaGetLastError();
 }
 

@@ -150,6 +150,12 @@ cudaError_t launch_decode_step(const DecodeParams& p, const AppendParams& a, cud
 int mma_units_per_cta(int g);   // units (warp pairs) per CTA of the warp-MMA kernel for G heads per KV head
 cudaError_t launch_build_rk(const float* q, int64_t n, int hkv, float* rk, void* ws, cudaStream_t s);
 size_t build_rk_ws_bytes(int hkv);
+size_t cq_acc_bytes(int hkv);
+cudaError_t launch_cq_accumulate(const float* q, int64_t n, int hkv, void* acc, cudaStream_t s);
+cudaError_t launch_cq_finalize(const void* acc, int hkv, float* rk, void* ws, cudaStream_t s);
+int sv_max_keys();
+cudaError_t launch_score_weighted(const float* q, int64_t n, const float* k, const float* v, int t_keys, int hkv, float* y,
+                                  cudaStream_t s);
 
 void count_launches(int n);
 
