@@ -55,7 +55,9 @@ using namespace ptx;
 // warps per CTA: 12 (168 registers each) when one m-tile holds the G heads (G <= 8); 8 (255
 // registers) for two head tiles, whose query fragments and accumulators need twice the registers
 __host__ __device__ constexpr int warps_for(int G) { return G <= 8 ? 12 : 8; }
-constexpr int kStagesPerWarp = 3;
+// page stages per warp: 2 for one head tile (measured: no slower than 3, and 61 KB of shared memory
+// freed), 3 for two head tiles, whose longer compute per page needs the deeper prefetch
+__host__ __device__ constexpr int stages_for(int G) { return G <= 8 ? 2 : 3; }
 // A raise of the reference max leaves the largest logit this far below tau.  The half step keeps
 // the largest probabilities off exact powers of two: with p = 2^k (1 - e) for a nearly flat
 // attention, fp16(p * s_V) would round back to the fp16 value 2^k s_V for every token, a bias
@@ -66,14 +68,15 @@ constexpr float kTauMax = 40.0f;    // tau of a segment before any non-zero valu
 constexpr float kQScaleM = 1.4426950408889634f * 0.08838834764831845f;   // log2(e) / sqrt(128)
 constexpr float kTwo18 = 262144.0f;
 
-template <int W>
+template <int W, int S>
 struct MmaSmem {
-    uint8_t stage[W][kStagesPerWarp][kPageHeadBytes];
-    uint64_t full[W][kStagesPerWarp];
+    uint8_t stage[W][S][kPageHeadBytes];
+    uint64_t full[W][S];
     // per-token scales of the current page, token pairs (2p, 2p + 1) side by side:
     // [0] key (2^18 s0, 2^18 s0'), (m0, m0'); [1] key (2^18 s1, ...), (m1, ...); [2] value (s0, ...), (m0, ...);
     // [3] value (s1, ...), (m1, ...)
     float4 tsc[W][4][32];
+    float tau[W];       // each warp's reference slack tau (log2 units), see the kernel
 };
 
 
@@ -141,7 +144,9 @@ __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
 }
 
 
-template <int G>
+// FMT64: the default page format (keys and values in groups of 64) as compile-time offsets;
+// otherwise the cache's format is read from the parameters.
+template <int G, bool FMT64>
 __global__ void __launch_bounds__(32 * warps_for(G), 1) decode_mma(const __grid_constant__ DecodeParams p) {
     constexpr int MT = (G + 7) / 8;              // heads per thread (rows g and g + 8 of each m-tile)
     constexpr int NT = MT == 1 ? 4 : 2;          // score n-tiles per chunk (8 tokens each)
@@ -149,10 +154,12 @@ __global__ void __launch_bounds__(32 * warps_for(G), 1) decode_mma(const __grid_
     constexpr int KK = NT / 2;                   // PV k-steps per chunk
     extern __shared__ __align__(128) uint8_t smem_raw[];
     constexpr int W = warps_for(G);
-    MmaSmem<W>* sm = reinterpret_cast<MmaSmem<W>*>(smem_raw);
+    constexpr int kStagesPerWarp = stages_for(G);
+    MmaSmem<W, kStagesPerWarp>* sm = reinterpret_cast<MmaSmem<W, kStagesPerWarp>*>(smem_raw);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int g = lane >> 2, tig = lane & 3;
+    const PageFmt f = FMT64 ? page_fmt(64, 64) : p.fmt;
     const int gw = blockIdx.x * W + warp;
     const int P0 = (int)(((long long)gw * p.total_pages) / p.n_units);
     const int P1 = (int)(((long long)(gw + 1) * p.total_pages) / p.n_units);
@@ -183,8 +190,8 @@ __global__ void __launch_bounds__(32 * warps_for(G), 1) decode_mma(const __grid_
         if (lane == 0) {
             const int s = q % kStagesPerWarp;
             const uint32_t bar = smem_u32(&sm->full[warp][s]);
-            mbar_expect_tx(bar, p.fmt.bytes);
-            bulk_g2s(smem_u32(sm->stage[warp][s]), p.pool + (size_t)blk * p.fmt.bytes, p.fmt.bytes, bar);
+            mbar_expect_tx(bar, f.bytes);
+            bulk_g2s(smem_u32(sm->stage[warp][s]), p.pool + (size_t)blk * f.bytes, f.bytes, bar);
         }
         ++issued;
     };
@@ -199,9 +206,9 @@ __global__ void __launch_bounds__(32 * warps_for(G), 1) decode_mma(const __grid_
     float qscale = 1.f, kscale = kTwo18;   // power-of-two query scale of the segment and 2^18 / it
     // Reference-max slack tau (log2 units): probabilities stay at most 2^tau, and tau is lowered so
     // that 2^tau times the largest value scale seen in the segment stays below 2^15, so that
-    // P' = p * s_V cannot overflow fp16; ptau = 2^tau.  A raise of the reference puts the largest
-    // logit at tau - 7.5, so the dominant probabilities sit about 2^7.5 below the limit.
-    float tau = kTauMax, ptau = __uint_as_float((uint32_t)(127 + (int)kTauMax) << 23);
+    // P' = p * s_V cannot overflow fp16.  A raise of the reference puts the largest logit at
+    // tau - 7.5, so the dominant probabilities sit about 2^7.5 below the limit.  tau lives in shared
+    // memory (sm->tau[warp]): it changes rarely and is read once per page and once per chunk.
     float o[8][MT][4];              // output^T accumulators: channel tile cm, head tile nh
     // sum of P' over the current page: rows g (value group 0) and g + 8 (group 1) of one MMA
     // accumulator, heads 2 tig, 2 tig + 1
@@ -290,8 +297,8 @@ __global__ void __launch_bounds__(32 * warps_for(G), 1) decode_mma(const __grid_
             for (int k = 0; k < MT; ++k) psum[k][0] = psum[k][1] = psum[k][2] = psum[k][3] = 0.f;
             seg_start = false;
             fresh = true;
-            tau = kTauMax;
-            ptau = __uint_as_float((uint32_t)(127 + (int)kTauMax) << 23);
+            if (lane == 0) sm->tau[warp] = kTauMax;
+            __syncwarp();
         }
         const bool got = wait_full(smem_u32(&sm->full[warp][s]), (i / kStagesPerWarp) & 1, p.err, p.wait_iters);
         if (!__all_sync(0xffffffffu, got)) break;      // error word set; stop issuing, drain below
@@ -304,58 +311,57 @@ __global__ void __launch_bounds__(32 * warps_for(G), 1) decode_mma(const __grid_
         // Slots past the request's end are staged as 0 (their bytes may be anything); a full page
         // takes a copy of the loop without that test
         auto stage = [&](const bool full) {
-        float val[2][8];
+        float vmax = 0.f;   // largest value scale of this thread's two tokens
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
             const int t = lane + 32 * hh;
             const bool live = full || t < n_live;
             // one (s, m) pair per 64-channel group, or one pair for both halves of a 128-channel group
             uint2 ksm, vsm;
-            if (p.fmt.gk == 64) {
+            if (FMT64 || f.gk == 64) {
                 ksm = *reinterpret_cast<const uint2*>(pg + kKSm + t * 8);
             } else {
                 ksm.x = ksm.y = *reinterpret_cast<const uint32_t*>(pg + kKSm + t * 4);
             }
-            if (p.fmt.gv == 64) {
-                vsm = *reinterpret_cast<const uint2*>(pg + p.fmt.v_sm + t * 8);
+            if (FMT64 || f.gv == 64) {
+                vsm = *reinterpret_cast<const uint2*>(pg + f.v_sm + t * 8);
             } else {
-                vsm.x = vsm.y = *reinterpret_cast<const uint32_t*>(pg + p.fmt.v_sm + t * 4);
+                vsm.x = vsm.y = *reinterpret_cast<const uint32_t*>(pg + f.v_sm + t * 4);
             }
-            val[hh][0] = live ? kscale * __half2float(__ushort_as_half(ksm.x & 0xffff)) : 0.f;
-            val[hh][1] = live ? __half2float(__ushort_as_half(ksm.x >> 16)) : 0.f;
-            val[hh][2] = live ? kscale * __half2float(__ushort_as_half(ksm.y & 0xffff)) : 0.f;
-            val[hh][3] = live ? __half2float(__ushort_as_half(ksm.y >> 16)) : 0.f;
             // values: the scale s, and the centred minimum m + 1.5 s (the output MMAs take code - 1.5)
             const float sv0 = __half2float(__ushort_as_half(vsm.x & 0xffff));
             const float sv1 = __half2float(__ushort_as_half(vsm.y & 0xffff));
-            val[hh][4] = live ? sv0 : 0.f;
-            val[hh][5] = live ? fmaf(1.5f, sv0, __half2float(__ushort_as_half(vsm.x >> 16))) : 0.f;
-            val[hh][6] = live ? sv1 : 0.f;
-            val[hh][7] = live ? fmaf(1.5f, sv1, __half2float(__ushort_as_half(vsm.y >> 16))) : 0.f;
+            const float val[8] = {
+                live ? kscale * __half2float(__ushort_as_half(ksm.x & 0xffff)) : 0.f,
+                live ? __half2float(__ushort_as_half(ksm.x >> 16)) : 0.f,
+                live ? kscale * __half2float(__ushort_as_half(ksm.y & 0xffff)) : 0.f,
+                live ? __half2float(__ushort_as_half(ksm.y >> 16)) : 0.f,
+                live ? sv0 : 0.f,
+                live ? fmaf(1.5f, sv0, __half2float(__ushort_as_half(vsm.x >> 16))) : 0.f,
+                live ? sv1 : 0.f,
+                live ? fmaf(1.5f, sv1, __half2float(__ushort_as_half(vsm.y >> 16))) : 0.f};
+            vmax = fmaxf(vmax, fmaxf(val[4], val[6]));
+            float* row = reinterpret_cast<float*>(&sm->tsc[warp][0][t >> 1]);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                row[j * 128 + (t & 1)] = val[2 * j];
+                row[j * 128 + 2 + (t & 1)] = val[2 * j + 1];
+            }
         }
-        // value scales against the slack: 2^tau * s_V must stay below 2^15 (thread-local test; the
-        // warp-wide maximum and the new tau only on the rare path: the first page with non-zero
-        // value scales of a segment, or a page whose scales are larger than any before)
-        const float vmax = fmaxf(fmaxf(val[0][4], val[0][6]), fmaxf(val[1][4], val[1][6]));
-        if (__any_sync(0xffffffffu, vmax * ptau >= 32768.f)) {
+        // value scales against the slack: 2^tau * s_V must stay below 2^15, i.e. s_V < vlim =
+        // 2^(15 - tau) (thread-local test; the warp-wide maximum and the new tau only on the rare
+        // path: the first page with non-zero value scales of a segment, or a page whose scales are
+        // larger than any before)
+        const float vlim = __uint_as_float((uint32_t)(127 + 15 - (int)sm->tau[warp]) << 23);
+        if (__any_sync(0xffffffffu, vmax >= vlim)) {
             float w = vmax;
 #pragma unroll
             for (int o2 = 1; o2 < 32; o2 <<= 1) w = fmaxf(w, __shfl_xor_sync(0xffffffffu, w, o2));
             // w * 2^tau in [2^14, 2^15): tau = 14 - floor(log2 w) (w > 0 and normal: an fp16 value)
             const int ew = (int)((__float_as_uint(w) >> 23) & 0xff) - 127;
             const int tnew = 14 - ew;
-            tau = (float)tnew;
-            ptau = __uint_as_float((uint32_t)(127 + tnew) << 23);
-        }
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-            const int t = lane + 32 * hh;
-            float* row = reinterpret_cast<float*>(&sm->tsc[warp][0][t >> 1]);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                row[j * 128 + (t & 1)] = val[hh][2 * j];
-                row[j * 128 + 2 + (t & 1)] = val[hh][2 * j + 1];
-            }
+            __syncwarp();
+            if (lane == 0) sm->tau[warp] = (float)tnew;
         }
         };
         if (n_live == kPage) stage(true);
@@ -427,6 +433,7 @@ __global__ void __launch_bounds__(32 * warps_for(G), 1) decode_mma(const __grid_
         };
         // reference-max update (thread-local test, rare warp-wide raise)
         auto update = [&](float2 (&lg)[MT][NT]) {
+            const float tau = sm->tau[warp];
             // thread-local test first: the row-group reduction runs only when some logit of the
             // warp passed the reference by 2^tau (or the segment is fresh)
             float cml[MT];
@@ -511,7 +518,7 @@ __global__ void __launch_bounds__(32 * warps_for(G), 1) decode_mma(const __grid_
             // ---- output^T: O[cm] += V^T[channels 16 cm + g, + 8][tokens] x P'_{group(cm)}
             // value words of this thread for the chunk's k-steps: [channel half q][k-step][s]
             {
-                const uint8_t* vsrc = pg + p.fmt.v_codes + 1024 * (cbase >> 5) + 16 * lane;
+                const uint8_t* vsrc = pg + f.v_codes + 1024 * (cbase >> 5) + 16 * lane;
                 uint32_t vw[2][KK][2];
 #pragma unroll
                 for (int q = 0; q < 2; ++q) {
@@ -665,22 +672,28 @@ __global__ void __launch_bounds__(32 * warps_for(G), 1) decode_mma(const __grid_
             wait_full(smem_u32(&sm->full[warp][q % kStagesPerWarp]), (q / kStagesPerWarp) & 1, p.err, kDrainIters);
 }
 
-template <int G>
-cudaError_t launch_mma_g(const DecodeParams& p, cudaStream_t s) {
+template <int G, bool FMT64>
+cudaError_t launch_mma_gf(const DecodeParams& p, cudaStream_t s) {
     constexpr int W = warps_for(G);
-    const int smem = (int)sizeof(MmaSmem<W>);
+    const int smem = (int)sizeof(MmaSmem<W, stages_for(G)>);
     static bool attr_set[kMaxDevices] = {};   // once per instantiation and device
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
     if (!attr_set[dev]) {
-        e = cudaFuncSetAttribute(decode_mma<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        e = cudaFuncSetAttribute(decode_mma<G, FMT64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
-    decode_mma<G><<<p.n_units / W, 32 * W, smem, s>>>(p);
+    decode_mma<G, FMT64><<<p.n_units / W, 32 * W, smem, s>>>(p);
     return cudaGetLastError();
+}
+
+template <int G>
+cudaError_t launch_mma_g(const DecodeParams& p, cudaStream_t s) {
+    if (p.fmt.gk == 64 && p.fmt.gv == 64) return launch_mma_gf<G, true>(p, s);
+    return launch_mma_gf<G, false>(p, s);
 }
 
 }  // namespace

@@ -317,3 +317,18 @@ class OracleCache:
     def attend(self, q: np.ndarray):
         k16, v16 = self.bf16_tokens()
         return attention(q, self.rk, self.kc, self.ks, self.vc, self.vs, k16, v16, self.group_k, self.group_v)
+
+    def attend_upto(self, q: np.ndarray, last: int):
+        """Attention of G heads over the cached positions 0 .. last only, each at the precision the
+        cache holds it in now (the causal view of one query of a chunk appended as a whole; reading
+        of the mixed-precision cache for chunked prefill)."""
+        (s0, s1), (i0, i1), (w0, w1), _ = regions(self.length, self.sink, self.window)
+        pos = [p for p in list(range(s0, s1)) + list(range(w0, w1)) if p <= last]
+        n_int2 = max(0, min(i1, last + 1) - i0)
+        if pos:
+            k16 = np.stack([self.k16[p] for p in pos])
+            v16 = np.stack([self.v16[p] for p in pos])
+        else:
+            k16 = v16 = np.zeros((0, D), np.uint16)
+        return attention(q, self.rk, self.kc[:n_int2], self.ks[:n_int2], self.vc[:n_int2], self.vs[:n_int2],
+                         k16, v16, self.group_k, self.group_v)
