@@ -222,6 +222,26 @@ int oscar_decode_step(oscar_cache *c, const void *k, const void *v, const void *
                       const float *rk, void *out, int32_t out_dtype, void *workspace,
                       size_t workspace_bytes, void *stream);
 
+/* oscar_prefill_attention: attention of the queries of a chunk of new tokens (chunked prefill).
+ * Each request b must have just appended its last n_q[b] tokens (host array, 0 <= n_q[b] <= 256 and
+ * <= its length) through kv_quant_append; q (device, [sum_b n_q[b]][num_q_heads][128], requests in
+ * order, tokens in position order; OSCAR_DTYPE_F32 or OSCAR_DTYPE_BF16) holds their queries, and
+ * out (device, same layout, out_dtype) receives, for the query at position p, softmax attention over
+ * the request's cached positions 0 .. p, each in the precision the cache holds it in after the append
+ * (BF16 sink and window, INT2 history): with at most 256 new tokens every INT2 token precedes every
+ * query, so the causal limit only cuts the BF16 window.  The queries of a request are processed in
+ * groups of up to 16 / G that share every unpacked page (as extra head rows of the decode kernels).
+ * workspace (device, >= oscar_prefill_workspace_bytes(c), 16-byte aligned).  Requires the
+ * warp-MMA decode path (OSCAR_EINVAL otherwise).  Errors: OSCAR_ERANGE (an n_q out of range),
+ * OSCAR_EWORKSPACE, OSCAR_EALIGN, OSCAR_EINVAL.
+ * Source: techllm.github.io page, section "OSCAR" (the mixed-precision paged cache serves long
+ * prompts); the causal view of a cache that holds the chunk in mixed precision is this library's
+ * reading (the pages do not describe prefill attention). */
+size_t oscar_prefill_workspace_bytes(const oscar_cache *c);
+int oscar_prefill_attention(oscar_cache *c, const void *q, int32_t q_dtype, const int32_t *n_q,
+                            const float *rk, void *out, int32_t out_dtype, void *workspace,
+                            size_t workspace_bytes, void *stream);
+
 /* Which decode kernel oscar_decode_attention runs (process-wide; default OSCAR_PATH_WARP_MMA):
  * OSCAR_PATH_WARP_MMA: every warp streams its own contiguous run of INT2 pages through a
  *                      bulk-async-copy ring and runs scores and P.V on warp-level tensor-core
@@ -243,9 +263,9 @@ int oscar_set_decode_path(int32_t path);
  * measurement aid. */
 int oscar_kernel_timing(oscar_cache *c, int32_t capacity);
 int oscar_kernel_timing_read(oscar_cache *c, float *ms, int32_t max_n, int32_t *n_out);
-/* Synchronise `stream` and report whether the last decode call that used `workspace`
+/* Synchronise `stream` and report whether the last decode or prefill call that used `workspace`
  * completed normally (OSCAR_OK) or one of its bounded in-kernel waits gave up
- * (OSCAR_ETIMEOUT; its output is then undefined). */
+ * (OSCAR_ETIMEOUT; its output is then undefined).  The flag is the workspace's first word. */
 int oscar_decode_status(const void *workspace, size_t workspace_bytes, const oscar_cache *c,
                         void *stream);
 /* Limit of the bounded waits inside the decode kernels (process-wide): a wait for a page copy

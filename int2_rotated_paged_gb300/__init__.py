@@ -38,7 +38,8 @@ EXPORTS = [
     "oscar_set_decode_path", "oscar_decode_status", "oscar_decode_attention_noalloc", "oscar_decode_step",
     "oscar_kernel_timing", "oscar_kernel_timing_read", "oscar_set_wait_limit", "oscar_decode_status_noalloc",
     "oscar_set_wait_probe", "oscar_page_head_bytes", "oscar_cq_accumulator_bytes", "oscar_cq_reset",
-    "oscar_cq_accumulate", "oscar_cq_finalize", "oscar_score_weighted_values",
+    "oscar_cq_accumulate", "oscar_cq_finalize", "oscar_score_weighted_values", "oscar_prefill_workspace_bytes",
+    "oscar_prefill_attention",
 ]
 OSCAR_ESCRATCH = -8
 OSCAR_ETIMEOUT = -7
@@ -110,6 +111,8 @@ def lib() -> ctypes.CDLL:
         "oscar_set_wait_limit": (ctypes.c_int, [I32]),
         "oscar_set_wait_probe": (ctypes.c_int, [I32]),
         "oscar_cq_accumulator_bytes": (SZ, [I32]),
+        "oscar_prefill_workspace_bytes": (SZ, [P]),
+        "oscar_prefill_attention": (ctypes.c_int, [P, P, I32, P, P, P, I32, P, SZ, P]),
         "oscar_cq_reset": (ctypes.c_int, [P, I32, P]),
         "oscar_cq_accumulate": (ctypes.c_int, [P, I64, I32, P, P]),
         "oscar_cq_finalize": (ctypes.c_int, [P, I32, P, P, SZ, P]),
@@ -234,6 +237,19 @@ def oscar_build_rk(q, n: int, num_kv_heads: int, rk, workspace, stream=None):
     nbytes = workspace.numel() * workspace.element_size()
     _check("oscar_build_rk", lib().oscar_build_rk(_ptr(q), n, num_kv_heads, _ptr(rk), _ptr(workspace),
                                                   nbytes, _stream(stream)))
+
+
+def oscar_prefill_workspace_bytes(cache) -> int:
+    return int(lib().oscar_prefill_workspace_bytes(cache))
+
+
+def oscar_prefill_attention(cache, q, q_dtype: int, n_q: Sequence[int], rk, out, out_dtype: int, workspace,
+                            stream=None):
+    """Causal attention of the queries of the chunk each request just appended (n_q[b] tokens)."""
+    nbytes = workspace.numel() * workspace.element_size()
+    _check("oscar_prefill_attention", lib().oscar_prefill_attention(
+        cache, _ptr(q), q_dtype, _host_i32(n_q), _ptr(rk), _ptr(out), out_dtype, _ptr(workspace), nbytes,
+        _stream(stream)))
 
 
 def oscar_cq_accumulator_bytes(num_kv_heads: int) -> int:
@@ -375,6 +391,16 @@ class Cache:
         qd = DTYPE_BF16 if str(q.dtype) == "torch.bfloat16" else DTYPE_F32
         od = DTYPE_BF16 if str(out.dtype) == "torch.bfloat16" else DTYPE_F32
         oscar_decode_step(self.handle, k, v, q, qd, rk, out, od, self.workspace, stream)
+
+    def prefill(self, q, n_q: Sequence[int], rk, out, workspace=None, stream=None):
+        """Chunked-prefill attention of the n_q[b] tokens each request just appended (queries q)."""
+        import torch
+        if workspace is None:
+            workspace = torch.empty(oscar_prefill_workspace_bytes(self.handle), dtype=torch.uint8, device=q.device)
+        qd = DTYPE_BF16 if str(q.dtype) == "torch.bfloat16" else DTYPE_F32
+        od = DTYPE_BF16 if str(out.dtype) == "torch.bfloat16" else DTYPE_F32
+        oscar_prefill_attention(self.handle, q, qd, n_q, rk, out, od, workspace, stream)
+        return workspace
 
     def status(self, stream=None):
         """Raise if the last decode on this cache's workspace hit a bounded in-kernel wait."""

@@ -343,6 +343,18 @@ int kv_quant_append(oscar_cache* c, const void* k, const void* v, const int32_t*
 
 // ------------------------------------------------------------------ read path
 
+// request slots of a decode call: slot b is request b with its one query (identity mapping)
+static void identity_slots(DecodeParams& p) {
+    p.g_real = p.g;
+    p.qpr = 1;
+    for (int32_t b = 0; b < p.batch; ++b) {
+        p.row[b] = b;
+        p.q0[b] = b;
+        p.nq[b] = 1;
+        p.lim[b] = INT32_MAX;
+    }
+}
+
 static const int kMaxSplits = 64;   // SIMT path: INT2 splits + 1 BF16 split per (request, KV head)
 static std::atomic<int> g_decode_path{OSCAR_PATH_WARP_MMA};
 static constexpr int kDefaultWaitIters = 2000;   // about 2 s
@@ -389,16 +401,18 @@ struct WsLayout {
     size_t qrot, simt, mma, bf16, err, total;
 };
 
+// Workspace layouts: the error word first (offset 0 in every layout, so one status query serves
+// decode and prefill workspaces alike), then the rotated queries and the split-K partials.
 static WsLayout ws_layout(const oscar_cache* c) {
     const size_t per = (size_t)c->g * (2 + kD) * sizeof(float);
     const size_t bh = (size_t)c->d.batch * c->d.num_kv_heads;
     WsLayout w;
-    w.qrot = 0;
+    w.err = 0;
+    w.qrot = 256;
     w.simt = w.qrot + (size_t)c->d.batch * c->d.num_q_heads * kD * sizeof(float);
     w.mma = w.simt + bh * kMaxSplits * per;
     w.bf16 = w.mma + (bh + kMaxMmaUnits) * per;   // one slot per (request, KV head) run of a unit
-    w.err = w.bf16 + bh * per;
-    w.total = w.err + 16;
+    w.total = w.bf16 + bh * per;
     return w;
 }
 
@@ -431,7 +445,7 @@ int oscar_set_wait_probe(int32_t on) {
 int oscar_decode_status(const void* workspace, size_t workspace_bytes, const oscar_cache* c, void* stream) {
     if (!c || !workspace) return OSCAR_EINVAL;
     const WsLayout w = ws_layout(c);
-    if (workspace_bytes < w.total) return OSCAR_EWORKSPACE;
+    if (workspace_bytes < w.err + sizeof(int32_t)) return OSCAR_EWORKSPACE;
     int32_t err = 0;
     cudaError_t e = cudaMemcpyAsync(&err, (const uint8_t*)workspace + w.err, sizeof(err), cudaMemcpyDeviceToHost,
                                     S(stream));
@@ -491,6 +505,7 @@ static int prepare_decode(oscar_cache* c, const void* q, int32_t q_dtype, const 
     p.page_off[c->d.batch] = (int32_t)pages;
     if (pages > INT32_MAX / 4) return OSCAR_ERANGE;
     p.total_pages = (int32_t)pages;
+    identity_slots(p);
     if (p.path == OSCAR_PATH_WARP_MMA && pages > 0) {
         rc = mma_unit_count(c->g, pages, &p.n_units);
         if (rc != OSCAR_OK) return rc;
@@ -569,6 +584,123 @@ int oscar_kernel_timing_read(oscar_cache* c, float* ms, int32_t max_n, int32_t* 
     }
     *n_out = n;
     c->timing_used = 0;
+    return OSCAR_OK;
+}
+
+// ------------------------------------------------------------------ chunked prefill attention
+
+// Query tokens per request slot: the most that keep qpr * G a head count the kernels take
+// (1..8, 12, 16), so that one unpacked page serves several queries.
+static int prefill_qpr(int g) {
+    for (int k = 16 / g; k > 1; --k) {
+        const int gv = k * g;
+        if (gv <= 8 || gv == 12 || gv == 16) return k;
+    }
+    return 1;
+}
+
+static WsLayout prefill_ws_layout(const oscar_cache* c) {
+    const int gv = c->g * prefill_qpr(c->g);
+    const size_t per = (size_t)gv * (2 + kD) * sizeof(float);
+    const size_t bh = (size_t)kMaxBatch * c->d.num_kv_heads;
+    WsLayout w;
+    w.err = 0;
+    w.qrot = 256;
+    w.simt = w.qrot + (size_t)kMaxBatch * c->d.num_kv_heads * gv * kD * sizeof(float);
+    w.mma = w.simt;                                 // no SIMT partials on this path
+    w.bf16 = w.mma + (bh + kMaxMmaUnits) * per;
+    w.total = w.bf16 + bh * per;
+    return w;
+}
+
+size_t oscar_prefill_workspace_bytes(const oscar_cache* c) {
+    if (!c) return 0;
+    return prefill_ws_layout(c).total;
+}
+
+int oscar_prefill_attention(oscar_cache* c, const void* q, int32_t q_dtype, const int32_t* n_q, const float* rk,
+                            void* out, int32_t out_dtype, void* workspace, size_t workspace_bytes, void* stream) {
+    if (!c || !n_q) return OSCAR_EINVAL;
+    if (g_decode_path != OSCAR_PATH_WARP_MMA) return OSCAR_EINVAL;
+    int64_t rows = 0;
+    for (int32_t b = 0; b < c->d.batch; ++b) {
+        if (n_q[b] < 0 || n_q[b] > kWindow || n_q[b] > c->len[b]) return OSCAR_ERANGE;
+        rows += n_q[b];
+    }
+    if (rows == 0) return OSCAR_OK;
+    if (!q || !rk || !out) return OSCAR_EINVAL;
+    if ((q_dtype != OSCAR_DTYPE_F32 && q_dtype != OSCAR_DTYPE_BF16) ||
+        (out_dtype != OSCAR_DTYPE_F32 && out_dtype != OSCAR_DTYPE_BF16))
+        return OSCAR_EINVAL;
+    const WsLayout w = prefill_ws_layout(c);
+    if (!workspace || workspace_bytes < w.total) return OSCAR_EWORKSPACE;
+    if (!aligned16(q) || !aligned16(rk) || !aligned16(out) || !aligned16(workspace)) return OSCAR_EALIGN;
+    int rc = sync(c, S(stream));
+    if (rc != OSCAR_OK) return rc;
+    const int qpr = prefill_qpr(c->g);
+    uint8_t* ws = (uint8_t*)workspace;
+    // request slots: runs of qpr consecutive chunk queries of one request, launched 256 slots at a time
+    struct Slot {
+        int32_t row, q0, nq, lim;
+    };
+    std::vector<Slot> slots;
+    int64_t qrow = 0;
+    for (int32_t b = 0; b < c->d.batch; ++b) {
+        const int64_t first = c->len[b] - n_q[b];     // position of the chunk's first token
+        for (int32_t i = 0; i < n_q[b]; i += qpr)
+            slots.push_back({b, (int32_t)(qrow + i), std::min(qpr, n_q[b] - i), (int32_t)(first + i)});
+        qrow += n_q[b];
+    }
+    for (size_t s0 = 0; s0 < slots.size(); s0 += kMaxBatch) {
+        const int32_t nb = (int32_t)std::min<size_t>(kMaxBatch, slots.size() - s0);
+        DecodeParams p;
+        std::memset(&p, 0, sizeof(p));
+        p.fmt = c->fmt;
+        p.batch = nb;
+        p.hkv = c->d.num_kv_heads;
+        p.g = c->g * qpr;
+        p.g_real = c->g;
+        p.qpr = qpr;
+        p.pps = 4;
+        p.max_splits = kMaxSplits;
+        p.q = q;
+        p.q_dtype = q_dtype;
+        p.rk = rk;
+        p.out = out;
+        p.out_dtype = out_dtype;
+        p.pool = c->pool;
+        p.bf16 = c->bf16;
+        p.page_table = c->pt;
+        p.max_pps = c->d.max_pages_per_seq;
+        p.qrot = (float*)(ws + w.qrot);
+        p.partial = nullptr;
+        p.part_mma = (float*)(ws + w.mma);
+        p.part_bf16 = (float*)(ws + w.bf16);
+        p.err = (int32_t*)(ws + w.err);
+        p.path = OSCAR_PATH_WARP_MMA;
+        p.wait_iters = g_wait_iters;
+        p.wait_probe = g_wait_probe;
+        int64_t pages = 0;
+        for (int32_t v = 0; v < nb; ++v) {
+            const Slot& sl = slots[s0 + v];
+            p.len[v] = (int32_t)c->len[sl.row];
+            p.row[v] = sl.row;
+            p.q0[v] = sl.q0;
+            p.nq[v] = sl.nq;
+            p.lim[v] = sl.lim;
+            p.page_off[v] = (int32_t)pages;
+            pages += (int64_t)int2_pages(p.len[v]) * c->d.num_kv_heads;
+        }
+        p.page_off[nb] = (int32_t)pages;
+        if (pages > INT32_MAX / 4) return OSCAR_ERANGE;
+        p.total_pages = (int32_t)pages;
+        if (pages > 0) {
+            rc = mma_unit_count(p.g, pages, &p.n_units);
+            if (rc != OSCAR_OK) return rc;
+        }
+        cudaError_t e = launch_decode(p, S(stream));
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
     return OSCAR_OK;
 }
 
@@ -768,6 +900,7 @@ int noalloc_decode_params(oscar_cache* c, const void* q, int32_t q_dtype, const 
     p.page_off[c->d.batch] = (int32_t)pages;
     if (pages > INT32_MAX / 4) return OSCAR_ERANGE;
     p.total_pages = (int32_t)pages;
+    identity_slots(p);
     if (pages > 0) {
         const int rc = mma_unit_count(c->g, pages, &p.n_units);
         if (rc != OSCAR_OK) return rc;

@@ -355,7 +355,10 @@ __global__ void __launch_bounds__(32 * kMaxG) combine_mma(const __grid_constant_
         r0 = make_float2(o0.x * inv, o0.y * inv);
         r1 = make_float2(o1.x * inv, o1.y * inv);
     }
-    const size_t obase = ((size_t)b * p.hkv * p.g + (size_t)h * p.g + hh) * kD;
+    // output row of head row hh: query token hh / g_real of the slot, head h * g_real + hh % g_real
+    const int j = hh / p.g_real;
+    if (j >= p.nq[b]) return;
+    const size_t obase = (((size_t)p.q0[b] + j) * p.hkv * p.g_real + (size_t)h * p.g_real + hh % p.g_real) * kD;
     if (p.out_dtype == 0) {
         float* out = reinterpret_cast<float*>(p.out) + obase;
         *reinterpret_cast<float2*>(out + 2 * lane) = r0;

@@ -178,7 +178,7 @@ __global__ void __launch_bounds__(32 * warps_for(G), 1) decode_mma(const __grid_
         if (base + lane >= n) return 0;
         PageIt t;
         t.init(p, P);
-        return p.page_table[(size_t)t.b * p.max_pps + t.j] * p.hkv + t.h;
+        return p.page_table[(size_t)p.row[t.b] * p.max_pps + t.j] * p.hkv + t.h;
     };
     int pt_base = 0;
     int32_t pt_cur = fetch_pt(0);

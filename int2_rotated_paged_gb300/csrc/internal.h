@@ -121,6 +121,17 @@ struct DecodeParams {
     int32_t total_pages;   // INT2 pages over all (request, KV head)
     int32_t n_units;       // page-streaming units (warp pairs) of the warp-MMA kernel
     int32_t page_off[kMaxBatch + 1];   // sum over earlier requests of pages * hkv
+    // Request slots and query rows.  Slot b of a launch reads the page-table row, BF16 region and
+    // cached tokens of request row[b] (len[b] is that request's length); its g query rows are qpr
+    // query tokens x g_real heads, query j of the slot being row q0[b] + j of the caller's q and out
+    // ([rows][hkv * g_real][128]) and seeing positions <= lim[b] + j; rows of queries j >= nq[b] are
+    // unused.  A decode call is the identity (row[b] = q0[b] = b, qpr = 1, nq = 1, lim = INT32_MAX);
+    // chunked prefill packs qpr queries of one request into a slot.
+    int32_t g_real, qpr;
+    int32_t row[kMaxBatch];
+    int32_t q0[kMaxBatch];
+    int32_t nq[kMaxBatch];
+    int32_t lim[kMaxBatch];
 };
 
 // Split-K partition of one request: INT2 splits of `pps` pages plus one BF16 split.

@@ -106,7 +106,14 @@ __device__ __forceinline__ void prep_body(const DecodeParams& p, const AppendPar
         }
         if (h == 0 && c == 0) ap->seq_lens[b] = r.len0 + r.n_new;
     }
-    for (int i = c; i < G * kD; i += NT) qs[i / kD][i % kD] = load_query(p, qbase + (size_t)i);
+    // query row r of the slot: query token r / g_real (of the slot's nq) and head h * g_real + r % g_real
+    // of the caller's layout [rows][hkv * g_real][128]; rows of missing query tokens are zero
+    for (int i = c; i < G * kD; i += NT) {
+        const int r = i / kD, j = r / p.g_real;
+        qs[r][i % kD] = j < p.nq[b] ? load_query(p, (((size_t)p.q0[b] + j) * p.hkv * p.g_real + (size_t)h * p.g_real +
+                                                     r % p.g_real) * kD + i % kD)
+                                    : 0.f;
+    }
     __syncthreads();
 
     // ---- q~[i][col] = sum_j q[i][j] R_h[j][col]: column col of R_h, 32 rows in flight; with
@@ -152,6 +159,11 @@ __device__ __forceinline__ void prep_body(const DecodeParams& p, const AppendPar
     // ---- BF16 sink + window
     const int len = p.len[b];
     const int n_sink = min(len, kSink), n_win = min(kWindow, max(0, len - kSink));
+    // causal view (chunked prefill): head row x of query token x / g_real sees positions <= lim + x / g_real;
+    // a window slot holds position w0 + ((slot - 64 - (w0 - 64)) mod 256), w0 the window's first position
+    const int w0 = max(kSink, len - kWindow);
+    const int lim = p.lim[b];
+    auto slot_pos = [&](int sl) { return sl < kSink ? sl : w0 + (((sl - kSink) - (w0 - kSink)) % kWindow + kWindow) % kWindow; };
     // query fragments: k-step ks holds channels 16 ks + 2 tig + e (+ 8 for registers 2, 3);
     // row g = bf16 high part of head g + 8 k, row g + 8 = its bf16 low part
     uint32_t qa[MT][8][4];
@@ -176,8 +188,8 @@ __device__ __forceinline__ void prep_body(const DecodeParams& p, const AppendPar
             qa[k][ks][3] = pack_bf16x2(lv[1][0], lv[1][1]);
         }
     }
-    const uint16_t* kb = p.bf16 + (((size_t)b * p.hkv + h) * 2 + 0) * kSlots * kD;
-    const uint16_t* vb = p.bf16 + (((size_t)b * p.hkv + h) * 2 + 1) * kSlots * kD;
+    const uint16_t* kb = p.bf16 + (((size_t)p.row[b] * p.hkv + h) * 2 + 0) * kSlots * kD;
+    const uint16_t* vb = p.bf16 + (((size_t)p.row[b] * p.hkv + h) * 2 + 1) * kSlots * kD;
     float m[MT], lpart[MT];           // running max of head g + 8 k (base 2); this thread's part of the sum
 #pragma unroll
     for (int k = 0; k < MT; ++k) m[k] = -INFINITY, lpart[k] = 0.f;
@@ -205,14 +217,19 @@ __device__ __forceinline__ void prep_body(const DecodeParams& p, const AppendPar
         for (int k = 0; k < MT; ++k) {
             float x[2];
 #pragma unroll
-            for (int e = 0; e < 2; ++e)
-                x[e] = slot_live(s0 + 2 * tig + e, n_sink, n_win) ? acc[k][e] + acc[k][2 + e] : -INFINITY;
+            for (int e = 0; e < 2; ++e) {
+                const int sl = s0 + 2 * tig + e;
+                const bool seen = lim == INT32_MAX || slot_pos(sl) <= lim + (g + 8 * k) / p.g_real;
+                x[e] = slot_live(sl, n_sink, n_win) && seen ? acc[k][e] + acc[k][2 + e] : -INFINITY;
+            }
             float cm = fmaxf(x[0], x[1]);
             cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, 1));
             cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, 2));
-            const float mn = fmaxf(m[k], cm);            // finite: the tile holds a live slot
-            const float f = m[k] == -INFINITY ? 0.f : exp2_approx(m[k] - mn);
-            const float p0 = exp2_approx(x[0] - mn), p1 = exp2_approx(x[1] - mn);
+            const float mn = fmaxf(m[k], cm);
+            // mn is -inf only while a row (under the causal view of chunked prefill) has seen no slot
+            const bool none = mn == -INFINITY;
+            const float f = none ? 1.f : (m[k] == -INFINITY ? 0.f : exp2_approx(m[k] - mn));
+            const float p0 = none ? 0.f : exp2_approx(x[0] - mn), p1 = none ? 0.f : exp2_approx(x[1] - mn);
             lpart[k] = fmaf(lpart[k], f, p0 + p1);
             m[k] = mn;
             ps[warp][2 * tig][g + 8 * k] = p0;
