@@ -58,6 +58,7 @@ def parse():
                     help="requests per GPU (0 = the workload's batch); smaller values are for profiling")
     ap.add_argument("--path", default="mma", choices=["mma", "simt"],
                     help="decode kernel: warp-level MMA (default) or the SIMT baseline")
+    ap.add_argument("--no-prefill", action="store_true", help="skip the chunked-prefill attention timing")
     ap.add_argument("--unfused", action="store_true",
                     help="run each step as kv_quant_append + oscar_decode_attention instead of oscar_decode_step")
     return ap.parse_args()
@@ -329,7 +330,7 @@ def run_ours(args, cfg, rank, world, dist):
     del ws, qcal
 
     # ---- cache with scrambled physical pages
-    per_seq = max(1, (max(lens0) + total_steps - 320 + 63) // 64 + 1)
+    per_seq = max(1, (max(lens0) + total_steps - 320 + 63) // 64 + 1) + 5   # + room for the 256-token prefill chunk
     total_pages = per_seq * B
     order = synth.page_order(seed, total_pages, cfg.table)
     cache = K.Cache(B, hq, hkv, total_pages, per_seq, page_order=order)
@@ -435,6 +436,31 @@ def run_ours(args, cfg, rank, world, dist):
     achieved = k_bytes / k_t / 1e9
     peak, peak_kind = peaks()
 
+    # ---- chunked prefill: every request appends a 256-token chunk and its queries attend causally
+    # (outside the timed decode steps; the cache grows by the chunk)
+    prefill = None
+    if args.path == "mma" and not args.no_prefill:
+        nq = [256] * B
+        lens_p = [cache.length(b) for b in range(B)]
+        if all(lens_p[b] + 256 <= (per_seq - 1) * 64 + 320 for b in range(B)):
+            kp, vp = synth.kv_block(seed + 1, nq, lens_p, hkv, device=dev)
+            qp = torch.randn(sum(nq), hq, 128, device=dev, generator=torch.Generator(device=dev).manual_seed(seed))
+            outp = torch.empty_like(qp)
+            wsp = torch.empty(K.oscar_prefill_workspace_bytes(cache.handle), dtype=torch.uint8, device=dev)
+            cache.append(kp, vp, nq, rk)
+            K.oscar_prefill_attention(cache.handle, qp, K.DTYPE_F32, nq, rk, outp, K.DTYPE_F32, wsp)   # warm
+            torch.cuda.synchronize()
+            p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            p0.record(stream)
+            K.oscar_prefill_attention(cache.handle, qp, K.DTYPE_F32, nq, rk, outp, K.DTYPE_F32, wsp)
+            p1.record(stream)
+            p1.synchronize()
+            pms = p0.elapsed_time(p1)
+            prefill = {"what": "oscar_prefill_attention: 256 new tokens per request attending causally over the "
+                               "mixed cache (INT2 history + BF16 sink / window)", "chunk": 256,
+                       "ms": pms, "query_tokens_per_s": sum(nq) / (pms * 1e-3)}
+            del kp, vp, qp, outp, wsp
+
     # ---- end to end: pinned host inputs in, output out, synchronised every step
     e2e = None
     if not args.no_e2e:
@@ -518,6 +544,7 @@ def run_ours(args, cfg, rank, world, dist):
         "append": {"prefill_tokens_per_s": tok_append / t_append, "prefill_tokens": tok_append,
                    "step_ms_outside_int2_kernel": (per_step - k_t) * 1e3},
         "calibration": calib,
+        "prefill_attention": prefill,
         "clocks": clk,
         "gpu_launches": launches,
         "e2e": e2e,
