@@ -35,7 +35,11 @@
 //            one AND per register from a 16-byte load in fragment order (v_code_byte), with
 //            channel tile cm carrying 4^(cm mod 4) * 2^-24 (removed when the partial is
 //            written); B = P' = p * s_V (fp16, columns = 8 heads) straight from the score
-//            accumulators' register layout; the m_V term sum_t p m_V runs on the CUDA cores.
+//            accumulators' register layout.  Centred values: one more MMA per k-step sums the
+//            same fp16 P' (A = a selector of ones), and after each page the output takes
+//            -1.5 times that sum, so it accumulates P' (code - 1.5), a zero-mean factor that keeps
+//            the rounding of P' from adding up over long nearly flat attention; the minimum term
+//            sum_t p (m_V + 1.5 s_V) runs on the CUDA cores.
 // Tokens are in natural order everywhere: n-tile nt of a chunk holds tokens 8 nt .. 8 nt + 7,
 // and PV k-step kk takes n-tiles 2 kk (k 0..7) and 2 kk + 1 (k 8..15).  At the end of each
 // (request, KV head) run the warp writes (reference max, sum, unnormalised output) to the
