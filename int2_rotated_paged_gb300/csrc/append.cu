@@ -252,14 +252,11 @@ __global__ void __launch_bounds__(kQPThreads) quant_pages(const __grid_constant_
             // code of channel 8 cb + jj at bits 2 rpos of byte jj & 3 of word jj >> 2; after the OR
             // over the four code positions every byte is complete
             uint32_t w[2] = {0u, 0u};
-            uint16_t s16 = 0, m16 = 0;
+            const QuantGroup qg = quant_group(gs, p.clip_k);
+            const uint16_t s16 = qg.s16, m16 = qg.m16;
 #pragma unroll
-            for (int jj = 0; jj < 8; ++jj) {
-                const Quant q = quantise(acc[i][jj], gs, p.clip_k);
-                w[jj >> 2] |= (uint32_t)q.code << (8 * (jj & 3) + 2 * rpos);
-                s16 = q.s16;
-                m16 = q.m16;
-            }
+            for (int jj = 0; jj < 8; ++jj)
+                w[jj >> 2] |= (uint32_t)quant_code(acc[i][jj], qg) << (8 * (jj & 3) + 2 * rpos);
             w[0] = or_over_r(w[0]);
             w[1] = or_over_r(w[1]);
             // the row's word at 8 x + 4 u holds the bytes (e, y) = (0, 0), (0, 1), (1, 0), (1, 1) of
@@ -295,14 +292,11 @@ __global__ void __launch_bounds__(kQPThreads) quant_pages(const __grid_constant_
             for (int jj = 1; jj < 8; ++jj) mn = fminf(mn, vx[jj]), mx = fmaxf(mx, vx[jj]);
             const GroupStat gs = group_minmax_lanes(mn, mx, p.fmt.gv);
             uint32_t w[2] = {0u, 0u};
-            uint16_t s16 = 0, m16 = 0;
+            const QuantGroup qg = quant_group(gs, p.clip_v);
+            const uint16_t s16 = qg.s16, m16 = qg.m16;
 #pragma unroll
-            for (int jj = 0; jj < 8; ++jj) {
-                const Quant q = quantise(vx[jj], gs, p.clip_v);
-                w[jj >> 2] |= (uint32_t)q.code << (8 * (jj & 3) + 2 * rpos);
-                s16 = q.s16;
-                m16 = q.m16;
-            }
+            for (int jj = 0; jj < 8; ++jj)
+                w[jj >> 2] |= (uint32_t)quant_code(vx[jj], qg) << (8 * (jj & 3) + 2 * rpos);
             w[0] = or_over_r(w[0]);
             w[1] = or_over_r(w[1]);
             // channel 8 cb + jj = 64 u + 16 rpos + 8 y + jj: the byte of (slot s, channel 64 u + 8 y + jj)

@@ -4,8 +4,9 @@
 // The arithmetic is the write path's bit-exact contract (axbrief.com OSCAR page, section
 // "attention-statistics rotation + Triton kernels": per-token asymmetric INT2 in 64-channel groups
 // (128-channel groups as a per-cache option, the variants behind the page's 2.28 / 2.38 bits),
-// c_K = 0.96, c_V = 0.92): clip products, the range subtraction and both divisions are single IEEE
-// fp32 operations (explicit _rn intrinsics), fp16 conversions round to nearest even, codes use rint.
+// c_K = 0.96, c_V = 0.92): clip products, the range subtraction and the division by 3 are single
+// IEEE fp32 operations (explicit _rn intrinsics), fp16 conversions round to nearest even, and each
+// code is the one rint of the IEEE quotient (x - m) / s gives, decided by exact compares (quant_code).
 #pragma once
 
 #include <cuda_fp16.h>
@@ -40,22 +41,50 @@ struct Quant {
     uint16_t s16, m16;
 };
 
-__device__ __forceinline__ Quant quantise(float y, GroupStat g, float clip) {
-    const float lo = __fmul_rn(clip, g.mn);
-    const float hi = __fmul_rn(clip, g.mx);
-    const float s_exact = __fdiv_rn(__fsub_rn(hi, lo), 3.0f);
-    Quant q;
+// What one group's codes depend on: the clip range, the fp16 minimum m and the three code
+// thresholds of the fp16 scale s.
+struct QuantGroup {
+    float lo, hi, m;
+    float t0, t1, t2;
+    uint16_t s16, m16;
+};
+
+// The code of a value is clamp(rint(fl((xc - m) / s)), 0, 3) with one IEEE division and
+// round-half-even.  Because s is an fp16 value (at most 11 significant bits), 0.5 s, 1.5 s and 2.5 s
+// are exact fp32 numbers, and the halfway points of the division (0.5 + 2^-25, 1.5 - 2^-24 and
+// 2.5 + 2^-23 times s) each fall strictly inside one fp32 spacing of them.  So, for d = fl(xc - m),
+//   rint(fl(d / s)) >= 1  iff  d >  0.5 s     (rint(0.5) = 0)
+//   rint(fl(d / s)) >= 2  iff  d >= 1.5 s     (rint(1.5) = 2)
+//   rint(fl(d / s)) >= 3  iff  d >  2.5 s     (rint(2.5) = 2)
+// and the code is the number of thresholds d passes: the same code, decided by three compares
+// instead of a division per value.  s = 0 gives code 0 (all thresholds +inf).
+__device__ __forceinline__ QuantGroup quant_group(GroupStat g, float clip) {
+    QuantGroup q;
+    q.lo = __fmul_rn(clip, g.mn);
+    q.hi = __fmul_rn(clip, g.mx);
+    const float s_exact = __fdiv_rn(__fsub_rn(q.hi, q.lo), 3.0f);
     q.s16 = __half_as_ushort(__float2half_rn(s_exact));
-    q.m16 = __half_as_ushort(__float2half_rn(lo));
+    q.m16 = __half_as_ushort(__float2half_rn(q.lo));
     const float s = __half2float(__ushort_as_half(q.s16));
-    const float m = __half2float(__ushort_as_half(q.m16));
-    const float xc = fminf(fmaxf(y, lo), hi);
-    int code = 0;
-    if (s != 0.0f) {
-        const float t = rintf(__fdiv_rn(__fsub_rn(xc, m), s));
-        code = t < 0.0f ? 0 : (t > 3.0f ? 3 : (int)t);
-    }
-    q.code = code;
+    q.m = __half2float(__ushort_as_half(q.m16));
+    const bool zero = s == 0.0f;
+    q.t0 = zero ? INFINITY : __fmul_rn(0.5f, s);
+    q.t1 = zero ? INFINITY : __fmul_rn(1.5f, s);
+    q.t2 = zero ? INFINITY : __fmul_rn(2.5f, s);
+    return q;
+}
+
+__device__ __forceinline__ int quant_code(float y, const QuantGroup& q) {
+    const float d = __fsub_rn(fminf(fmaxf(y, q.lo), q.hi), q.m);
+    return (int)(d > q.t0) + (int)(d >= q.t1) + (int)(d > q.t2);
+}
+
+__device__ __forceinline__ Quant quantise(float y, GroupStat g, float clip) {
+    const QuantGroup qg = quant_group(g, clip);
+    Quant q;
+    q.code = quant_code(y, qg);
+    q.s16 = qg.s16;
+    q.m16 = qg.m16;
     return q;
 }
 
