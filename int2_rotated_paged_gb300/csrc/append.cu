@@ -317,25 +317,32 @@ __global__ void __launch_bounds__(kQPThreads) quant_pages(const __grid_constant_
     }
 }
 
-// New tokens that stay in BF16 (sink, or the final window) -> their slots.
-__global__ void __launch_bounds__(128) insert_bf16(const __grid_constant__ AppendParams p) {
+// New tokens that stay in BF16 (sink, or the final window) -> their slots.  One CTA per (request, KV
+// head, K or V); the rows are copied as 16-byte pieces, all independent, so a CTA keeps many loads
+// in flight instead of one row at a time.
+constexpr int kInsThreads = 256;
+__global__ void __launch_bounds__(kInsThreads) insert_bf16(const __grid_constant__ AppendParams p) {
     const int b = blockIdx.x;
     const int h = blockIdx.y;
+    const int kv = blockIdx.z;
     const AppendReq& r = p.req[b];
     const int l1 = r.len0 + r.n_new;
     const int wstart = max(kSink, l1 - kWindow);
-    for (int kv = 0; kv < 2; ++kv) {
-        const uint16_t* src_t = kv == 0 ? p.k : p.v;
-        uint16_t* dst_base = p.bf16 + ((((size_t)b * p.hkv + h) * 2 + kv) * kSlots) * kD;
-        // sink positions [len0, min(l1, sink)), then the final window [max(len0, wstart), l1)
-        const int ranges[2][2] = {{r.len0, min(l1, kSink)}, {max(r.len0, wstart), l1}};
-        for (int rg = 0; rg < 2; ++rg)
-            for (int pos = ranges[rg][0]; pos < ranges[rg][1]; ++pos) {
-                const uint16_t* src = src_t + ((size_t)(r.tok_off + (pos - r.len0)) * p.hkv + h) * kD;
-                dst_base[(size_t)bf16_slot(pos) * kD + threadIdx.x] = src[threadIdx.x];
-            }
+    // sink positions [len0, min(l1, sink)), then the final window [max(len0, wstart), l1): disjoint
+    const int a0 = r.len0, n0 = max(0, min(l1, kSink) - r.len0);
+    const int a1 = max(r.len0, wstart), n1 = max(0, l1 - a1);
+    const uint4* src = reinterpret_cast<const uint4*>(kv == 0 ? p.k : p.v);
+    uint4* dst = reinterpret_cast<uint4*>(p.bf16 + (((size_t)b * p.hkv + h) * 2 + kv) * kSlots * kD);
+    constexpr int kPieces = kD * 2 / 16;   // 16-byte pieces per 128-channel bf16 row
+    const int total = (n0 + n1) * kPieces;
+#pragma unroll 4
+    for (int idx = threadIdx.x; idx < total; idx += kInsThreads) {
+        const int row = idx / kPieces, piece = idx - row * kPieces;
+        const int pos = row < n0 ? a0 + row : a1 + (row - n0);
+        const uint4 w = __ldg(src + ((size_t)(r.tok_off + (pos - r.len0)) * p.hkv + h) * kPieces + piece);
+        dst[(size_t)bf16_slot(pos) * kPieces + piece] = w;
     }
-    if (h == 0 && threadIdx.x == 0) p.seq_lens[b] = l1;
+    if (h == 0 && kv == 0 && threadIdx.x == 0) p.seq_lens[b] = l1;
 }
 
 }  // namespace
@@ -368,7 +375,7 @@ cudaError_t launch_append(const AppendParams& p, cudaStream_t s) {
             quant_pages<<<dim3(p.n_jobs, p.hkv), kQPThreads, smem_tiled, s>>>(p);
         ++n;
     }
-    insert_bf16<<<dim3(p.batch, p.hkv), 128, 0, s>>>(p);
+    insert_bf16<<<dim3(p.batch, p.hkv, 2), kInsThreads, 0, s>>>(p);
     ++n;
     count_launches(n);
     return cudaGetLastError();
