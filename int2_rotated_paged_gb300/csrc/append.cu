@@ -18,9 +18,10 @@
 //
 // Bit-exact contract (shared with nothing but the written specification): the key
 // rotation is the serial chain acc = fma(x_j, R[j][c], acc), j = 0..127, acc0 = +0;
-// clip products, the range subtraction and both divisions are single IEEE fp32
+// clip products, the range subtraction and the divisions are single IEEE fp32
 // operations (explicit _rn intrinsics, so the compiler cannot contract them);
-// fp16 conversions round to nearest even; codes use rint (ties to even).
+// fp16 conversions round to nearest even; codes are rint (ties to even) of the IEEE
+// quotient, decided by the equivalent exact compares of token_quant.h.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -134,12 +135,12 @@ constexpr int kQPThreads = 256;   // threads of quant_pages
 __device__ __forceinline__ int rk_swz(int f) { return f ^ ((f >> 3) & 1); }
 constexpr int kSPT = kPage * 16 / kQPThreads;   // page slots per thread (16 lanes per slot)
 
-// One CTA per (touched INT2 page, KV head), 128 threads.  Thread t owns the 8 page slots
-// 8 (t >> 4) .. + 7 and the 8 channels 8 cb .. 8 cb + 7 (cb = t & 15), so a token's 128 channels sit
+// One CTA per (touched INT2 page, KV head), 256 threads.  Thread t owns the 4 page slots
+// 4 (t >> 4) .. + 3 and the 8 channels 8 cb .. 8 cb + 7 (cb = t & 15), so a token's 128 channels sit
 // in 16 lanes of one warp and a 64-channel group in 8 of them: group min / max and the packing of
 // four codes per byte are warp shuffles, with no block-wide barrier per token.
 // Keys: the 64 x 128 tile times R_K with each output the serial fmaf chain over ascending j
-// (the bit-exact contract), 8 tokens x 8 channels of independent chains per thread.
+// (the bit-exact contract), 4 tokens x 8 channels of independent chains per thread.
 __global__ void __launch_bounds__(kQPThreads) quant_pages(const __grid_constant__ AppendParams p) {
     extern __shared__ __align__(16) float smem[];
     float* R = smem;                   // [128][128]
