@@ -315,43 +315,39 @@ __global__ void __launch_bounds__(32 * warps_for(G), 1) decode_mma(const __grid_
         // Slots past the request's end are staged as 0 (their bytes may be anything); a full page
         // takes a copy of the loop without that test
         auto stage = [&](const bool full) {
-        float vmax = 0.f;   // largest value scale of this thread's two tokens
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-            const int t = lane + 32 * hh;
-            const bool live = full || t < n_live;
-            // one (s, m) pair per 64-channel group, or one pair for both halves of a 128-channel group
-            uint2 ksm, vsm;
-            if (FMT64 || f.gk == 64) {
-                ksm = *reinterpret_cast<const uint2*>(pg + kKSm + t * 8);
-            } else {
-                ksm.x = ksm.y = *reinterpret_cast<const uint32_t*>(pg + kKSm + t * 4);
-            }
-            if (FMT64 || f.gv == 64) {
-                vsm = *reinterpret_cast<const uint2*>(pg + f.v_sm + t * 8);
-            } else {
-                vsm.x = vsm.y = *reinterpret_cast<const uint32_t*>(pg + f.v_sm + t * 4);
-            }
-            // values: the scale s, and the centred minimum m + 1.5 s (the output MMAs take code - 1.5)
-            const float sv0 = __half2float(__ushort_as_half(vsm.x & 0xffff));
-            const float sv1 = __half2float(__ushort_as_half(vsm.y & 0xffff));
-            const float val[8] = {
-                live ? kscale * __half2float(__ushort_as_half(ksm.x & 0xffff)) : 0.f,
-                live ? __half2float(__ushort_as_half(ksm.x >> 16)) : 0.f,
-                live ? kscale * __half2float(__ushort_as_half(ksm.y & 0xffff)) : 0.f,
-                live ? __half2float(__ushort_as_half(ksm.y >> 16)) : 0.f,
-                live ? sv0 : 0.f,
-                live ? fmaf(1.5f, sv0, __half2float(__ushort_as_half(vsm.x >> 16))) : 0.f,
-                live ? sv1 : 0.f,
-                live ? fmaf(1.5f, sv1, __half2float(__ushort_as_half(vsm.y >> 16))) : 0.f};
-            vmax = fmaxf(vmax, fmaxf(val[4], val[6]));
-            float* row = reinterpret_cast<float*>(&sm->tsc[warp][0][t >> 1]);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                row[j * 128 + (t & 1)] = val[2 * j];
-                row[j * 128 + 2 + (t & 1)] = val[2 * j + 1];
-            }
+        // thread = token pair (2 lane, 2 lane + 1): its scales and minima are one 16-byte load per
+        // tensor (8 bytes for 128-channel groups), its four table entries one 16-byte store each
+        const int t0 = 2 * lane;
+        const bool live0 = full || t0 < n_live, live1 = full || t0 + 1 < n_live;
+        uint4 ksm, vsm;   // (s, m) of group 0 / 1 for token t0 (x, y) and t0 + 1 (z, w)
+        if (FMT64 || f.gk == 64) {
+            ksm = *reinterpret_cast<const uint4*>(pg + kKSm + t0 * 8);
+        } else {   // one (s, m) pair per token for both halves of a 128-channel group
+            const uint2 k2 = *reinterpret_cast<const uint2*>(pg + kKSm + t0 * 4);
+            ksm = make_uint4(k2.x, k2.x, k2.y, k2.y);
         }
+        if (FMT64 || f.gv == 64) {
+            vsm = *reinterpret_cast<const uint4*>(pg + f.v_sm + t0 * 8);
+        } else {
+            const uint2 v2 = *reinterpret_cast<const uint2*>(pg + f.v_sm + t0 * 4);
+            vsm = make_uint4(v2.x, v2.x, v2.y, v2.y);
+        }
+        auto lo = [](uint32_t w) { return __half2float(__ushort_as_half((unsigned short)(w & 0xffff))); };
+        auto hi = [](uint32_t w) { return __half2float(__ushort_as_half((unsigned short)(w >> 16))); };
+        // keys: (2^18 / qscale) s and m; values: s and the centred minimum m + 1.5 s (the output MMAs
+        // take code - 1.5).  Slots past the request's end are staged as 0
+        const float sv00 = live0 ? lo(vsm.x) : 0.f, sv01 = live0 ? lo(vsm.y) : 0.f;
+        const float sv10 = live1 ? lo(vsm.z) : 0.f, sv11 = live1 ? lo(vsm.w) : 0.f;
+        float4* row = &sm->tsc[warp][0][lane];
+        row[0] = make_float4(live0 ? kscale * lo(ksm.x) : 0.f, live1 ? kscale * lo(ksm.z) : 0.f,
+                             live0 ? hi(ksm.x) : 0.f, live1 ? hi(ksm.z) : 0.f);
+        row[32] = make_float4(live0 ? kscale * lo(ksm.y) : 0.f, live1 ? kscale * lo(ksm.w) : 0.f,
+                              live0 ? hi(ksm.y) : 0.f, live1 ? hi(ksm.w) : 0.f);
+        row[64] = make_float4(sv00, sv10, live0 ? fmaf(1.5f, sv00, hi(vsm.x)) : 0.f,
+                              live1 ? fmaf(1.5f, sv10, hi(vsm.z)) : 0.f);
+        row[96] = make_float4(sv01, sv11, live0 ? fmaf(1.5f, sv01, hi(vsm.y)) : 0.f,
+                              live1 ? fmaf(1.5f, sv11, hi(vsm.w)) : 0.f);
+        const float vmax = fmaxf(fmaxf(sv00, sv01), fmaxf(sv10, sv11));   // largest value scale of the pair
         // value scales against the slack: 2^tau * s_V must stay below 2^15, i.e. s_V < vlim =
         // 2^(15 - tau) (thread-local test; the warp-wide maximum and the new tau only on the rare
         // path: the first page with non-zero value scales of a segment, or a page whose scales are
