@@ -112,7 +112,11 @@ size_t oscar_page_head_bytes(const oscar_cache_desc *d);
  *               [b][h][K|V][slot][128]; slot = pos for pos < sink, else
  *               sink + (pos - sink) % window.
  *   page_table: batch * max_pages_per_seq int32 ([b][logical page] -> physical page).
- *   seq_lens:   batch int32 (tokens held per request). */
+ *   seq_lens:   per-request metadata: batch int32 (tokens held per request), then, from byte
+ *               16 * ceil(batch / 4), uint32 [batch][num_kv_heads]: the fp16 bits of the largest
+ *               value scale the write path has quantised for that (request, KV head), zeroed
+ *               when the request is released.  The read path derives its fp16 range limit for
+ *               p * s_V from it.  Size: the sum of both parts rounded up to 16 bytes. */
 size_t oscar_pool_bytes(const oscar_cache_desc *d);
 size_t oscar_bf16_bytes(const oscar_cache_desc *d);
 size_t oscar_page_table_bytes(const oscar_cache_desc *d);

@@ -16,10 +16,12 @@ struct oscar_cache {
     uint16_t* bf16;
     int32_t* pt;
     int32_t* lens_dev;
+    uint32_t* vmax_dev;                       // [batch][hkv] after the lengths (vmax_offset)
     std::vector<int64_t> len;                 // tokens held per request
     std::vector<std::vector<int32_t>> rows;   // physical pages held per request
     std::vector<int32_t> free_list;           // popped from the back
     std::vector<int32_t> dirty_lo;            // first row entry not yet on the device
+    std::vector<char> vmax_stale;             // the request's value-scale maxima need zeroing
     bool clear_device;                        // the device table / lengths need zeroing
     bool lens_dirty;
     int32_t g;
@@ -97,6 +99,13 @@ int sync(oscar_cache* c, cudaStream_t s) {
         if (e != cudaSuccess) return cuda_fail(e);
         c->clear_device = false;
         c->lens_dirty = true;
+        std::fill(c->vmax_stale.begin(), c->vmax_stale.end(), 0);
+    }
+    for (int32_t b = 0; b < c->d.batch; ++b) {
+        if (!c->vmax_stale[b]) continue;
+        e = cudaMemsetAsync(c->vmax_dev + (size_t)b * c->d.num_kv_heads, 0, sizeof(uint32_t) * c->d.num_kv_heads, s);
+        if (e != cudaSuccess) return cuda_fail(e);
+        c->vmax_stale[b] = 0;
     }
     for (int32_t b = 0; b < c->d.batch; ++b) {
         const int32_t lo = c->dirty_lo[b];
@@ -161,7 +170,7 @@ size_t oscar_page_table_bytes(const oscar_cache_desc* d) {
 }
 size_t oscar_seq_lens_bytes(const oscar_cache_desc* d) {
     if (!desc_ok(d)) return 0;
-    return (size_t)d->batch * sizeof(int32_t);
+    return (vmax_offset(d->batch) + (size_t)d->batch * d->num_kv_heads * sizeof(uint32_t) + 15) / 16 * 16;
 }
 
 int oscar_cache_create(const oscar_cache_desc* d, void* pool, void* bf16, int32_t* page_table,
@@ -179,6 +188,8 @@ int oscar_cache_create(const oscar_cache_desc* d, void* pool, void* bf16, int32_
     c->bf16 = (uint16_t*)bf16;
     c->pt = page_table;
     c->lens_dev = seq_lens;
+    c->vmax_dev = (uint32_t*)((uint8_t*)seq_lens + vmax_offset(d->batch));
+    c->vmax_stale.assign(d->batch, 0);
     c->len.assign(d->batch, 0);
     c->rows.assign(d->batch, {});
     c->g = d->num_q_heads / d->num_kv_heads;
@@ -243,6 +254,7 @@ int kv_page_table_release(oscar_cache* c, int32_t b) {
     c->dirty_lo[b] = INT32_MAX;
     c->len[b] = 0;
     c->lens_dirty = true;
+    c->vmax_stale[b] = 1;
     return OSCAR_OK;
 }
 
@@ -308,6 +320,7 @@ static int prepare_append(oscar_cache* c, const void* k, const void* v, const in
     p.bf16 = c->bf16;
     p.page_table = c->pt;
     p.seq_lens = c->lens_dev;
+    p.vmax = c->vmax_dev;
     p.max_pps = d.max_pages_per_seq;
     int64_t off = 0;
     int32_t jobs = 0;
@@ -493,6 +506,7 @@ static int prepare_decode(oscar_cache* c, const void* q, int32_t q_dtype, const 
     p.part_mma = (float*)(ws + w.mma);
     p.part_bf16 = (float*)(ws + w.bf16);
     p.err = (int32_t*)(ws + w.err);
+    p.vmax = c->vmax_dev;
     p.path = g_decode_path;
     p.wait_iters = g_wait_iters;
     p.wait_probe = g_wait_probe;
@@ -677,6 +691,7 @@ int oscar_prefill_attention(oscar_cache* c, const void* q, int32_t q_dtype, cons
         p.part_mma = (float*)(ws + w.mma);
         p.part_bf16 = (float*)(ws + w.bf16);
         p.err = (int32_t*)(ws + w.err);
+        p.vmax = c->vmax_dev;
         p.path = OSCAR_PATH_WARP_MMA;
         p.wait_iters = g_wait_iters;
         p.wait_probe = g_wait_probe;
@@ -888,6 +903,7 @@ int noalloc_decode_params(oscar_cache* c, const void* q, int32_t q_dtype, const 
     p.bf16 = c->bf16;
     p.page_table = c->pt;
     p.max_pps = c->d.max_pages_per_seq;
+    p.vmax = c->vmax_dev;
     p.path = OSCAR_PATH_WARP_MMA;
     p.wait_iters = g_wait_iters;
     p.wait_probe = g_wait_probe;

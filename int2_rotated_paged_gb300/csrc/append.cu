@@ -97,7 +97,8 @@ __global__ void __launch_bounds__(128) quant_few(const __grid_constant__ AppendP
         for (int t = 0; t < n; ++t) {
             // K (rotated) and V (unrotated): per-token asymmetric INT2 in two 64-channel groups
             const float yv = bf16_bits_to_f32(token_src(p, b, h, 1, p0 + t)[c]);
-            store_token(blk, p.fmt, (p0 + t - kSink) % kPage, acc[t], yv, p.clip_k, p.clip_v, red, part);
+            store_token(blk, p.fmt, (p0 + t - kSink) % kPage, acc[t], yv, p.clip_k, p.clip_v, red, part,
+                        p.vmax + (size_t)b * p.hkv + h);
         }
     }
 }
@@ -239,6 +240,7 @@ __global__ void __launch_bounds__(kQPThreads) quant_pages(const __grid_constant_
     // ---- per token: clip, quantise, pack.  Channel c = 8 cb + jj: group u = cb >> 3, code
     // position r = (cb >> 1) & 3, y = cb & 1 in both page orders.
     const int u = cb >> 3, rpos = (cb >> 1) & 3, y = cb & 1;
+    uint32_t vbig = 0;   // largest fp16 value scale (bits) of this thread's live tokens
 #pragma unroll
     for (int i = 0; i < kSPT; ++i) {
         const int s = kSPT * tb + i;
@@ -309,8 +311,11 @@ __global__ void __launch_bounds__(kQPThreads) quant_pages(const __grid_constant_
             if (live && (8 * cb) % p.fmt.gv == 0)
                 *reinterpret_cast<uint32_t*>(ob + p.fmt.v_sm + s * p.fmt.v_stride + (8 * cb / p.fmt.gv) * 4) =
                     (uint32_t)s16 | ((uint32_t)m16 << 16);
+            if (live) vbig = max(vbig, (uint32_t)s16);
         }
     }
+    vbig = __reduce_max_sync(0xffffffffu, vbig);
+    if ((t & 31) == 0 && vbig) atomicMax(p.vmax + (size_t)b * p.hkv + h, vbig);
     if (whole) {
         __syncthreads();
         for (int i = t; i < p.fmt.bytes / 16; i += kQPThreads)

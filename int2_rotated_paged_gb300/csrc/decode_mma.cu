@@ -26,9 +26,10 @@
 //            logit = 2^18 s_g S_g / qscale + m_g sum_{c in g} q~_c (log2 units);
 //   softmax  online, per head, with a lazily raised reference max (output rescaled only when a
 //            logit passes the reference by 2^tau, tested per thread first, so the row-group max
-//            reduction runs only on that rare path; tau is chosen per segment from the largest
-//            value scale so that P' stays inside fp16); logits are formed relative to the reference
-//            and all the per-token arithmetic runs on packed fp32 pairs (f32x2 FMA / MUL / ADD:
+//            reduction runs only on that rare path; tau is set per (request, KV head) from the largest
+//            value scale the write path recorded, so that P' stays inside fp16); logits are formed
+//            relative to the reference and all the per-token arithmetic runs on packed fp32 pairs
+//            (f32x2 FMA / MUL / ADD:
 //            the two tokens 2 tig, 2 tig + 1 of a score column pair), which halves the FP32
 //            instructions and, unlike scalar FFMA, overlaps the MMAs almost fully;
 //   output   O^T += V^T P'^T on the same MMA: A = the value codes (rows = 16 channels), again
@@ -68,7 +69,7 @@ __host__ __device__ constexpr int stages_for(int G) { return G <= 8 ? 2 : 3; }
 // that the output's cancellation between sum P' code and sum p m_V magnifies; at 2^(k + 1/2) the
 // rounding errors are spread evenly and average out.
 constexpr float kTauSlack = 7.5f;
-constexpr float kTauMax = 40.0f;    // tau of a segment before any non-zero value scale is seen
+constexpr float kTauMax = 40.0f;    // tau of a (request, KV head) without a non-zero value scale
 constexpr float kQScaleM = 1.4426950408889634f * 0.08838834764831845f;   // log2(e) / sqrt(128)
 constexpr float kTwo18 = 262144.0f;
 
@@ -208,11 +209,11 @@ __global__ void __launch_bounds__(32 * warps_for(G), 1) decode_mma(const __grid_
     float2 lsum[MT], mv[MT][2];     // per token parity e, summed when the partial is written
     bool fresh = true;
     float qscale = 1.f, kscale = kTwo18;   // power-of-two query scale of the segment and 2^18 / it
-    // Reference-max slack tau (log2 units): probabilities stay at most 2^tau, and tau is lowered so
-    // that 2^tau times the largest value scale seen in the segment stays below 2^15, so that
+    // Reference-max slack tau (log2 units): probabilities stay at most 2^tau, and tau is set so that
+    // 2^tau times the largest value scale of the (request, KV head) stays below 2^15, so that
     // P' = p * s_V cannot overflow fp16.  A raise of the reference puts the largest logit at
     // tau - 7.5, so the dominant probabilities sit about 2^7.5 below the limit.  tau lives in shared
-    // memory (sm->tau[warp]): it changes rarely and is read once per page and once per chunk.
+    // memory (sm->tau[warp]): it is set once per segment and read once per chunk.
     float o[8][MT][4];              // output^T accumulators: channel tile cm, head tile nh
     // sum of P' over the current page: rows g (value group 0) and g + 8 (group 1) of one MMA
     // accumulator, heads 2 tig, 2 tig + 1
@@ -301,7 +302,17 @@ __global__ void __launch_bounds__(32 * warps_for(G), 1) decode_mma(const __grid_
             for (int k = 0; k < MT; ++k) psum[k][0] = psum[k][1] = psum[k][2] = psum[k][3] = 0.f;
             seg_start = false;
             fresh = true;
-            if (lane == 0) sm->tau[warp] = kTauMax;
+            if (lane == 0) {
+                // tau from the largest value scale the write path has quantised for this (request,
+                // KV head): 2^tau * s_V in [2^14, 2^15) for the largest s_V, so P' = p * s_V < 2^15
+                const uint32_t w16 = p.vmax[(size_t)p.row[it.b] * p.hkv + it.h] & 0xffffu;
+                float tau = kTauMax;
+                if (w16) {
+                    const float w = __half2float(__ushort_as_half((unsigned short)w16));
+                    tau = fminf(kTauMax, (float)(14 - ((int)((__float_as_uint(w) >> 23) & 0xff) - 127)));
+                }
+                sm->tau[warp] = tau;
+            }
             __syncwarp();
         }
         const bool got = wait_full(smem_u32(&sm->full[warp][s]), (i / kStagesPerWarp) & 1, p.err, p.wait_iters);
@@ -347,22 +358,6 @@ __global__ void __launch_bounds__(32 * warps_for(G), 1) decode_mma(const __grid_
                               live1 ? fmaf(1.5f, sv10, hi(vsm.z)) : 0.f);
         row[96] = make_float4(sv01, sv11, live0 ? fmaf(1.5f, sv01, hi(vsm.y)) : 0.f,
                               live1 ? fmaf(1.5f, sv11, hi(vsm.w)) : 0.f);
-        const float vmax = fmaxf(fmaxf(sv00, sv01), fmaxf(sv10, sv11));   // largest value scale of the pair
-        // value scales against the slack: 2^tau * s_V must stay below 2^15, i.e. s_V < vlim =
-        // 2^(15 - tau) (thread-local test; the warp-wide maximum and the new tau only on the rare
-        // path: the first page with non-zero value scales of a segment, or a page whose scales are
-        // larger than any before)
-        const float vlim = __uint_as_float((uint32_t)(127 + 15 - (int)sm->tau[warp]) << 23);
-        if (__any_sync(0xffffffffu, vmax >= vlim)) {
-            float w = vmax;
-#pragma unroll
-            for (int o2 = 1; o2 < 32; o2 <<= 1) w = fmaxf(w, __shfl_xor_sync(0xffffffffu, w, o2));
-            // w * 2^tau in [2^14, 2^15): tau = 14 - floor(log2 w) (w > 0 and normal: an fp16 value)
-            const int ew = (int)((__float_as_uint(w) >> 23) & 0xff) - 127;
-            const int tnew = 14 - ew;
-            __syncwarp();
-            if (lane == 0) sm->tau[warp] = (float)tnew;
-        }
         };
         if (n_live == kPage) stage(true);
         else stage(false);

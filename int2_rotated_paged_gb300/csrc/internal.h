@@ -93,6 +93,7 @@ struct AppendParams {
     const int32_t* page_table;
     int32_t* seq_lens;
     int32_t max_pps;
+    uint32_t* vmax;        // [batch][hkv] largest fp16 value scale quantised so far (fp16 bits)
     AppendReq req[kMaxBatch];
 };
 
@@ -115,6 +116,7 @@ struct DecodeParams {
     float* part_mma;       // warp-MMA path: [batch * hkv + n_units][g][2 + 128], slot (b * hkv + h) + unit
     float* part_bf16;      // [batch * hkv][g][2 + 128]: the BF16 sink / window split
     int32_t* err;          // nonzero after a bounded wait gave up
+    const uint32_t* vmax;  // [batch][hkv] largest fp16 value scale in the request's INT2 pages (bits)
     int32_t wait_iters;    // a bounded wait gives up after this many tests of up to 1 ms each
     int32_t wait_probe;    // nonzero: the first kernel also waits on a barrier nothing arrives at
     // warp-MMA path
@@ -133,6 +135,12 @@ struct DecodeParams {
     int32_t nq[kMaxBatch];
     int32_t lim[kMaxBatch];
 };
+
+// The per-request metadata buffer (seq_lens) holds the lengths, int32[batch], then from this byte
+// offset the largest fp16 value scale quantised so far per (request, KV head), uint32[batch][hkv]
+// (fp16 bits; a positive fp16 value orders like its bits).  The read path takes its fp16 range
+// limit for P' = p * s_V from it once per (request, KV head) instead of testing every page.
+__host__ __device__ inline size_t vmax_offset(int batch) { return ((size_t)batch * 4 + 15) / 16 * 16; }
 
 // Split-K partition of one request: INT2 splits of `pps` pages plus one BF16 split.
 __host__ __device__ inline int int2_tokens(int len) {

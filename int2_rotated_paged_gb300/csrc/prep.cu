@@ -152,7 +152,7 @@ __device__ __forceinline__ void prep_body(const DecodeParams& p, const AppendPar
             const int phys = ap->page_table[(size_t)b * ap->max_pps + pg];
             uint8_t* blk = ap->pool + ((size_t)phys * p.hkv + h) * ap->fmt.bytes;
             tq::store_token(blk, ap->fmt, (r.e0 - kSink) % kPage, c < kD ? acck : 0.f, yv, ap->clip_k, ap->clip_v, red,
-                            tpart);
+                            tpart, ap->vmax + (size_t)b * p.hkv + h);
         }
     }
 

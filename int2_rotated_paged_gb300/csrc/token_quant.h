@@ -119,17 +119,20 @@ __device__ __forceinline__ GroupStat group_minmax(float y, float* red, int group
 // Quantise one token (channel c of the key y_k and value y_v in thread c < 128; any further threads
 // of the block take part in the barriers only) and store its codes and scales into slot `slot` of the
 // page-head block `blk` (layout f).  `red` holds 2 floats per warp of the block, `part` 2 x 4 x 16 bytes.
+// The value scales also raise *vmax, the largest fp16 value scale of the (request, KV head).
 __device__ __forceinline__ void store_token(uint8_t* blk, const PageFmt& f, int slot, float yk, float yv, float clip_k,
-                                            float clip_v, float* red, uint8_t (*part)[4][16]) {
+                                            float clip_v, float* red, uint8_t (*part)[4][16], uint32_t* vmax) {
     const int c = threadIdx.x, lane = c & 31;
     const Quant qk = quantise(yk, group_minmax(yk, red, f.gk), clip_k);
     const Quant qv = quantise(yv, group_minmax(yv, red, f.gv), clip_v);
     if (c < kD && (c & (f.gk - 1)) == 0)
         *reinterpret_cast<uint32_t*>(blk + f.k_sm + slot * f.k_stride + (c / f.gk) * 4) =
             (uint32_t)qk.s16 | ((uint32_t)qk.m16 << 16);
-    if (c < kD && (c & (f.gv - 1)) == 0)
+    if (c < kD && (c & (f.gv - 1)) == 0) {
         *reinterpret_cast<uint32_t*>(blk + f.v_sm + slot * f.v_stride + (c / f.gv) * 4) =
             (uint32_t)qv.s16 | ((uint32_t)qv.m16 << 16);
+        if (qv.s16) atomicMax(vmax, (uint32_t)qv.s16);
+    }
     // pack: every code byte holds the codes of four channels c0 + 16 r (r = 0..3) of this token, two
     // from lanes l and l ^ 16 of one warp and two from the next warp
     uint32_t pk = (uint32_t)qk.code << k_code_shift(c & (kD - 1));

@@ -62,7 +62,8 @@ def test_descriptor_defaults_and_sizes(K):
     assert d.group_size_v == 64 and L.oscar_page_head_bytes(ctypes.byref(d)) == 5120
     assert L.oscar_bf16_bytes(ctypes.byref(d)) == 4 * 8 * 2 * 320 * 128 * 2
     assert L.oscar_page_table_bytes(ctypes.byref(d)) == 4 * 8 * 4
-    assert L.oscar_seq_lens_bytes(ctypes.byref(d)) == 16
+    # 4 lengths (16 bytes), then 4 x 8 value-scale maxima
+    assert L.oscar_seq_lens_bytes(ctypes.byref(d)) == 16 + 4 * 8 * 4
 
 
 @pytest.mark.parametrize("field,value", [("head_dim", 64), ("page_size", 32), ("group_size", 32),

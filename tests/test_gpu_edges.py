@@ -263,3 +263,66 @@ def test_value_scale_rising_across_pages():
         return synth.queries(9, s, 1, hq, hkv, device="cuda")
 
     _run(hq, hkv, [L], kfn, vfn, qfn, rk, steps=2)
+
+
+def _recorded_vmax(cache, B, hkv):
+    """The largest-value-scale words the write path keeps after the lengths (fp16 bits)."""
+    off = 4 * ((B + 3) // 4)                                   # int32 index of the first word
+    return cache.seq_lens[off:off + B * hkv].cpu().numpy().view(np.uint32).reshape(B, hkv)
+
+
+def _stored_vmax(cache, b, h, n_int2):
+    """The largest fp16 value scale stored in the request's INT2 pages (bits), read back."""
+    if n_int2 == 0:
+        return 0
+    _, _, _, vs = K.oscar_read_int2(cache.handle, b, h, 64, n_int2)
+    return int(np.asarray(vs, np.uint16)[:, 0::2].max())
+
+
+def test_recorded_value_scale_maxima_follow_appends_steps_and_release():
+    # the read path takes its fp16 range limit for P' = p * s_V from these words, so each must be the
+    # largest value scale of its (request, KV head) INT2 pages, grown by appends and fused decode steps,
+    # and zeroed when the request is released
+    hq, hkv, B = 16, 2, 3
+    seed = 77
+    rk = oracle_rk(seed, hkv, 1024)
+    rk_dev = torch.tensor(rk, device="cuda")
+    cache = K.Cache(B, hq, hkv, 3 * 40, 40)
+    lens = [2500, 900, 330]
+    k, v = synth.kv_block(seed, lens, [0] * B, hkv, device="cuda")
+    v[:lens[0]] *= 100.0                      # request 0's values 100x larger than the others'
+    cache.append(k, v, lens, rk_dev)
+    torch.cuda.synchronize()
+    rec = _recorded_vmax(cache, B, hkv)
+    for b in range(B):
+        for h in range(hkv):
+            assert rec[b, h] == _stored_vmax(cache, b, h, max(0, lens[b] - 320)), (b, h)
+    assert rec[2].max() > 0 and rec[0].min() > rec[1].max()
+    # fused decode steps quantise the token leaving the window: one with 1000x larger values
+    out = torch.empty(B, hq, 128, device="cuda")
+    for s in range(3):
+        k1, v1 = synth.kv_block(seed, [1] * B, [lens[b] + s for b in range(B)], hkv, device="cuda")
+        q = synth.queries(seed, s, B, hq, hkv, device="cuda")
+        if s == 0:
+            v1 *= 1000.0   # enters the window now, leaves it 256 steps later: not quantised yet
+        cache.step(k1, v1, q, rk_dev, out)
+    torch.cuda.synchronize()
+    lens = [L + 3 for L in lens]
+    rec = _recorded_vmax(cache, B, hkv)
+    for b in range(B):
+        for h in range(hkv):
+            assert rec[b, h] == _stored_vmax(cache, b, h, max(0, lens[b] - 320)), (b, h)
+    # release request 1: its words are zeroed at the next sync, the others stay
+    K.kv_page_table_release(cache.handle, 1)
+    K.kv_page_table_sync(cache.handle)
+    torch.cuda.synchronize()
+    rec2 = _recorded_vmax(cache, B, hkv)
+    assert (rec2[1] == 0).all() and (rec2[0] == rec[0]).all() and (rec2[2] == rec[2]).all()
+    # refilled with small values, request 1 records only those
+    k, v = synth.kv_block(seed + 1, [0, 700, 0], [0, 0, 0], hkv, device="cuda")
+    cache.append(k, v * 0.01, [0, 700, 0], rk_dev)
+    torch.cuda.synchronize()
+    rec3 = _recorded_vmax(cache, B, hkv)
+    for h in range(hkv):
+        assert rec3[1, h] == _stored_vmax(cache, 1, h, 700 - 320)
+    assert rec3[1].max() < rec[1].min()
