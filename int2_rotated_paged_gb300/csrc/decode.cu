@@ -312,8 +312,10 @@ __global__ void __launch_bounds__(128) combine(const __grid_constant__ DecodePar
 
 // Warp-MMA path: one CTA per (KV head, request), one warp per query head, lane = channels
 // 2 lane, 2 lane + 1, 64 + 2 lane, 65 + 2 lane.  Merges the BF16 partial with the partials of the
-// warps w0 .. w1 that owned pages of (b, h) (warps whose page range is empty wrote nothing):
-// first the common max, then the sums, so that every load is independent of the merge.
+// warps w0 .. w1 that owned pages of (b, h) (warps whose page range is empty wrote nothing).  Lane i
+// reads the reference max and sum of partial w0 + i (and further ones 32 apart), so the common max
+// and the total sum are warp reductions; the unnormalised outputs are then summed four partials at a
+// time, every load independent of the merge.
 __global__ void __launch_bounds__(32 * kMaxG) combine_mma(const __grid_constant__ DecodeParams p) {
     const int h = blockIdx.x, b = blockIdx.y;
     const int hh = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -333,24 +335,60 @@ __global__ void __launch_bounds__(32 * kMaxG) combine_mma(const __grid_constant_
         auto owns = [&](int w) {
             return ((long long)w * p.total_pages) / p.n_units != ((long long)(w + 1) * p.total_pages) / p.n_units;
         };
+        const int n = w1 - w0 + 1;   // candidate partials (those of warps that own no page are skipped)
+        // common max: the BF16 partial's and every owned INT2 partial's reference max
         float M = pb[0];
-        for (int w = w0; w <= w1; ++w)
-            if (owns(w)) M = fmaxf(M, slot(w)[0]);
+        for (int i = lane; i < n; i += 32)
+            if (owns(w0 + i)) M = fmaxf(M, slot(w0 + i)[0]);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
         float L = 0.f;
         float2 o0 = r0, o1 = r0;
         auto add = [&](const float* ph, float f) {
-            L = fmaf(f, ph[1], L);
             const float2 a = *reinterpret_cast<const float2*>(ph + 2 + 2 * lane);
             const float2 c = *reinterpret_cast<const float2*>(ph + 2 + 64 + 2 * lane);
             o0 = make_float2(fmaf(f, a.x, o0.x), fmaf(f, a.y, o0.y));
             o1 = make_float2(fmaf(f, c.x, o1.x), fmaf(f, c.y, o1.y));
         };
-        if (pb[0] != -INFINITY) add(pb, exp2f(pb[0] - M));
-        for (int w = w0; w <= w1; ++w)
-            if (owns(w)) {
-                const float* ph = slot(w);
-                add(ph, exp2f(ph[0] - M));
+        if (pb[0] != -INFINITY) {
+            const float f = exp2f(pb[0] - M);
+            if (lane == 0) L = f * pb[1];
+            add(pb, f);
+        }
+        for (int i0 = 0; i0 < n; i0 += 32) {
+            // lane i: the weight of partial w0 + i0 + i (0 if it does not exist) and its share of L
+            const int wi = w0 + i0 + lane;
+            float f = 0.f;
+            if (i0 + lane < n && owns(wi)) {
+                const float* ph = slot(wi);
+                f = exp2f(ph[0] - M);
+                L = fmaf(f, ph[1], L);
             }
+            const int m = min(32, n - i0);
+            int k = 0;
+            for (; k + 4 <= m; k += 4) {
+                float fk[4];
+                float2 a[4], c[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    fk[e] = __shfl_sync(0xffffffffu, f, k + e);
+                    const float* ph = slot(w0 + i0 + k + e);
+                    a[e] = fk[e] != 0.f ? *reinterpret_cast<const float2*>(ph + 2 + 2 * lane) : make_float2(0.f, 0.f);
+                    c[e] = fk[e] != 0.f ? *reinterpret_cast<const float2*>(ph + 2 + 64 + 2 * lane) : make_float2(0.f, 0.f);
+                }
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    o0 = make_float2(fmaf(fk[e], a[e].x, o0.x), fmaf(fk[e], a[e].y, o0.y));
+                    o1 = make_float2(fmaf(fk[e], c[e].x, o1.x), fmaf(fk[e], c[e].y, o1.y));
+                }
+            }
+            for (; k < m; ++k) {
+                const float fk = __shfl_sync(0xffffffffu, f, k);
+                if (fk != 0.f) add(slot(w0 + i0 + k), fk);
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
         const float inv = 1.f / L;
         r0 = make_float2(o0.x * inv, o0.y * inv);
         r1 = make_float2(o1.x * inv, o1.y * inv);
