@@ -152,6 +152,39 @@ def test_rotate_is_row_vector_times_rk(orc):
     assert np.abs(x[0] @ r32 - r32 @ x[0]).max() > 1.0
 
 
+def test_rotate_is_the_serial_fused_chain_from_plus_zero(orc):
+    """Closed-form cases of the write contract: each rotated channel is acc = fma(x_j, R[j][c], acc)
+    over j = 0..127 in ascending order, from acc = +0, rounding once per step (fp32, nearest-even).
+    Column 0 pins the order: x = (1, 2^-24 x 127) against a column of ones adds 2^-24 to 1 at every
+    step, an exact tie that rounds back to 1, so the result is exactly 1; any other order (or a wider
+    accumulator) adds the small terms first and gives 1 + 2^-17.  Column 1 pins the fusion:
+    acc = -(1 + 2^-11) after j = 0, then x_1 R_11 = (1 + 2^-12)^2 = 1 + 2^-11 + 2^-24, so the fused
+    step gives 2^-24 exactly while a rounded product first gives 0.  Column 2 pins the start value:
+    a chain of -1 x +0 products ends at +0 only if it starts from +0."""
+    x = np.zeros(128, np.float32)
+    r = np.zeros((128, 128), np.float32)
+    # column 0: order
+    x0 = np.full(128, 2.0 ** -24, np.float32)
+    x0[0] = 1.0
+    r[:, 0] = 1.0
+    y = orc.rotate_f32(x0, r)
+    assert y[0] == np.float32(1.0)
+    assert np.float32(np.sum(x0.astype(np.float64))) != np.float32(1.0)   # what a wider sum gives
+    # column 1: fused multiply-add
+    x1 = np.zeros(128, np.float32)
+    x1[0], x1[1] = -(1.0 + 2.0 ** -11), 1.0 + 2.0 ** -12
+    r1 = np.zeros((128, 128), np.float32)
+    r1[0, 1], r1[1, 1] = 1.0, 1.0 + 2.0 ** -12
+    y1 = orc.rotate_f32(x1, r1)
+    assert y1[1] == np.float32(2.0 ** -24)
+    assert np.float32(x1[1]) * np.float32(r1[1, 1]) + np.float32(x1[0]) == np.float32(0.0)   # split
+    # column 2: the chain starts from +0 (every product is -1 x +0 = -0; -0 + -0 stays -0, so only a
+    # +0 start ends at +0)
+    x2 = np.full(128, -1.0, np.float32)
+    y2 = orc.rotate_f32(x2, np.zeros((128, 128), np.float32))
+    assert y2[2] == 0.0 and not np.signbit(y2[2])
+
+
 # ------------------------------------------------------------------ quantiser
 
 def test_golden_grid_example(orc):
