@@ -25,6 +25,11 @@ namespace {
 
 // warps per CTA: 8 when the per-warp output partials of G <= 8 heads fit in static shared memory
 __host__ __device__ constexpr int prep_warps(int G) { return G <= 8 ? 8 : 4; }
+// BF16 sink / window tiles of 8 slots, staged per warp in two buffers by asynchronous copies: K rows
+// padded to 272 bytes (the 8 rows of an MMA fragment load then fall on all 32 banks), V rows 256 bytes
+constexpr int kKRow = 272;
+constexpr int kTileBytes = 8 * kKRow + 8 * 256;
+__host__ __device__ constexpr int prep_dyn_smem(int G) { return prep_warps(G) * 2 * kTileBytes; }
 constexpr float kQScaleP = 1.4426950408889634f * 0.08838834764831845f;   // log2(e) / sqrt(128)
 
 __device__ __forceinline__ float bf16_to_f(uint16_t b) { return __uint_as_float(((uint32_t)b) << 16); }
@@ -116,6 +121,37 @@ __device__ __forceinline__ void prep_body(const DecodeParams& p, const AppendPar
     }
     __syncthreads();
 
+    // ---- this warp's BF16 tiles (8 slots each: tiles warp, warp + kPrepWarps, ...): the first two
+    // are requested now, so that their loads overlap the query rotation; tile i + 2 is requested
+    // once tile i has been used (one commit group per tile, empty ones included)
+    extern __shared__ __align__(16) uint8_t prep_dyn[];
+    uint8_t* wbuf = prep_dyn + (size_t)warp * 2 * kTileBytes;
+    const uint16_t* kb = p.bf16 + (((size_t)p.row[b] * p.hkv + h) * 2 + 0) * kSlots * kD;
+    const uint16_t* vb = p.bf16 + (((size_t)p.row[b] * p.hkv + h) * 2 + 1) * kSlots * kD;
+    const int len = p.len[b];
+    const int n_sink = min(len, kSink), n_win = min(kWindow, max(0, len - kSink));
+    constexpr int kTiles = (kSlots / 8 + kPrepWarps - 1) / kPrepWarps;
+    auto tile_used = [&](int nt) {
+        return nt < kSlots / 8 && (slot_live(8 * nt, n_sink, n_win) || slot_live(8 * nt + 7, n_sink, n_win));
+    };
+    auto request_tile = [&](int i) {
+        const int nt = warp + kPrepWarps * i;
+        if (i < kTiles && tile_used(nt)) {
+            const uint32_t dst = ptx::smem_u32(wbuf + (i & 1) * kTileBytes);
+            // 8 rows x 256 bytes of K, then of V: 256 pieces of 16 bytes, 8 per lane
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int piece = lane + 32 * j, kv = piece >> 7, row = (piece >> 4) & 7, ch = piece & 15;
+                const uint16_t* src = (kv ? vb : kb) + (size_t)(8 * nt + row) * kD + 8 * ch;
+                const uint32_t d = dst + (kv ? 8 * kKRow + 256 * row : kKRow * row) + 16 * ch;
+                asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(src) : "memory");
+            }
+        }
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    };
+    request_tile(0);
+    request_tile(1);
+
     // ---- q~[i][col] = sum_j q[i][j] R_h[j][col]: column col of R_h, 32 rows in flight; with
     // 8 warps the two halves of the CTA take alternate heads
     {
@@ -157,8 +193,6 @@ __device__ __forceinline__ void prep_body(const DecodeParams& p, const AppendPar
     }
 
     // ---- BF16 sink + window
-    const int len = p.len[b];
-    const int n_sink = min(len, kSink), n_win = min(kWindow, max(0, len - kSink));
     // causal view (chunked prefill): head row x of query token x / g_real sees positions <= lim + x / g_real;
     // a window slot holds position w0 + ((slot - 64 - (w0 - 64)) mod 256), w0 the window's first position
     const int w0 = max(kSink, len - kWindow);
@@ -188,8 +222,6 @@ __device__ __forceinline__ void prep_body(const DecodeParams& p, const AppendPar
             qa[k][ks][3] = pack_bf16x2(lv[1][0], lv[1][1]);
         }
     }
-    const uint16_t* kb = p.bf16 + (((size_t)p.row[b] * p.hkv + h) * 2 + 0) * kSlots * kD;
-    const uint16_t* vb = p.bf16 + (((size_t)p.row[b] * p.hkv + h) * 2 + 1) * kSlots * kD;
     float m[MT], lpart[MT];           // running max of head g + 8 k (base 2); this thread's part of the sum
 #pragma unroll
     for (int k = 0; k < MT; ++k) m[k] = -INFINITY, lpart[k] = 0.f;
@@ -197,18 +229,26 @@ __device__ __forceinline__ void prep_body(const DecodeParams& p, const AppendPar
 #pragma unroll
     for (int i = 0; i < G; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
 
-    for (int nt = warp; nt < kSlots / 8; nt += kPrepWarps) {
+    for (int i = 0; i < kTiles; ++i) {
+        asm volatile("cp.async.wait_group 1;" ::: "memory");   // tile i has landed (tile i + 1 may not)
+        __syncwarp();
+        const int nt = warp + kPrepWarps * i;
+        if (!tile_used(nt)) {   // whole tile empty (or past the region)
+            request_tile(i + 2);
+            continue;
+        }
         const int s0 = 8 * nt;
-        if (!slot_live(s0, n_sink, n_win) && !slot_live(s0 + 7, n_sink, n_win)) continue;   // whole tile empty
+        const uint8_t* kbuf = wbuf + (i & 1) * kTileBytes;
+        const uint8_t* vbuf = kbuf + 8 * kKRow;
         // scores of slots s0 .. s0 + 7
         float acc[MT][4];
 #pragma unroll
         for (int k = 0; k < MT; ++k) acc[k][0] = acc[k][1] = acc[k][2] = acc[k][3] = 0.f;
-        const uint16_t* krow = kb + (size_t)(s0 + g) * kD + 2 * tig;
+        const uint8_t* krow = kbuf + g * kKRow + 4 * tig;
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
-            const uint32_t b0 = *reinterpret_cast<const uint32_t*>(krow + 16 * ks);
-            const uint32_t b1 = *reinterpret_cast<const uint32_t*>(krow + 16 * ks + 8);
+            const uint32_t b0 = *reinterpret_cast<const uint32_t*>(krow + 32 * ks);
+            const uint32_t b1 = *reinterpret_cast<const uint32_t*>(krow + 32 * ks + 16);
 #pragma unroll
             for (int k = 0; k < MT; ++k) mma_bf16(acc[k], qa[k][ks], b0, b1);
         }
@@ -242,26 +282,28 @@ __device__ __forceinline__ void prep_body(const DecodeParams& p, const AppendPar
 #pragma unroll
         for (int t = 0; t < 8; ++t) {
             const bool live = slot_live(s0 + t, n_sink, n_win);
-            const uint2 w = *reinterpret_cast<const uint2*>(vb + (size_t)(s0 + t) * kD + 4 * lane);
+            const uint2 w = *reinterpret_cast<const uint2*>(vbuf + 256 * t + 8 * lane);
             v[t][0] = live ? bf16_to_f(w.x & 0xffff) : 0.f;     // dead slots may hold anything
             v[t][1] = live ? bf16_to_f(w.x >> 16) : 0.f;
             v[t][2] = live ? bf16_to_f(w.y & 0xffff) : 0.f;
             v[t][3] = live ? bf16_to_f(w.y >> 16) : 0.f;
         }
 #pragma unroll
-        for (int i = 0; i < G; ++i) {
-            const float f = fs[warp][i];
+        for (int hd = 0; hd < G; ++hd) {
+            const float f = fs[warp][hd];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) o[i][j] *= f;
+            for (int j = 0; j < 4; ++j) o[hd][j] *= f;
 #pragma unroll
             for (int t = 0; t < 8; ++t) {
-                const float pr = ps[warp][t][i];
+                const float pr = ps[warp][t][hd];
 #pragma unroll
-                for (int j = 0; j < 4; ++j) o[i][j] = fmaf(pr, v[t][j], o[i][j]);
+                for (int j = 0; j < 4; ++j) o[hd][j] = fmaf(pr, v[t][j], o[hd][j]);
             }
         }
-        __syncwarp();
+        __syncwarp();            // every lane is done with buffer i & 1 before it is refilled
+        request_tile(i + 2);
     }
+    asm volatile("cp.async.wait_all;" ::: "memory");
 
     // ---- merge the warps' partials and write this request's BF16 partial
 #pragma unroll
@@ -315,42 +357,55 @@ __global__ void __launch_bounds__(32 * prep_warps(G)) prep_step(const __grid_con
     prep_body<G, true>(p, &a);
 }
 
-}  // namespace
-
-cudaError_t launch_prep_step(const DecodeParams& p, const AppendParams& a, cudaStream_t s) {
-    const dim3 grid(p.hkv, p.batch);
-    switch (p.g) {
-        case 1: prep_step<1><<<grid, 32 * prep_warps(1), 0, s>>>(p, a); break;
-        case 2: prep_step<2><<<grid, 32 * prep_warps(2), 0, s>>>(p, a); break;
-        case 3: prep_step<3><<<grid, 32 * prep_warps(3), 0, s>>>(p, a); break;
-        case 4: prep_step<4><<<grid, 32 * prep_warps(4), 0, s>>>(p, a); break;
-        case 5: prep_step<5><<<grid, 32 * prep_warps(5), 0, s>>>(p, a); break;
-        case 6: prep_step<6><<<grid, 32 * prep_warps(6), 0, s>>>(p, a); break;
-        case 7: prep_step<7><<<grid, 32 * prep_warps(7), 0, s>>>(p, a); break;
-        case 8: prep_step<8><<<grid, 32 * prep_warps(8), 0, s>>>(p, a); break;
-        case 12: prep_step<12><<<grid, 32 * prep_warps(12), 0, s>>>(p, a); break;
-        case 16: prep_step<16><<<grid, 32 * prep_warps(16), 0, s>>>(p, a); break;
-        default: return cudaErrorInvalidValue;
+// Launch with the per-warp tile buffers as dynamic shared memory (opted in once per device).
+template <int G, bool STEP>
+cudaError_t launch_prep_g(const DecodeParams& p, const AppendParams* a, cudaStream_t s) {
+    static bool attr_set[kMaxDevices] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    if (!attr_set[dev]) {
+        if constexpr (STEP)
+            e = cudaFuncSetAttribute(prep_step<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, prep_dyn_smem(G));
+        else
+            e = cudaFuncSetAttribute(prep<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, prep_dyn_smem(G));
+        if (e != cudaSuccess) return e;
+        attr_set[dev] = true;
     }
+    const dim3 grid(p.hkv, p.batch);
+    if constexpr (STEP)
+        prep_step<G><<<grid, 32 * prep_warps(G), prep_dyn_smem(G), s>>>(p, *a);
+    else
+        prep<G><<<grid, 32 * prep_warps(G), prep_dyn_smem(G), s>>>(p);
     return cudaGetLastError();
 }
 
-cudaError_t launch_prep(const DecodeParams& p, cudaStream_t s) {
-    const dim3 grid(p.hkv, p.batch);
+template <bool STEP>
+cudaError_t launch_prep_any(const DecodeParams& p, const AppendParams* a, cudaStream_t s) {
     switch (p.g) {
-        case 1: prep<1><<<grid, 32 * prep_warps(1), 0, s>>>(p); break;
-        case 2: prep<2><<<grid, 32 * prep_warps(2), 0, s>>>(p); break;
-        case 3: prep<3><<<grid, 32 * prep_warps(3), 0, s>>>(p); break;
-        case 4: prep<4><<<grid, 32 * prep_warps(4), 0, s>>>(p); break;
-        case 5: prep<5><<<grid, 32 * prep_warps(5), 0, s>>>(p); break;
-        case 6: prep<6><<<grid, 32 * prep_warps(6), 0, s>>>(p); break;
-        case 7: prep<7><<<grid, 32 * prep_warps(7), 0, s>>>(p); break;
-        case 8: prep<8><<<grid, 32 * prep_warps(8), 0, s>>>(p); break;
-        case 12: prep<12><<<grid, 32 * prep_warps(12), 0, s>>>(p); break;
-        case 16: prep<16><<<grid, 32 * prep_warps(16), 0, s>>>(p); break;
+        case 1: return launch_prep_g<1, STEP>(p, a, s);
+        case 2: return launch_prep_g<2, STEP>(p, a, s);
+        case 3: return launch_prep_g<3, STEP>(p, a, s);
+        case 4: return launch_prep_g<4, STEP>(p, a, s);
+        case 5: return launch_prep_g<5, STEP>(p, a, s);
+        case 6: return launch_prep_g<6, STEP>(p, a, s);
+        case 7: return launch_prep_g<7, STEP>(p, a, s);
+        case 8: return launch_prep_g<8, STEP>(p, a, s);
+        case 12: return launch_prep_g<12, STEP>(p, a, s);
+        case 16: return launch_prep_g<16, STEP>(p, a, s);
         default: return cudaErrorInvalidValue;
     }
-    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_prep_step(const DecodeParams& p, const AppendParams& a, cudaStream_t s) {
+    return launch_prep_any<true>(p, &a, s);
+}
+
+cudaError_t launch_prep(const DecodeParams& p, cudaStream_t s) {
+    return launch_prep_any<false>(p, nullptr, s);
 }
 
 }  // namespace oscar
