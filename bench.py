@@ -59,6 +59,7 @@ def parse():
     ap.add_argument("--path", default="mma", choices=["mma", "simt"],
                     help="decode kernel: warp-level MMA (default) or the SIMT baseline")
     ap.add_argument("--no-prefill", action="store_true", help="skip the chunked-prefill attention timing")
+    ap.add_argument("--no-layers", action="store_true", help="skip the multi-layer append timing")
     ap.add_argument("--unfused", action="store_true",
                     help="run each step as kv_quant_append + oscar_decode_attention instead of oscar_decode_step")
     return ap.parse_args()
@@ -461,6 +462,10 @@ def run_ours(args, cfg, rank, world, dist):
                        "ms": pms, "query_tokens_per_s": sum(nq) / (pms * 1e-3)}
             del kp, vp, qp, outp, wsp
 
+    layers = None
+    if not args.no_layers and world == 1:
+        layers = time_layer_appends(B, hq, hkv, dev)
+
     # ---- end to end: pinned host inputs in, output out, synchronised every step
     e2e = None
     if not args.no_e2e:
@@ -545,12 +550,58 @@ def run_ours(args, cfg, rank, world, dist):
                    "step_ms_outside_int2_kernel": (per_step - k_t) * 1e3},
         "calibration": calib,
         "prefill_attention": prefill,
+        "append_layers": layers,
         "clocks": clk,
         "gpu_launches": launches,
         "e2e": e2e,
         "cpu_baseline": cpu,
     }
     print(json.dumps(line), flush=True)
+
+
+def time_layer_appends(B, hq, hkv, dev, n_layers=64, L0=512, chunk=16, reps=10):
+    """Write path of one step of an n_layers-layer model: every layer's cache appends `chunk` tokens
+    per request, as one kv_quant_append_layers call or as one kv_quant_append call per layer.  Host
+    wall time per step (enqueue included, synchronised after the timed steps)."""
+    import time
+
+    import torch
+
+    import synth
+    import int2_rotated_paged_gb300 as K
+    per_seq = (L0 + chunk * (reps + 4) - 320 + 63) // 64 + 2
+    sets = [[K.Cache(B, hq, hkv, per_seq * B, per_seq) for _ in range(n_layers)] for _ in range(2)]
+    rk = torch.linalg.qr(torch.randn(hkv, 128, 128, device=dev))[0].contiguous()
+    k0, v0 = synth.kv_block(3, [L0] * B, [0] * B, hkv, device=dev)
+    for cs in sets:
+        for c in cs:
+            c.append(k0, v0, [L0] * B, rk)
+    k1, v1 = synth.kv_block(4, [chunk] * B, [L0] * B, hkv, device=dev)
+    ws = torch.empty(K.kv_quant_append_layers_workspace_bytes(n_layers), dtype=torch.uint8, device=dev)
+    n = [chunk] * B
+
+    def batched():
+        K.kv_quant_append_layers(sets[0], [k1] * n_layers, [v1] * n_layers, n, [rk] * n_layers, ws)
+
+    def per_layer():
+        for c in sets[1]:
+            c.append(k1, v1, n, rk)
+    res = {}
+    for name, f in (("batched", batched), ("per_layer", per_layer)):
+        f()
+        f()
+        torch.cuda.synchronize()
+        t = time.perf_counter()
+        for _ in range(reps):
+            f()
+        torch.cuda.synchronize()
+        res[name] = (time.perf_counter() - t) / reps * 1e3
+    del sets
+    torch.cuda.empty_cache()
+    return {"what": f"one step's write path of a {n_layers}-layer model: {chunk} new tokens per request into every "
+                    "layer's cache (host wall time per step, enqueue included)",
+            "layers": n_layers, "tokens_per_request": chunk,
+            "one_call_ms": res["batched"], "call_per_layer_ms": res["per_layer"]}
 
 
 def relaunch_under_torchrun(args) -> int:

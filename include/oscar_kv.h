@@ -186,6 +186,24 @@ int32_t kv_page_table_free_pages(const oscar_cache *c);
 int kv_quant_append(oscar_cache *c, const void *k, const void *v, const int32_t *new_tokens,
                     const float *rk, void *stream);
 
+/* kv_quant_append_layers: the same append for n_layers caches at once (the layers of one model,
+ * which append the same tokens per request), in two kernel launches in all instead of two per
+ * layer.  caches[l], k[l], v[l] and rk[l] (host arrays of n_layers entries) are layer l's cache,
+ * new keys, new values and R_K, each exactly as for kv_quant_append; new_tokens is shared.  Every
+ * cache must have the same batch, KV heads, group sizes and current lengths (OSCAR_EINVAL
+ * otherwise); clip factors may differ.  workspace (device, 16-byte aligned, at least
+ * kv_quant_append_layers_workspace_bytes(n_layers)) receives the layers' kernel parameters, so it
+ * must not be reused until the call's kernels have run.  The bytes stored are those of n_layers
+ * kv_quant_append calls.  Pages are reserved layer by layer: OSCAR_ENOPAGES for layer l leaves
+ * layers 0 .. l - 1 with pages reserved for the new tokens but no token appended anywhere.
+ * Errors: OSCAR_EINVAL, OSCAR_EALIGN, OSCAR_EWORKSPACE, OSCAR_ENOPAGES, OSCAR_ECUDA.
+ * Source: the fused write path of the axbrief.com OSCAR page, section "attention-statistics
+ * rotation + Triton kernels", applied to every layer's cache. */
+size_t kv_quant_append_layers_workspace_bytes(int32_t n_layers);
+int kv_quant_append_layers(oscar_cache *const *caches, int32_t n_layers, const void *const *k,
+                           const void *const *v, const int32_t *new_tokens, const float *const *rk,
+                           void *workspace, size_t workspace_bytes, void *stream);
+
 /* ---------------------------------------------------------------- read path
  * oscar_decode_attention: one decode query per request and query head against every
  * token the request holds.  q (device, [batch, num_q_heads, 128], OSCAR_DTYPE_F32 or

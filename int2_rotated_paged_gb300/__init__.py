@@ -32,7 +32,8 @@ EXPORTS = [
     "oscar_seq_lens_bytes", "oscar_cache_create", "oscar_cache_destroy", "oscar_cache_length",
     "kv_page_table_init", "kv_page_table_reserve", "kv_page_table_release", "kv_page_table_sync",
     "kv_page_table_read",
-    "kv_page_table_free_pages", "kv_quant_append", "oscar_decode_workspace_bytes",
+    "kv_page_table_free_pages", "kv_quant_append", "kv_quant_append_layers_workspace_bytes",
+    "kv_quant_append_layers", "oscar_decode_workspace_bytes",
     "oscar_decode_attention", "oscar_build_rk_workspace_bytes", "oscar_build_rk", "oscar_read_int2",
     "oscar_read_bf16", "oscar_strerror", "oscar_last_cuda_error", "oscar_launch_count",
     "oscar_set_decode_path", "oscar_decode_status", "oscar_decode_attention_noalloc", "oscar_decode_step",
@@ -93,6 +94,8 @@ def lib() -> ctypes.CDLL:
         "kv_page_table_read": (ctypes.c_int, [P, I32, P, I32]),
         "kv_page_table_free_pages": (I32, [P]),
         "kv_quant_append": (ctypes.c_int, [P, P, P, P, P, P]),
+        "kv_quant_append_layers_workspace_bytes": (SZ, [I32]),
+        "kv_quant_append_layers": (ctypes.c_int, [P, I32, P, P, P, P, P, SZ, P]),
         "oscar_decode_workspace_bytes": (SZ, [P]),
         "oscar_decode_attention": (ctypes.c_int, [P, P, I32, P, P, I32, P, SZ, P]),
         "oscar_build_rk_workspace_bytes": (SZ, [I32]),
@@ -203,6 +206,26 @@ def kv_page_table_read(cache, b: int, max_out: int = 1 << 20):
 def kv_quant_append(cache, k, v, new_tokens: Sequence[int], rk, stream=None):
     _check("kv_quant_append", lib().kv_quant_append(cache, _ptr(k), _ptr(v), _host_i32(new_tokens),
                                                     _ptr(rk), _stream(stream)))
+
+
+def kv_quant_append_layers_workspace_bytes(n_layers: int) -> int:
+    return int(lib().kv_quant_append_layers_workspace_bytes(n_layers))
+
+
+def kv_quant_append_layers(caches, ks, vs, new_tokens: Sequence[int], rks, workspace, stream=None):
+    """One append of new_tokens per request to every layer's cache (kv_quant_append_layers): caches,
+    ks, vs, rks are per-layer sequences (cache handles, bf16 keys, bf16 values, fp32 R_K)."""
+    n = len(caches)
+    if not (len(ks) == len(vs) == len(rks) == n):
+        raise ValueError("one key, value and R_K tensor per layer")
+    arr = lambda xs: (ctypes.c_void_p * n)(*[_ptr(x) for x in xs])
+    nbytes = workspace.numel() * workspace.element_size()
+    def handle(c):   # a Cache, a handle from oscar_cache_create, or its address
+        c = getattr(c, "handle", c)
+        return c if isinstance(c, int) else c.value
+    _check("kv_quant_append_layers", lib().kv_quant_append_layers(
+        (ctypes.c_void_p * n)(*[handle(c) for c in caches]), n,
+        arr(ks), arr(vs), _host_i32(new_tokens), arr(rks), _ptr(workspace), nbytes, _stream(stream)))
 
 
 def oscar_decode_workspace_bytes(cache) -> int:

@@ -354,6 +354,44 @@ int kv_quant_append(oscar_cache* c, const void* k, const void* v, const int32_t*
     return OSCAR_OK;
 }
 
+size_t kv_quant_append_layers_workspace_bytes(int32_t n_layers) {
+    if (n_layers < 1 || n_layers > kMaxAppendLayers) return 0;
+    return ((size_t)n_layers * sizeof(AppendParams) + 255) / 256 * 256;
+}
+
+int kv_quant_append_layers(oscar_cache* const* caches, int32_t n_layers, const void* const* k, const void* const* v,
+                           const int32_t* new_tokens, const float* const* rk, void* workspace, size_t workspace_bytes,
+                           void* stream) {
+    if (!caches || !k || !v || !rk || !new_tokens || n_layers < 1 || n_layers > kMaxAppendLayers) return OSCAR_EINVAL;
+    const oscar_cache* c0 = caches[0];
+    if (!c0) return OSCAR_EINVAL;
+    for (int32_t l = 0; l < n_layers; ++l) {
+        const oscar_cache* c = caches[l];
+        if (!c || c->d.batch != c0->d.batch || c->d.num_kv_heads != c0->d.num_kv_heads ||
+            c->fmt.gk != c0->fmt.gk || c->fmt.gv != c0->fmt.gv || c->len != c0->len)
+            return OSCAR_EINVAL;
+        for (int32_t j = 0; j < l; ++j)
+            if (caches[j] == c) return OSCAR_EINVAL;   // a cache twice would append twice
+    }
+    if (!workspace || workspace_bytes < kv_quant_append_layers_workspace_bytes(n_layers)) return OSCAR_EWORKSPACE;
+    if (!aligned16(workspace)) return OSCAR_EALIGN;
+    const cudaStream_t s = S(stream);
+    std::vector<AppendParams> ps(n_layers);
+    for (int32_t l = 0; l < n_layers; ++l) {
+        bool any = false;
+        int rc = prepare_append(caches[l], k[l], v[l], new_tokens, rk[l], s, ps[l], &any);
+        if (rc != OSCAR_OK) return rc;
+        if (!any) return OSCAR_OK;   // no token for any request (the same for every layer)
+    }
+    cudaError_t e = cudaMemcpyAsync(workspace, ps.data(), sizeof(AppendParams) * n_layers, cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    e = launch_append_layers((const AppendParams*)workspace, ps[0], n_layers, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    for (int32_t l = 0; l < n_layers; ++l)
+        for (int32_t b = 0; b < caches[l]->d.batch; ++b) caches[l]->len[b] += new_tokens[b];
+    return OSCAR_OK;
+}
+
 // ------------------------------------------------------------------ read path
 
 // request slots of a decode call: slot b is request b with its one query (identity mapping)

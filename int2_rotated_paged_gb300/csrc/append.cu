@@ -44,15 +44,13 @@ constexpr int kFew = 8;   // tokens per (page, KV head) up to which quant_few is
 
 // Appends that quantise at most kFew tokens per (page, KV head) -- every decode step: thread =
 // channel, the kFew tokens' rotation chains side by side, block-wide group min / max per token.
-__global__ void __launch_bounds__(128) quant_few(const __grid_constant__ AppendParams p) {
+__device__ __forceinline__ void quant_few_body(const AppendParams& p, const int job, const int h) {
     extern __shared__ __align__(16) float smem[];
     float* R = smem;                   // [128][128]
     float* xs = R + kD * kD;           // [kFew][128]
     float* red = xs + kFew * kD;       // [8]
     __shared__ uint8_t part[2][4][16];  // [K|V][warp][lane < 16]: half-packed code bytes of one token
 
-    const int job = blockIdx.x;
-    const int h = blockIdx.y;
     const int c = threadIdx.x;
     const int b = find_request(p, job);
     const AppendReq& r = p.req[b];
@@ -142,15 +140,13 @@ constexpr int kSPT = kPage * 16 / kQPThreads;   // page slots per thread (16 lan
 // four codes per byte are warp shuffles, with no block-wide barrier per token.
 // Keys: the 64 x 128 tile times R_K with each output the serial fmaf chain over ascending j
 // (the bit-exact contract), 4 tokens x 8 channels of independent chains per thread.
-__global__ void __launch_bounds__(kQPThreads) quant_pages(const __grid_constant__ AppendParams p) {
+__device__ __forceinline__ void quant_pages_body(const AppendParams& p, const int job, const int h) {
     extern __shared__ __align__(16) float smem[];
     float* R = smem;                   // [128][128]
     float* xt = R + kD * kD;           // [128][64]: key inputs, channel-major (xt[j][slot]); after the
                                        // rotation, the page-head block being built (full pages)
     uint16_t* vt = reinterpret_cast<uint16_t*>(xt + kD * kPage);   // [64][128]: value rows (bf16)
 
-    const int job = blockIdx.x;
-    const int h = blockIdx.y;
     const int t = threadIdx.x;
     const int tb = t >> 4, cb = t & 15;
     const int b = find_request(p, job);
@@ -327,10 +323,7 @@ __global__ void __launch_bounds__(kQPThreads) quant_pages(const __grid_constant_
 // head, K or V); the rows are copied as 16-byte pieces, all independent, so a CTA keeps many loads
 // in flight instead of one row at a time.
 constexpr int kInsThreads = 256;
-__global__ void __launch_bounds__(kInsThreads) insert_bf16(const __grid_constant__ AppendParams p) {
-    const int b = blockIdx.x;
-    const int h = blockIdx.y;
-    const int kv = blockIdx.z;
+__device__ __forceinline__ void insert_bf16_body(const AppendParams& p, const int b, const int h, const int kv) {
     const AppendReq& r = p.req[b];
     const int l1 = r.len0 + r.n_new;
     const int wstart = max(kSink, l1 - kWindow);
@@ -351,37 +344,90 @@ __global__ void __launch_bounds__(kInsThreads) insert_bf16(const __grid_constant
     if (h == 0 && kv == 0 && threadIdx.x == 0) p.seq_lens[b] = l1;
 }
 
-}  // namespace
+// Kernels.  One cache: the parameters are a kernel argument.  Several layers in one launch: one
+// parameter block per layer in device memory, the layer in blockIdx.z (blockIdx.z / 2 for the window
+// insert, whose z also selects K or V).
+__global__ void __launch_bounds__(128) quant_few(const __grid_constant__ AppendParams p) {
+    quant_few_body(p, blockIdx.x, blockIdx.y);
+}
+__global__ void __launch_bounds__(128) quant_few_layers(const AppendParams* __restrict__ ps) {
+    quant_few_body(ps[blockIdx.z], blockIdx.x, blockIdx.y);
+}
+__global__ void __launch_bounds__(kQPThreads) quant_pages(const __grid_constant__ AppendParams p) {
+    quant_pages_body(p, blockIdx.x, blockIdx.y);
+}
+__global__ void __launch_bounds__(kQPThreads) quant_pages_layers(const AppendParams* __restrict__ ps) {
+    quant_pages_body(ps[blockIdx.z], blockIdx.x, blockIdx.y);
+}
+__global__ void __launch_bounds__(kInsThreads) insert_bf16(const __grid_constant__ AppendParams p) {
+    insert_bf16_body(p, blockIdx.x, blockIdx.y, blockIdx.z);
+}
+__global__ void __launch_bounds__(kInsThreads) insert_bf16_layers(const AppendParams* __restrict__ ps) {
+    insert_bf16_body(ps[blockIdx.z >> 1], blockIdx.x, blockIdx.y, blockIdx.z & 1);
+}
 
-cudaError_t launch_append(const AppendParams& p, cudaStream_t s) {
-    // at most kFew tokens leave the window per request (every decode step): the per-channel
-    // kernel; otherwise (prefill, chunked appends) the tiled one
-    int most = 0;
-    for (int b = 0; b < p.batch; ++b) most = max(most, p.req[b].e1 - p.req[b].e0);
-    const bool few = most <= kFew;
-    const size_t smem_tiled = (size_t)(kD * kD + kD * kPage) * sizeof(float) + (size_t)kPage * kD * sizeof(uint16_t);
-    const size_t smem_few = (size_t)(kD * kD + kFew * kD + 8) * sizeof(float);
-    static bool attr_set[kMaxDevices] = {};   // once per device
+constexpr size_t kSmemTiled = (size_t)(kD * kD + kD * kPage) * sizeof(float) + (size_t)kPage * kD * sizeof(uint16_t);
+constexpr size_t kSmemFew = (size_t)(kD * kD + kFew * kD + 8) * sizeof(float);
+
+// dynamic shared-memory opt-in of the quantisation kernels, once per device
+cudaError_t append_attrs() {
+    static bool attr_set[kMaxDevices] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
     if (!attr_set[dev]) {
-        e = cudaFuncSetAttribute(quant_pages, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_tiled);
+        e = cudaFuncSetAttribute(quant_pages, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemTiled);
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(quant_few, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_few);
+            e = cudaFuncSetAttribute(quant_pages_layers, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemTiled);
+        if (e == cudaSuccess) e = cudaFuncSetAttribute(quant_few, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemFew);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(quant_few_layers, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemFew);
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
+    return cudaSuccess;
+}
+
+// at most kFew tokens leave the window per request (every decode step): the per-channel kernel;
+// otherwise (prefill, chunked appends) the tiled one
+bool few_tokens(const AppendParams& p) {
+    int most = 0;
+    for (int b = 0; b < p.batch; ++b) most = max(most, p.req[b].e1 - p.req[b].e0);
+    return most <= kFew;
+}
+
+}  // namespace
+
+cudaError_t launch_append(const AppendParams& p, cudaStream_t s) {
+    cudaError_t e = append_attrs();
+    if (e != cudaSuccess) return e;
     int n = 0;
     if (p.n_jobs > 0) {
-        if (few)
-            quant_few<<<dim3(p.n_jobs, p.hkv), 128, smem_few, s>>>(p);
+        if (few_tokens(p))
+            quant_few<<<dim3(p.n_jobs, p.hkv), 128, kSmemFew, s>>>(p);
         else
-            quant_pages<<<dim3(p.n_jobs, p.hkv), kQPThreads, smem_tiled, s>>>(p);
+            quant_pages<<<dim3(p.n_jobs, p.hkv), kQPThreads, kSmemTiled, s>>>(p);
         ++n;
     }
     insert_bf16<<<dim3(p.batch, p.hkv, 2), kInsThreads, 0, s>>>(p);
+    ++n;
+    count_launches(n);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_append_layers(const AppendParams* dev_params, const AppendParams& p0, int n_layers, cudaStream_t s) {
+    cudaError_t e = append_attrs();
+    if (e != cudaSuccess) return e;
+    int n = 0;
+    if (p0.n_jobs > 0) {
+        if (few_tokens(p0))
+            quant_few_layers<<<dim3(p0.n_jobs, p0.hkv, n_layers), 128, kSmemFew, s>>>(dev_params);
+        else
+            quant_pages_layers<<<dim3(p0.n_jobs, p0.hkv, n_layers), kQPThreads, kSmemTiled, s>>>(dev_params);
+        ++n;
+    }
+    insert_bf16_layers<<<dim3(p0.batch, p0.hkv, 2 * n_layers), kInsThreads, 0, s>>>(dev_params);
     ++n;
     count_launches(n);
     return cudaGetLastError();

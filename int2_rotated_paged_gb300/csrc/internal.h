@@ -17,6 +17,7 @@ constexpr int kSink = 64;          // BF16 sink tokens
 constexpr int kWindow = 256;       // BF16 recent-window tokens
 constexpr int kSlots = kSink + kWindow;
 constexpr int kMaxBatch = 256;     // requests per call (kernel-parameter tables)
+constexpr int kMaxAppendLayers = 4096;   // caches per kv_quant_append_layers call (grid z = 2 x layers)
 constexpr int kMaxG = 16;          // query heads per KV head
 constexpr int kMaxDevices = 64;    // devices whose per-device launch settings are cached
 
@@ -157,6 +158,9 @@ constexpr int kMaxMmaUnits = 2048;     // units of one warp-MMA launch (partial-
 
 // Launchers (each returns the cudaError_t of its launch).
 cudaError_t launch_append(const AppendParams& p, cudaStream_t s);
+// The same for several caches (layers) that append the same tokens per request: parameter blocks in
+// device memory (dev_params[layer]); p0 is layer 0's host copy (grid sizes, kernel choice).
+cudaError_t launch_append_layers(const AppendParams* dev_params, const AppendParams& p0, int n_layers, cudaStream_t s);
 // timing: null, or two events recorded on `s` around the INT2 attention kernel's launch
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t s, cudaEvent_t* timing = nullptr);
 cudaError_t launch_decode_mma(const DecodeParams& p, cudaStream_t s);
