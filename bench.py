@@ -489,6 +489,10 @@ def run_ours(args, cfg, rank, world, dist):
         e_bytes = 0
         enqueue = 0.0
         lens_e = [cache.length(b) for b in range(B)]
+        # the fused step takes the host buffers itself (oscar_decode_step_host: copies in, step, copy out)
+        qd_e = K.DTYPE_BF16 if qs[0].dtype == torch.bfloat16 else K.DTYPE_F32
+        staging = None if args.unfused else torch.empty(
+            K.oscar_decode_step_host_staging_bytes(cache.handle, qd_e, K.DTYPE_F32), dtype=torch.uint8, device=dev)
         for s in range(args.warmup + args.steps):
             if s == args.warmup:
                 if dist is not None:
@@ -496,9 +500,14 @@ def run_ours(args, cfg, rank, world, dist):
                 torch.cuda.synchronize()
                 w0 = time.perf_counter()
             h0 = time.perf_counter()
-            d_in.copy_(h_in[s], non_blocking=True)
-            step_call(dk, dv, dq)
-            host_out.copy_(out, non_blocking=True)
+            if staging is not None:
+                a = h_in[s].data_ptr()
+                K.oscar_decode_step_host(cache.handle, a + nq, a + nq + nk, a, qd_e, rk, host_out, K.DTYPE_F32,
+                                         staging, cache.workspace, stream)
+            else:
+                d_in.copy_(h_in[s], non_blocking=True)
+                step_call(dk, dv, dq)
+                host_out.copy_(out, non_blocking=True)
             if s >= args.warmup:
                 enqueue += time.perf_counter() - h0
             stream.synchronize()
@@ -508,7 +517,11 @@ def run_ours(args, cfg, rank, world, dist):
         welapsed = w1 - w0
         welapsed = max_over_ranks(welapsed, dist, dev)
         h2d = d_in.numel()
-        e2e = {"value": e_bytes * world / welapsed / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+        e2e = {"call": ("oscar_decode_step_host on page-locked host q, k, v and output (copies in, fused step, "
+                        "copy out)" if staging is not None else
+                        "host-to-device copy, kv_quant_append + oscar_decode_attention, device-to-host copy") +
+                       ", stream synchronised every step",
+               "value": e_bytes * world / welapsed / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": host_out.numel() * host_out.element_size(),
                "ms_per_step": welapsed / args.steps * 1e3,
                "host_enqueue_ms_per_step": enqueue / args.steps * 1e3}

@@ -244,6 +244,23 @@ int oscar_decode_step(oscar_cache *c, const void *k, const void *v, const void *
                       const float *rk, void *out, int32_t out_dtype, void *workspace,
                       size_t workspace_bytes, void *stream);
 
+/* oscar_decode_step_host: oscar_decode_step with the step's inputs and output in host memory.  It
+ * enqueues on stream the copies of k_host and v_host (bf16 [batch, num_kv_heads, 128]) and q_host
+ * (q_dtype [batch, num_q_heads, 128]) into the device buffer staging, oscar_decode_step on those
+ * copies, and the copy of the output (out_dtype [batch, num_q_heads, 128]) to out_host.  Nothing
+ * waits: out_host holds the result once the stream has passed the call (synchronise the stream, or
+ * an event recorded after the call).  Host buffers in page-locked memory keep the copies
+ * asynchronous; pageable memory works, but its copies wait for the host.  staging (device, 16-byte
+ * aligned, >= oscar_decode_step_host_staging_bytes(c, q_dtype, out_dtype) bytes; 0 for invalid
+ * arguments) must not be reused until the stream has passed the call.  Results, cache contents and
+ * errors are those of oscar_decode_step on device copies of the inputs; argument errors
+ * (OSCAR_EINVAL for a NULL host pointer, OSCAR_EWORKSPACE for a short staging buffer) are found before
+ * anything is enqueued. */
+size_t oscar_decode_step_host_staging_bytes(const oscar_cache *c, int32_t q_dtype, int32_t out_dtype);
+int oscar_decode_step_host(oscar_cache *c, const void *k_host, const void *v_host, const void *q_host,
+                           int32_t q_dtype, const float *rk, void *out_host, int32_t out_dtype, void *staging,
+                           size_t staging_bytes, void *workspace, size_t workspace_bytes, void *stream);
+
 /* oscar_prefill_attention: attention of the queries of a chunk of new tokens (chunked prefill).
  * Each request b must have just appended its last n_q[b] tokens (host array, 0 <= n_q[b] <= 256 and
  * <= its length) through kv_quant_append; q (device, [sum_b n_q[b]][num_q_heads][128], requests in

@@ -33,7 +33,8 @@ EXPORTS = [
     "kv_page_table_init", "kv_page_table_reserve", "kv_page_table_release", "kv_page_table_sync",
     "kv_page_table_read",
     "kv_page_table_free_pages", "kv_quant_append", "kv_quant_append_layers_workspace_bytes",
-    "kv_quant_append_layers", "oscar_decode_workspace_bytes",
+    "kv_quant_append_layers", "oscar_decode_workspace_bytes", "oscar_decode_step_host_staging_bytes",
+    "oscar_decode_step_host",
     "oscar_decode_attention", "oscar_build_rk_workspace_bytes", "oscar_build_rk", "oscar_read_int2",
     "oscar_read_bf16", "oscar_strerror", "oscar_last_cuda_error", "oscar_launch_count",
     "oscar_set_decode_path", "oscar_decode_status", "oscar_decode_attention_noalloc", "oscar_decode_step",
@@ -96,6 +97,8 @@ def lib() -> ctypes.CDLL:
         "kv_quant_append": (ctypes.c_int, [P, P, P, P, P, P]),
         "kv_quant_append_layers_workspace_bytes": (SZ, [I32]),
         "kv_quant_append_layers": (ctypes.c_int, [P, I32, P, P, P, P, P, SZ, P]),
+        "oscar_decode_step_host_staging_bytes": (SZ, [P, I32, I32]),
+        "oscar_decode_step_host": (ctypes.c_int, [P, P, P, P, I32, P, P, I32, P, SZ, P, SZ, P]),
         "oscar_decode_workspace_bytes": (SZ, [P]),
         "oscar_decode_attention": (ctypes.c_int, [P, P, I32, P, P, I32, P, SZ, P]),
         "oscar_build_rk_workspace_bytes": (SZ, [I32]),
@@ -226,6 +229,21 @@ def kv_quant_append_layers(caches, ks, vs, new_tokens: Sequence[int], rks, works
     _check("kv_quant_append_layers", lib().kv_quant_append_layers(
         (ctypes.c_void_p * n)(*[handle(c) for c in caches]), n,
         arr(ks), arr(vs), _host_i32(new_tokens), arr(rks), _ptr(workspace), nbytes, _stream(stream)))
+
+
+def oscar_decode_step_host_staging_bytes(cache, q_dtype: int, out_dtype: int) -> int:
+    return int(lib().oscar_decode_step_host_staging_bytes(cache, q_dtype, out_dtype))
+
+
+def oscar_decode_step_host(cache, k_host, v_host, q_host, q_dtype: int, rk, out_host, out_dtype: int, staging, workspace,
+                           stream=None):
+    """oscar_decode_step on host buffers (pinned tensors or host addresses): copies in, step, copy out,
+    all enqueued; the output is in out_host once the stream has passed the call."""
+    sbytes = staging.numel() * staging.element_size()
+    wbytes = workspace.numel() * workspace.element_size()
+    _check("oscar_decode_step_host", lib().oscar_decode_step_host(
+        cache, _ptr(k_host), _ptr(v_host), _ptr(q_host), q_dtype, _ptr(rk), _ptr(out_host), out_dtype,
+        _ptr(staging), sbytes, _ptr(workspace), wbytes, _stream(stream)))
 
 
 def oscar_decode_workspace_bytes(cache) -> int:

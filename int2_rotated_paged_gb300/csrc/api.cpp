@@ -611,6 +611,56 @@ int oscar_decode_step(oscar_cache* c, const void* k, const void* v, const void* 
     return e == cudaSuccess ? OSCAR_OK : cuda_fail(e);
 }
 
+// Device staging of oscar_decode_step_host: keys, values, queries, output (256-byte aligned parts).
+struct StepStaging {
+    size_t kv_bytes, q_bytes, out_bytes;
+    size_t k, v, q, out, total;
+};
+static StepStaging step_staging(const oscar_cache* c, int32_t q_dtype, int32_t out_dtype) {
+    auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+    StepStaging st;
+    st.kv_bytes = (size_t)c->d.batch * c->d.num_kv_heads * kD * sizeof(uint16_t);
+    st.q_bytes = (size_t)c->d.batch * c->d.num_q_heads * kD * (q_dtype == OSCAR_DTYPE_BF16 ? 2 : 4);
+    st.out_bytes = (size_t)c->d.batch * c->d.num_q_heads * kD * (out_dtype == OSCAR_DTYPE_BF16 ? 2 : 4);
+    st.k = 0;
+    st.v = up(st.kv_bytes);
+    st.q = st.v + up(st.kv_bytes);
+    st.out = st.q + up(st.q_bytes);
+    st.total = st.out + up(st.out_bytes);
+    return st;
+}
+
+size_t oscar_decode_step_host_staging_bytes(const oscar_cache* c, int32_t q_dtype, int32_t out_dtype) {
+    if (!c || (q_dtype != OSCAR_DTYPE_F32 && q_dtype != OSCAR_DTYPE_BF16) ||
+        (out_dtype != OSCAR_DTYPE_F32 && out_dtype != OSCAR_DTYPE_BF16))
+        return 0;
+    return step_staging(c, q_dtype, out_dtype).total;
+}
+
+int oscar_decode_step_host(oscar_cache* c, const void* k_host, const void* v_host, const void* q_host, int32_t q_dtype,
+                           const float* rk, void* out_host, int32_t out_dtype, void* staging, size_t staging_bytes,
+                           void* workspace, size_t workspace_bytes, void* stream) {
+    if (!c || !k_host || !v_host || !q_host || !out_host) return OSCAR_EINVAL;
+    const size_t need = oscar_decode_step_host_staging_bytes(c, q_dtype, out_dtype);
+    if (need == 0) return OSCAR_EINVAL;
+    if (!staging || staging_bytes < need) return OSCAR_EWORKSPACE;
+    if (!aligned16(staging)) return OSCAR_EALIGN;
+    const StepStaging st = step_staging(c, q_dtype, out_dtype);
+    uint8_t* sb = (uint8_t*)staging;
+    int rc = check_decode_args(c, sb + st.q, q_dtype, rk, sb + st.out, out_dtype, workspace, workspace_bytes);
+    if (rc != OSCAR_OK) return rc;
+    const cudaStream_t s = S(stream);
+    cudaError_t e = cudaMemcpyAsync(sb + st.k, k_host, st.kv_bytes, cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(sb + st.v, v_host, st.kv_bytes, cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(sb + st.q, q_host, st.q_bytes, cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    rc = oscar_decode_step(c, sb + st.k, sb + st.v, sb + st.q, q_dtype, rk, sb + st.out, out_dtype, workspace,
+                           workspace_bytes, stream);
+    if (rc != OSCAR_OK) return rc;
+    e = cudaMemcpyAsync(out_host, sb + st.out, st.out_bytes, cudaMemcpyDeviceToHost, s);
+    return e == cudaSuccess ? OSCAR_OK : cuda_fail(e);
+}
+
 int oscar_kernel_timing(oscar_cache* c, int32_t capacity) {
     if (!c || capacity < 0 || capacity > (1 << 20)) return OSCAR_EINVAL;
     free_timing(c);

@@ -49,3 +49,51 @@ def test_fused_step_matches_append_then_attend(path, hq, hkv, lens):
         one.status()
     finally:
         K.oscar_set_decode_path(K.PATH_WARP_MMA)
+
+
+@pytest.mark.parametrize("pinned", [True, False])
+def test_host_buffer_step_matches_device_step(pinned):
+    # oscar_decode_step_host: the step's q, k, v and output in host memory (page-locked or pageable);
+    # outputs and cache bytes must equal those of oscar_decode_step on device copies
+    hq, hkv, lens, steps = 16, 2, [900, 330, 2000], 12
+    cfg = synth.LayerConfig("host", len(lens), hq, hkv, lens, steps, "permuted", "bf16", 4712)
+    rk = torch.tensor(oracle_rk(cfg.seed, hkv, 1024), device="cuda")
+    dev_c = make_cache(cfg, max(lens) + steps + 64)
+    host_c = make_cache(cfg, max(lens) + steps + 64)
+    for c in (dev_c, host_c):
+        c.pool.zero_()
+        append_initial(c, cfg, lens, rk)
+    B = len(lens)
+    out_dev = torch.empty(B, hq, 128, device="cuda")
+    out_host = torch.empty(B, hq, 128, pin_memory=pinned)
+    staging = None
+    for s in range(steps):
+        q = synth.queries(cfg.seed, s, B, hq, hkv, dtype="bf16", device="cuda").to(torch.bfloat16)
+        k, v = synth.kv_block(cfg.seed, [1] * B, [lens[b] + s for b in range(B)], hkv, device="cuda")
+        dev_c.step(k, v, q, rk, out_dev)
+        if staging is None:
+            staging = torch.empty(K.oscar_decode_step_host_staging_bytes(host_c.handle, K.DTYPE_BF16, K.DTYPE_F32),
+                                  dtype=torch.uint8, device="cuda")
+        qh, kh, vh = (t.contiguous().cpu() for t in (q, k, v))
+        if pinned:
+            qh, kh, vh = qh.pin_memory(), kh.pin_memory(), vh.pin_memory()
+        assert qh.dtype == torch.bfloat16 and kh.dtype == torch.bfloat16
+        K.oscar_decode_step_host(host_c.handle, kh, vh, qh, K.DTYPE_BF16, rk, out_host, K.DTYPE_F32, staging,
+                                 host_c.workspace)
+        torch.cuda.synchronize()
+        assert torch.equal(out_dev.cpu(), out_host), f"step {s}"
+    for name in ("seq_lens", "page_table", "pool", "bf16"):
+        assert torch.equal(getattr(dev_c, name), getattr(host_c, name)), name
+    host_c.status()
+    # argument errors before anything is enqueued: a short staging buffer, a missing host buffer
+    qh = torch.zeros(B, hq, 128, dtype=torch.bfloat16)
+    kh = torch.zeros(B, hkv, 128, dtype=torch.bfloat16)
+    with pytest.raises(K.OscarError) as e:
+        K.oscar_decode_step_host(host_c.handle, kh, kh, qh, K.DTYPE_BF16, rk, out_host, K.DTYPE_F32, staging[:256],
+                                 host_c.workspace)
+    assert e.value.code == K.OSCAR_EWORKSPACE
+    with pytest.raises(K.OscarError) as e:
+        K.oscar_decode_step_host(host_c.handle, kh, None, qh, K.DTYPE_BF16, rk, out_host, K.DTYPE_F32, staging,
+                                 host_c.workspace)
+    assert e.value.code == K.OSCAR_EINVAL
+    assert [host_c.length(b) for b in range(B)] == [n + steps for n in lens]
