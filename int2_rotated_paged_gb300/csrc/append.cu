@@ -15,6 +15,9 @@
 // Stream order makes kernel 1 read the window before kernel 2 overwrites it.  A decode step made
 // through oscar_decode_step does the same work for its one token per request inside prep_step
 // (prep.cu) with the per-token quantisation of token_quant.h, which quant_few uses as well.
+// kv_quant_append_layers runs the same two kernels once for all layers of a model (the *_layers
+// forms: one parameter block per layer in device memory, the layer in blockIdx.z).  Every writer
+// also raises the (request, KV head)'s recorded largest value scale (AppendParams::vmax).
 //
 // Bit-exact contract (shared with nothing but the written specification): the key
 // rotation is the serial chain acc = fma(x_j, R[j][c], acc), j = 0..127, acc0 = +0;

@@ -9,10 +9,12 @@
 //      section "OSCAR release": BF16 sink and recent window), written as one split-K partial
 //      (reference max, sum, unnormalised output) that combine merges with the INT2 partials.
 // Scores of the BF16 part run on mma.sync m16n8k16 with bf16 operands: A = the query (rows: the
-// bf16 high part of 8 heads, then their bf16 low parts, ~16 bits in all), B = key rows read
-// straight from the BF16 region (a fragment register is two adjacent channels of one token).
-// The online softmax runs per warp over 8-slot tiles; P.V runs on the CUDA cores with the
-// probabilities shared through shared memory (lane = 4 output channels).
+// bf16 high part of 8 heads, then their bf16 low parts, ~16 bits in all), B = key rows (a fragment
+// register is two adjacent channels of one token).  Each warp takes every kPrepWarps-th 8-slot tile
+// and stages its K and V rows in two shared-memory buffers by asynchronous copies, the first two
+// tiles requested before the query rotation so that their loads overlap it.  The online softmax
+// runs per warp over the tiles; P.V runs on the CUDA cores with the probabilities shared through
+// shared memory (lane = 4 output channels).
 // All softmax arithmetic is in base 2 (logits pre-scaled by log2(e) / sqrt(128)).
 #include <cuda_bf16.h>
 
