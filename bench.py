@@ -560,6 +560,9 @@ def run_ours(args, cfg, rank, world, dist):
                      "timing": "CUDA events recorded by the library on the launching stream around each launch",
                      "call": {"what": call_what, "bytes": dec_bytes, "ms": dec_t * 1e3, "gbs": dec_bytes / dec_t / 1e9}},
         "append": {"prefill_tokens_per_s": tok_append / t_append, "prefill_tokens": tok_append,
+                   # the two bounds of the bulk write path: FP32 FMA for the serial key rotation
+                   # (128 x 128 per token-head) and HBM (512 bytes read + 80 written per token-head)
+                   **write_path_fractions(tok_append * hkv / t_append, dev, clk, peak),
                    "step_ms_outside_int2_kernel": (per_step - k_t) * 1e3},
         "calibration": calib,
         "prefill_attention": prefill,
@@ -570,6 +573,24 @@ def run_ours(args, cfg, rank, world, dist):
         "cpu_baseline": cpu,
     }
     print(json.dumps(line), flush=True)
+
+
+def write_path_fractions(token_heads_per_s, dev, clk, hbm_peak):
+    """Bulk-prefill throughput against its two bounds: the FP32 FMA rate (SMs x 128 FMA per clock x the
+    maximum SM clock sampled, else 2070 MHz) that the 16384 FMA of each key rotation need, and HBM
+    (592 algorithmic bytes per token-head against the measured copy peak)."""
+    import torch
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    mhz = (clk or {}).get("sm_max_mhz") or 2070.0
+    fma_peak = sms * 128 * mhz * 1e6
+    fma = token_heads_per_s * ROTATION_FMA_PER_TOKEN_HEAD
+    gbs = token_heads_per_s * 592 / 1e9
+    return {"fp32_fma_per_s": fma, "fp32_fma_peak": fma_peak, "fp32_fma_frac": fma / fma_peak,
+            "fp32_fma_peak_rule": f"{sms} SMs x 128 FP32 FMA per clock x {mhz:.0f} MHz",
+            "hbm_gbs": gbs, "hbm_frac": gbs / hbm_peak}
+
+
+ROTATION_FMA_PER_TOKEN_HEAD = 128 * 128
 
 
 def time_layer_appends(B, hq, hkv, dev, n_layers=64, L0=512, chunk=16, reps=10):
