@@ -536,6 +536,12 @@ def run_ours(args, cfg, rank, world, dist):
                "sample": f"four decode steps (append 1 token + attend, fp64) of {len(pairs)} of {B * hkv} "
                          f"(request, KV head) pairs at full context on {threads} threads, "
                          f"{sum(times):.1f} s wall ({sum(times) * threads:.0f} thread-s)"}
+        if threads > 1:
+            # the same oracle on one host thread (one pair, two steps: a smaller sample of the same work)
+            nb1, t1, _, _ = cpu_oracle_sample(cfg, lens0, 1, reps=2, threads=1)
+            cpu["single_thread"] = {"value": sum(nb1) / sum(t1) / 1e9, "unit": "GB/s", "cores": 1,
+                                    "sample": "two decode steps of 1 (request, KV head) pair at full context, "
+                                              f"{sum(t1):.1f} s"}
     kname = dict(mma="decode_mma", simt="split_simt")[args.path]
     if args.unfused or args.path != "mma":
         call_what = (f"oscar_decode_attention: prep (q rotation + BF16 sink/window attention) + {kname} + combine"
