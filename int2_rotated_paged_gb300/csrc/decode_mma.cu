@@ -37,10 +37,10 @@
 //            channel tile cm carrying 4^(cm mod 4) * 2^-24 (removed when the partial is
 //            written); B = P' = p * s_V (fp16, columns = 8 heads) straight from the score
 //            accumulators' register layout.  Centred values: one more MMA per k-step sums the
-//            same fp16 P' (A = a selector of ones), and after each page the output takes
-//            -1.5 times that sum, so it accumulates P' (code - 1.5), a zero-mean factor that keeps
-//            the rounding of P' from adding up over long nearly flat attention; the minimum term
-//            sum_t p (m_V + 1.5 s_V) runs on the CUDA cores.
+//            same fp16 P' (A = those P' registers; B = ones that pick the value group), and after
+//            each page the output takes -1.5 times that sum, so it accumulates P' (code - 1.5), a
+//            zero-mean factor that keeps the rounding of P' from adding up over long nearly flat
+//            attention; the minimum term sum_t p (m_V + 1.5 s_V) runs on the CUDA cores.
 // Tokens are in natural order everywhere: n-tile nt of a chunk holds tokens 8 nt .. 8 nt + 7,
 // and PV k-step kk takes n-tiles 2 kk (k 0..7) and 2 kk + 1 (k 8..15).  At the end of each
 // (request, KV head) run the warp writes (reference max, sum, unnormalised output) to the
@@ -215,8 +215,8 @@ __global__ void __launch_bounds__(32 * warps_for(G), 1) decode_mma(const __grid_
     // tau - 7.5, so the dominant probabilities sit about 2^7.5 below the limit.  tau lives in shared
     // memory (sm->tau[warp]): it is set once per segment and read once per chunk.
     float o[8][MT][4];              // output^T accumulators: channel tile cm, head tile nh
-    // sum of P' over the current page: rows g (value group 0) and g + 8 (group 1) of one MMA
-    // accumulator, heads 2 tig, 2 tig + 1
+    // sums of P' over the current page for this thread's head g (+ 8 k) and value group tig / 2:
+    // [0] over the first 8 tokens of each k-step, [2] over the last 8 ([1], [3] repeat them)
     float psum[MT][4];
     PageIt it;
     it.init(p, P0);
@@ -460,6 +460,10 @@ __global__ void __launch_bounds__(32 * warps_for(G), 1) decode_mma(const __grid_
                         lsum[k] = __fmul2_rn(lsum[k], f2);
                         mv[k][0] = __fmul2_rn(mv[k][0], f2);
                         mv[k][1] = __fmul2_rn(mv[k][1], f2);
+                        psum[k][0] *= fown[k];
+                        psum[k][1] *= fown[k];
+                        psum[k][2] *= fown[k];
+                        psum[k][3] *= fown[k];
                     }
                 }
                 fresh = false;
@@ -480,10 +484,6 @@ __global__ void __launch_bounds__(32 * warps_for(G), 1) decode_mma(const __grid_
                         o[c][k][2] *= f0;
                         o[c][k][3] *= f1;
                     }
-                    psum[k][0] *= f0;
-                    psum[k][1] *= f1;
-                    psum[k][2] *= f0;
-                    psum[k][3] *= f1;
                 }
             }
         };
@@ -548,16 +548,20 @@ __global__ void __launch_bounds__(32 * warps_for(G), 1) decode_mma(const __grid_
                         OSCAR_PV_STEP(3)
 #undef OSCAR_PV_STEP
                     }
-                // the page's sum of P', exactly as the output MMAs see it: B = group 0's P' of an
-                // n-tile in k 0..7 and group 1's in k 8..15, A = 1 on (rows 0..7, k 0..7) and
-                // (rows 8..15, k 8..15), 0 elsewhere
-                const uint32_t sel[4] = {0x3C003C00u, 0u, 0u, 0x3C003C00u};
+                // the page's sums of P', of exactly the fp16 values the output MMAs see.  A = the
+                // output MMAs' B registers of the k-step in their own order, so row g holds head g's
+                // P' of tokens 0..7 (group 0 in k 0..7, group 1 in k 8..15) and row g + 8 those of
+                // tokens 8..15; B = 1 on (k 0..7, columns 0..3) and (k 8..15, columns 4..7).  Result
+                // columns 0..3 then sum group 0 and columns 4..7 group 1, each over half the tokens
+                // in rows g and g + 8
+                const uint32_t sb0 = (g < 4) ? 0x3C003C00u : 0u, sb1 = (g < 4) ? 0u : 0x3C003C00u;
 #pragma unroll
                 for (int kk = 0; kk < KK; ++kk)
 #pragma unroll
-                    for (int hf = 0; hf < 2; ++hf)
-#pragma unroll
-                        for (int k = 0; k < MT; ++k) mma16816(psum[k], sel, pb[0][kk][k][hf], pb[1][kk][k][hf]);
+                    for (int k = 0; k < MT; ++k) {
+                        const uint32_t pa[4] = {pb[0][kk][k][0], pb[0][kk][k][1], pb[1][kk][k][0], pb[1][kk][k][1]};
+                        mma16816(psum[k], pa, sb0, sb1);
+                    }
             }
         };
         constexpr int NC = kPage / CT;
@@ -586,14 +590,25 @@ __global__ void __launch_bounds__(32 * warps_for(G), 1) decode_mma(const __grid_
         }
 
         // ---- centre the page's output: -1.5 P' per head and value group, in the units of channel
-        // tile cm (4^(cm mod 4) 2^-24), then start the next page's sum
+        // tile cm (4^(cm mod 4) 2^-24), then start the next page's sum.  O^T holds heads 2 tig,
+        // 2 tig + 1 (+ 8 k); the sum of head h's group q sits in lane 4 h + 2 q
+        float ps_a[MT][2], ps_b[MT][2];
+#pragma unroll
+        for (int k = 0; k < MT; ++k) {
+            const float t = psum[k][0] + psum[k][2];
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                ps_a[k][q] = __shfl_sync(0xffffffffu, t, (2 * tig) * 4 + 2 * q);
+                ps_b[k][q] = __shfl_sync(0xffffffffu, t, (2 * tig + 1) * 4 + 2 * q);
+            }
+        }
 #pragma unroll
         for (int cm = 0; cm < 8; ++cm) {
             const float c = -1.5f * (float)(1 << (2 * (cm & 3))) * 5.9604644775390625e-08f;   // -1.5 * 4^r * 2^-24
             const int q = cm >> 2;
 #pragma unroll
             for (int k = 0; k < MT; ++k) {
-                const float2 sq = make_float2(psum[k][2 * q], psum[k][2 * q + 1]);
+                const float2 sq = make_float2(ps_a[k][q], ps_b[k][q]);
                 const float2 cc = make_float2(c, c);
                 const float2 a = __ffma2_rn(cc, sq, make_float2(o[cm][k][0], o[cm][k][1]));
                 const float2 b = __ffma2_rn(cc, sq, make_float2(o[cm][k][2], o[cm][k][3]));
