@@ -16,7 +16,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "liboscar_kv.so")
-SOURCES = ["api.cpp", "append.cu", "decode.cu", "prep.cu", "decode_mma.cu", "calib.cu", "noalloc.cu"]
+SOURCES = ["api.cpp", "append.cu", "decode.cu", "prep.cu", "decode_mma.cu", "decode_mma_t.cu", "calib.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", os.path.join(ROOT, "include")]
 

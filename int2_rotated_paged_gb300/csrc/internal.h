@@ -164,6 +164,9 @@ cudaError_t launch_append_layers(const AppendParams* dev_params, const AppendPar
 // timing: null, or two events recorded on `s` around the INT2 attention kernel's launch
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t s, cudaEvent_t* timing = nullptr);
 cudaError_t launch_decode_mma(const DecodeParams& p, cudaStream_t s);
+// the transposed-score kernel (decode_mma_t.cu) for the head counts it serves: G <= 4 and G = 12
+bool decode_mma_t_serves(int g);
+cudaError_t launch_decode_mma_t(const DecodeParams& p, cudaStream_t s);
 cudaError_t launch_prep(const DecodeParams& p, cudaStream_t s);
 cudaError_t launch_prep_step(const DecodeParams& p, const AppendParams& a, cudaStream_t s);
 // fused decode step (warp-MMA path): prep with the append of one token per request, then the INT2
