@@ -110,11 +110,12 @@ def peaks():
 
 def kernel_source_hash():
     """Hash of the sources that decide the INT2 attention kernel's memory traffic: the kernel's
-    device code, its copy helpers and the page layout / parameter structs of internal.h (host-side
+    device code and the helpers it shares with the transposed-score kernel, its copy helpers and
+    the page layout / parameter structs of internal.h (host-side
     launchers and their declarations are left out), with comments and blank space removed so that
     editing a comment keeps the recorded counters valid."""
     h = hashlib.sha256()
-    for name in ("decode_mma.cu", "ptx_async.h", "internal.h"):
+    for name in ("decode_mma.cu", "decode_mma_common.h", "ptx_async.h", "internal.h"):
         text = open(os.path.join(ROOT, "int2_rotated_paged_gb300", "csrc", name)).read()
         if name == "internal.h":
             text = text[:text.index("cudaError_t launch_")]

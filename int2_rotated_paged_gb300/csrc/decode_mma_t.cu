@@ -421,13 +421,13 @@ __global__ void __launch_bounds__(32 * warps_t(G), 1) decode_mma_t(const __grid_
                     for (int mo = 0; mo < MO; ++mo) {
                         uint32_t xa = __shfl_sync(0xffffffffu, pk[u][2 * mo], srcA);
                         uint32_t xb = __shfl_sync(0xffffffffu, pk[u][2 * mo], srcB);
+                        // (heads past the last head tile, g >= 4 there, take copies of real P': their
+                        // output columns and page sums are finite and never written out)
                         if (2 * mo + 1 < NS) {
                             const int j1 = 2 * mo + 1 < NS ? 2 * mo + 1 : 0;
                             const uint32_t ya = __shfl_sync(0xffffffffu, pk[u][j1], srcA);
                             const uint32_t yb = __shfl_sync(0xffffffffu, pk[u][j1], srcB);
                             if (g >= 4) xa = ya, xb = yb;
-                        } else if (g >= 4) {
-                            xa = xb = 0u;      // heads past G: zero columns
                         }
                         pb[u][m][mo][0] = __byte_perm(xa, xb, 0x5410);
                         pb[u][m][mo][1] = __byte_perm(xa, xb, 0x7632);
