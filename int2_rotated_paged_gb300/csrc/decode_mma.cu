@@ -46,6 +46,9 @@
 // (request, KV head) run the warp writes (reference max, sum, unnormalised output) to the
 // split-K partial buffer.
 //
+// Head counts whose query rows would leave MMA rows empty (G <= 4, G = 12) run the transposed-score
+// kernel of decode_mma_t.cu instead.
+//
 // mbarrier waits are bounded; on timeout the kernel records an error word and the warp stops.
 #include <cuda_fp16.h>
 
