@@ -410,7 +410,8 @@ class Cache:
         self.seq_lens = torch.zeros(sizes[3] // 4, dtype=torch.int32, device=device)
         self.handle = oscar_cache_create(d, self.pool, self.bf16, self.page_table, self.seq_lens)
         kv_page_table_init(self.handle, page_order)
-        self.workspace = torch.empty(oscar_decode_workspace_bytes(self.handle), dtype=torch.uint8,
+        # zeroed once, so that status() before the first decode call reads a clear error word
+        self.workspace = torch.zeros(oscar_decode_workspace_bytes(self.handle), dtype=torch.uint8,
                                      device=device)
 
     def __del__(self):

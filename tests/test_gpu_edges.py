@@ -12,7 +12,8 @@ never produce:
     of their range.
 Codes and fp16 scale/min are checked bit for bit, the BF16 region byte for byte, and attention
 within rel-L2 1e-3 / max-abs 2e-3 against the oracle's fp64 attention on the same cache, on both
-decode kernels, through bulk appends and through fused decode steps (oscar_decode_step).
+decode paths (G = 4 and 12 run the warp-MMA path's transposed-score kernel, G = 8 its query-as-A
+kernel), through bulk appends and through fused decode steps (oscar_decode_step).
 Source of the quantiser: axbrief.com OSCAR page, section "attention-statistics rotation + Triton
 kernels" (per-token asymmetric INT2 in 64-channel groups, clip factors c_K, c_V).
 """
@@ -175,7 +176,7 @@ def _run(hq, hkv, lens, kfn, vfn, qfn, rk, clip=(0.96, 0.92), steps=3, chunks=No
 
 
 @pytest.mark.parametrize("clip", [(1.0, 1.0), (0.96, 0.92)])
-@pytest.mark.parametrize("hq,hkv", [(16, 2), (24, 2)])
+@pytest.mark.parametrize("hq,hkv", [(8, 2), (16, 2), (24, 2)])
 def test_edge_groups_bit_exact_and_attention(clip, hq, hkv):
     rk = np.stack([signed_permutation(11 + h) for h in range(hkv)])
 
@@ -223,7 +224,7 @@ SCALES = [("k", 1e-5), ("k", 1e-3), ("k", 1e-1), ("k", 10.0), ("k", 100.0),
           ("q", 1e-5), ("q", 1e-3), ("q", 1e-1), ("q", 10.0), ("q", 100.0), ("q", 1e3)]
 
 
-@pytest.mark.parametrize("hq,hkv", [(16, 2), (24, 2)])
+@pytest.mark.parametrize("hq,hkv", [(8, 2), (16, 2), (24, 2)])
 @pytest.mark.parametrize("which,factor", SCALES)
 def test_scaled_inputs(which, factor, hq, hkv):
     seed = 4321

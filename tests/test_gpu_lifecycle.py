@@ -111,7 +111,8 @@ def test_release_refill_decode_and_prefill_cycles():
         lens1 = [cache.length(b) for b in range(B)]
         q = torch.tensor(rng.standard_normal((max(1, sum(nq)), HQ, D)).astype(np.float32), device="cuda")
         out = torch.empty_like(q)
-        cache.prefill(q, nq, rk_dev, out)
+        ws = cache.prefill(q, nq, rk_dev, out)
+        K.oscar_decode_status(cache.handle, ws)    # no bounded wait gave up
         torch.cuda.synchronize()
         rows, last, r = [], {}, 0
         for b in range(B):

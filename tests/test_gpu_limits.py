@@ -99,8 +99,8 @@ def test_prefill_slots_over_two_launches():
     qg = torch.Generator(device="cpu").manual_seed(seed + 1)
     q = (torch.randn(sum(n_q), hq, 128, generator=qg) * 0.7).cuda()
     out = torch.full_like(q, float("nan"))
-    cache.prefill(q, n_q, rk_dev, out)
-    cache.status()
+    ws = cache.prefill(q, n_q, rk_dev, out)
+    K.oscar_decode_status(cache.handle, ws)        # the error word of the workspace the prefill used
     torch.cuda.synchronize()
     got, qh = out.cpu().numpy(), q.cpu().numpy()
     assert np.isfinite(got).all()

@@ -126,7 +126,7 @@ def test_lengths_at_region_and_page_edges(lens):
     _run(cfg, lens, steps=3)
 
 
-@pytest.mark.parametrize("hq,hkv", [(2, 2), (8, 2), (16, 2), (24, 2), (32, 2), (12, 2), (14, 2)])
+@pytest.mark.parametrize("hq,hkv", [(2, 2), (4, 2), (6, 2), (8, 2), (16, 2), (24, 2), (32, 2), (12, 2), (14, 2)])
 def test_gqa_group_sizes(hq, hkv):
     base = synth.config("qwen3_4b")
     cfg = synth.LayerConfig("gqa", 2, hq, hkv, [1500, 900], 2, "permuted", "bf16", 4242)
