@@ -637,7 +637,7 @@ cudaError_t launch_mma_g(const DecodeParams& p, cudaStream_t s) {
 
 }  // namespace
 
-int mma_units_per_cta(int g) { return warps_for(g); }
+int mma_units_per_cta(int g) { return decode_mma_t_serves(g) ? mma_t_units_per_cta(g) : warps_for(g); }
 
 cudaError_t launch_decode_mma(const DecodeParams& p, cudaStream_t s) {
     if (p.total_pages == 0) return cudaSuccess;

@@ -14,8 +14,8 @@
 // 16-token m-tile: the softmax runs on real heads only, its per-token work packed as (g, g + 8)
 // pairs on f32x2 FMAs.  P' = p * s_V is packed per lane as the fp16 pair (token g, token g + 8)
 // and moved into the output MMA's B layout (tokens 2 tig, 2 tig + 1 of head g) with two shuffles
-// per register.  From there on (output MMAs O^T += V^T P'^T, the page sums of P', the centred
-// values, the partial results) the kernel is decode_mma.cu's.
+// and one byte permute per register.  From there on (output MMAs O^T += V^T P'^T, the page sums of
+// P', the centred values, the partial results) the kernel is decode_mma.cu's.
 //
 // mbarrier waits are bounded; on timeout the kernel records an error word and the warp stops.
 #include "decode_mma_common.h"
@@ -640,6 +640,7 @@ cudaError_t launch_t_g(const DecodeParams& p, cudaStream_t s) {
 }  // namespace
 
 bool decode_mma_t_serves(int g) { return g <= 4 || g == 12; }
+int mma_t_units_per_cta(int g) { return warps_t(g); }
 
 cudaError_t launch_decode_mma_t(const DecodeParams& p, cudaStream_t s) {
     switch (p.g) {

@@ -166,6 +166,7 @@ cudaError_t launch_decode(const DecodeParams& p, cudaStream_t s, cudaEvent_t* ti
 cudaError_t launch_decode_mma(const DecodeParams& p, cudaStream_t s);
 // the transposed-score kernel (decode_mma_t.cu) for the head counts it serves: G <= 4 and G = 12
 bool decode_mma_t_serves(int g);
+int mma_t_units_per_cta(int g);   // warps per CTA of the transposed-score kernel
 cudaError_t launch_decode_mma_t(const DecodeParams& p, cudaStream_t s);
 cudaError_t launch_prep(const DecodeParams& p, cudaStream_t s);
 cudaError_t launch_prep_step(const DecodeParams& p, const AppendParams& a, cudaStream_t s);
