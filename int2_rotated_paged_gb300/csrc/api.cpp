@@ -438,7 +438,7 @@ static int sm_count() {
     return cached[dev];
 }
 
-// Page-streaming units (warp pairs) of the warp-MMA kernel: one CTA per SM (fewer when there are few pages).
+// Page-streaming units (warps) of the warp-MMA kernel: one CTA per SM (fewer when there are few pages).
 static int mma_unit_count(int32_t g, int64_t pages, int32_t* n_units) {
     const int sms = sm_count();
     if (sms <= 0) return cuda_fail(cudaGetLastError());

@@ -122,7 +122,7 @@ struct DecodeParams {
     int32_t wait_probe;    // nonzero: the first kernel also waits on a barrier nothing arrives at
     // warp-MMA path
     int32_t total_pages;   // INT2 pages over all (request, KV head)
-    int32_t n_units;       // page-streaming units (warp pairs) of the warp-MMA kernel
+    int32_t n_units;       // page-streaming units (warps) of the warp-MMA kernel
     int32_t page_off[kMaxBatch + 1];   // sum over earlier requests of pages * hkv
     // Request slots and query rows.  Slot b of a launch reads the page-table row, BF16 region and
     // cached tokens of request row[b] (len[b] is that request's length); its g query rows are qpr
@@ -174,7 +174,7 @@ cudaError_t launch_prep_step(const DecodeParams& p, const AppendParams& a, cudaS
 // attention and the combine
 cudaError_t launch_decode_step(const DecodeParams& p, const AppendParams& a, cudaStream_t s,
                                cudaEvent_t* timing = nullptr);
-int mma_units_per_cta(int g);   // units (warp pairs) per CTA of the warp-MMA kernel for G heads per KV head
+int mma_units_per_cta(int g);   // warps per CTA of the warp-MMA decode kernel that serves G heads per KV head
 cudaError_t launch_build_rk(const float* q, int64_t n, int hkv, float* rk, void* ws, cudaStream_t s);
 size_t build_rk_ws_bytes(int hkv);
 size_t cq_acc_bytes(int hkv);
