@@ -154,44 +154,70 @@ __device__ __forceinline__ void prep_body(const DecodeParams& p, const AppendPar
     request_tile(0);
     request_tile(1);
 
-    // ---- q~[i][col] = sum_j q[i][j] R_h[j][col]: column col of R_h, 32 rows in flight; with
-    // 8 warps the two halves of the CTA take alternate heads
+    // ---- q~[i][col] = sum_j q[i][j] R_h[j][col]: column col of R_h, 32 rows in flight.  With 8
+    // warps the two halves of the CTA split the rows (each R_K entry is loaded once per CTA) and
+    // add their partial sums; with 4 warps one thread takes a whole column.  The leaving key takes
+    // the same R_K loads: k~_col = serial fmaf chain over ascending j from +0, which with 8 warps the
+    // first half runs over rows 0..63 and the second continues over rows 64..127 from that value
+    float acck = 0.f;
     {
-        constexpr int HS = kPrepWarps / 4;           // head stride
-        const int col = c & (kD - 1), h0 = c / kD;
-        float acc[(G + HS - 1) / HS];
+        const int col = c & (kD - 1), hf = c / kD;
+        constexpr int kRows = kPrepWarps == 8 ? kD / 2 : kD;
+        float acc[G];
 #pragma unroll
-        for (int i = 0; i < (G + HS - 1) / HS; ++i) acc[i] = 0.f;
-        // the leaving key takes the same R_K loads: k~_col = serial fmaf chain over ascending j from +0
-        float acck = 0.f;
+        for (int i = 0; i < G; ++i) acc[i] = 0.f;
         const float* R = p.rk + (size_t)h * kD * kD + col;
-        for (int j0 = 0; j0 < kD; j0 += 32) {
+        const int jb = hf * kRows;
+        for (int j0 = jb; j0 < jb + kRows; j0 += 32) {
             float r[32];
 #pragma unroll
             for (int j = 0; j < 32; ++j) r[j] = __ldg(R + (size_t)(j0 + j) * kD);
 #pragma unroll
             for (int j = 0; j < 32; ++j)
 #pragma unroll
-                for (int i = 0; i < (G + HS - 1) / HS; ++i)
-                    if (h0 + HS * i < G) acc[i] = fmaf(qs[h0 + HS * i][j0 + j], r[j], acc[i]);
-            if (evict) {
+                for (int i = 0; i < G; ++i) acc[i] = fmaf(qs[i][j0 + j], r[j], acc[i]);
+            if (evict && hf == 0) {
 #pragma unroll
                 for (int j = 0; j < 32; ++j) acck = __fmaf_rn(xk[j0 + j], r[j], acck);
             }
         }
+        if constexpr (kPrepWarps == 8) {
+            // the output partials' space is free until the BF16 part: the second half's sums, then
+            // the key's chain value at row 64
+            float* part2 = &ow[0][0][0];
+            if (hf == 1) {
 #pragma unroll
-        for (int i = 0; i < (G + HS - 1) / HS; ++i)
-            if (h0 + HS * i < G) p.qrot[qbase + (size_t)(h0 + HS * i) * kD + col] = acc[i];
-        if (evict) {
-            // clip, quantise and pack the leaving token into its INT2 slot (threads c < 128 hold
-            // channel c; thread c >= 128 of an 8-warp CTA only takes part in the barriers)
-            const AppendReq& r = ap->req[b];
-            const int pg = (r.e0 - kSink) / kPage;
-            const int phys = ap->page_table[(size_t)b * ap->max_pps + pg];
-            uint8_t* blk = ap->pool + ((size_t)phys * p.hkv + h) * ap->fmt.bytes;
-            tq::store_token(blk, ap->fmt, (r.e0 - kSink) % kPage, c < kD ? acck : 0.f, yv, ap->clip_k, ap->clip_v, red,
-                            tpart, ap->vmax + (size_t)b * p.hkv + h);
+                for (int i = 0; i < G; ++i) part2[i * kD + col] = acc[i];
+            } else if (evict) {
+                part2[G * kD + col] = acck;
+            }
+            __syncthreads();
+            if (hf == 0) {
+#pragma unroll
+                for (int i = 0; i < G; ++i) p.qrot[qbase + (size_t)i * kD + col] = acc[i] + part2[i * kD + col];
+            } else if (evict) {
+                float k2 = part2[G * kD + col];
+#pragma unroll 8
+                for (int j = kD / 2; j < kD; ++j) k2 = __fmaf_rn(xk[j], __ldg(R + (size_t)j * kD), k2);
+                part2[G * kD + col] = k2;
+            }
+            // every read of the partial sums is done before any warp writes its output partial here
+            __syncthreads();
+            if (evict) acck = part2[G * kD + (c & (kD - 1))];
+        } else {
+#pragma unroll
+            for (int i = 0; i < G; ++i) p.qrot[qbase + (size_t)i * kD + col] = acc[i];
         }
+    }
+    if (evict) {
+        // clip, quantise and pack the leaving token into its INT2 slot (threads c < 128 hold
+        // channel c; thread c >= 128 of an 8-warp CTA only takes part in the barriers)
+        const AppendReq& r = ap->req[b];
+        const int pg = (r.e0 - kSink) / kPage;
+        const int phys = ap->page_table[(size_t)b * ap->max_pps + pg];
+        uint8_t* blk = ap->pool + ((size_t)phys * p.hkv + h) * ap->fmt.bytes;
+        tq::store_token(blk, ap->fmt, (r.e0 - kSink) % kPage, c < kD ? acck : 0.f, yv, ap->clip_k, ap->clip_v, red,
+                        tpart, ap->vmax + (size_t)b * p.hkv + h);
     }
 
     // ---- BF16 sink + window
