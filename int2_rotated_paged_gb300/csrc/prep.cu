@@ -27,10 +27,10 @@ namespace {
 
 // warps per CTA: 8 when the per-warp output partials of G <= 8 heads fit in static shared memory
 __host__ __device__ constexpr int prep_warps(int G) { return G <= 8 ? 8 : 4; }
-// BF16 sink / window tiles of 8 slots, staged per warp in two buffers by asynchronous copies: K rows
-// padded to 272 bytes (the 8 rows of an MMA fragment load then fall on all 32 banks), V rows 256 bytes
+// BF16 sink / window tiles of 8 slots, staged per warp in two buffers by asynchronous copies: K and V
+// rows padded to 272 bytes (the 8 rows of an MMA fragment load or of an ldmatrix fall on all 32 banks)
 constexpr int kKRow = 272;
-constexpr int kTileBytes = 8 * kKRow + 8 * 256;
+constexpr int kTileBytes = 16 * kKRow;
 __host__ __device__ constexpr int prep_dyn_smem(int G) { return prep_warps(G) * 2 * kTileBytes; }
 constexpr float kQScaleP = 1.4426950408889634f * 0.08838834764831845f;   // log2(e) / sqrt(128)
 
@@ -58,6 +58,21 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], 
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// m16n8k8 with bf16 operands: A = rows g, g + 8 at k 2 tig, 2 tig + 1; B = k 2 tig, 2 tig + 1 of column g
+__device__ __forceinline__ void mma_bf16_k8(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t b0) {
+    asm("mma.sync.aligned.m16n8k8.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5}, {%6}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(b0));
+}
+
+// four 8 x 8 b16 matrices from shared memory, transposed: lanes 8 i .. 8 i + 7 give the row addresses
+// of matrix i; matrix i's element (row 2 tig + e, column g) lands in half e of register i of lane (g, tig)
+__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t (&r)[4], uint32_t addr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+
 // slot s of the BF16 region holds a token of a request of length len
 __device__ __forceinline__ bool slot_live(int s, int n_sink, int n_win) {
     return s < n_sink || (s >= kSink && s < kSink + n_win);
@@ -72,8 +87,6 @@ __device__ __forceinline__ void prep_body(const DecodeParams& p, const AppendPar
     constexpr int kPrepWarps = prep_warps(G);
     constexpr int NT = 32 * kPrepWarps;
     __shared__ float qs[G][kD];                      // plain queries
-    __shared__ float ps[kPrepWarps][8][8 * MT];      // probabilities of a warp's current tile [slot][head]
-    __shared__ float fs[kPrepWarps][8 * MT];         // rescale of a warp's running sums [head]
     __shared__ float mw[kPrepWarps][G], lw[kPrepWarps][G];
     __shared__ float ow[kPrepWarps][G][kD];
     const int h = blockIdx.x, b = blockIdx.y, c = threadIdx.x;
@@ -145,7 +158,7 @@ __device__ __forceinline__ void prep_body(const DecodeParams& p, const AppendPar
             for (int j = 0; j < 8; ++j) {
                 const int piece = lane + 32 * j, kv = piece >> 7, row = (piece >> 4) & 7, ch = piece & 15;
                 const uint16_t* src = (kv ? vb : kb) + (size_t)(8 * nt + row) * kD + 8 * ch;
-                const uint32_t d = dst + (kv ? 8 * kKRow + 256 * row : kKRow * row) + 16 * ch;
+                const uint32_t d = dst + (kv ? 8 * kKRow : 0) + kKRow * row + 16 * ch;
                 asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(src) : "memory");
             }
         }
@@ -253,9 +266,12 @@ __device__ __forceinline__ void prep_body(const DecodeParams& p, const AppendPar
     float m[MT], lpart[MT];           // running max of head g + 8 k (base 2); this thread's part of the sum
 #pragma unroll
     for (int k = 0; k < MT; ++k) m[k] = -INFINITY, lpart[k] = 0.f;
-    float o[G][4];                    // unnormalised output, channels 4 lane .. 4 lane + 3
+    // unnormalised output^T: channel tile cm (channels 16 cm + g, + 8) x heads 8 k + 2 tig, + 1
+    float o[8][MT][4];
 #pragma unroll
-    for (int i = 0; i < G; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    for (int cm = 0; cm < 8; ++cm)
+#pragma unroll
+        for (int k = 0; k < MT; ++k) o[cm][k][0] = o[cm][k][1] = o[cm][k][2] = o[cm][k][3] = 0.f;
 
     for (int i = 0; i < kTiles; ++i) {
         asm volatile("cp.async.wait_group 1;" ::: "memory");   // tile i has landed (tile i + 1 may not)
@@ -280,7 +296,10 @@ __device__ __forceinline__ void prep_body(const DecodeParams& p, const AppendPar
 #pragma unroll
             for (int k = 0; k < MT; ++k) mma_bf16(acc[k], qa[k][ks], b0, b1);
         }
-        // online softmax of head g + 8 k over the tile's slots 2 tig, 2 tig + 1
+        // online softmax of head g + 8 k over the tile's slots 2 tig, 2 tig + 1; the probabilities stay
+        // in the score layout, which is the B operand of the P.V MMA (k = slot, n = head)
+        uint32_t phi[MT], plo[MT];
+        float fk[MT];
 #pragma unroll
         for (int k = 0; k < MT; ++k) {
             float x[2];
@@ -300,32 +319,50 @@ __device__ __forceinline__ void prep_body(const DecodeParams& p, const AppendPar
             const float p0 = none ? 0.f : exp2_approx(x[0] - mn), p1 = none ? 0.f : exp2_approx(x[1] - mn);
             lpart[k] = fmaf(lpart[k], f, p0 + p1);
             m[k] = mn;
-            ps[warp][2 * tig][g + 8 * k] = p0;
-            ps[warp][2 * tig + 1][g + 8 * k] = p1;
-            if (tig == 0) fs[warp][g + 8 * k] = f;
+            fk[k] = f;
+            // p = high + low part in bf16 (about 16 significant bits)
+            const float h0 = __bfloat162float(__float2bfloat16_rn(p0)), h1 = __bfloat162float(__float2bfloat16_rn(p1));
+            phi[k] = pack_bf16x2(h0, h1);
+            plo[k] = pack_bf16x2(p0 - h0, p1 - h1);
         }
-        __syncwarp();
-        // P.V on the CUDA cores
-        float v[8][4];
+        // value rows of slots outside the sink and window may hold any bits (NaN included), which an MMA
+        // with P = 0 would still carry into the output: zero them first.  A tile lies wholly in the sink
+        // or wholly in the window region, so its live slots are one run from its first slot
+        if (!slot_live(s0 + 7, n_sink, n_win)) {
 #pragma unroll
-        for (int t = 0; t < 8; ++t) {
-            const bool live = slot_live(s0 + t, n_sink, n_win);
-            const uint2 w = *reinterpret_cast<const uint2*>(vbuf + 256 * t + 8 * lane);
-            v[t][0] = live ? bf16_to_f(w.x & 0xffff) : 0.f;     // dead slots may hold anything
-            v[t][1] = live ? bf16_to_f(w.x >> 16) : 0.f;
-            v[t][2] = live ? bf16_to_f(w.y & 0xffff) : 0.f;
-            v[t][3] = live ? bf16_to_f(w.y >> 16) : 0.f;
+            for (int q = 0; q < 4; ++q) {
+                const int idx = lane + 32 * q, t = idx >> 4, piece = idx & 15;
+                if (!slot_live(s0 + t, n_sink, n_win))
+                    *reinterpret_cast<uint4*>(const_cast<uint8_t*>(vbuf) + kKRow * t + 16 * piece) = make_uint4(0u, 0u, 0u, 0u);
+            }
+            __syncwarp();
         }
+        // rescale the output columns (heads 8 k + 2 tig + e; their factors sit in row groups 2 tig + e)
 #pragma unroll
-        for (int hd = 0; hd < G; ++hd) {
-            const float f = fs[warp][hd];
+        for (int k = 0; k < MT; ++k) {
+            const float f0 = __shfl_sync(0xffffffffu, fk[k], (2 * tig) * 4);
+            const float f1 = __shfl_sync(0xffffffffu, fk[k], (2 * tig + 1) * 4);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) o[hd][j] *= f;
+            for (int cm = 0; cm < 8; ++cm) {
+                o[cm][k][0] *= f0;
+                o[cm][k][1] *= f1;
+                o[cm][k][2] *= f0;
+                o[cm][k][3] *= f1;
+            }
+        }
+        // P.V on the tensor cores: O^T += V^T P^T, A = V^T of 16 channels (ldmatrix, transposed),
+        // B = P high and low parts
+        const uint32_t vaddr = ptx::smem_u32(vbuf) + kKRow * (lane & 7) + 16 * (lane >> 3);
 #pragma unroll
-            for (int t = 0; t < 8; ++t) {
-                const float pr = ps[warp][t][hd];
+        for (int cp = 0; cp < 4; ++cp) {
+            uint32_t a[4];
+            ldmatrix_x4_trans(a, vaddr + 64 * cp);
 #pragma unroll
-                for (int j = 0; j < 4; ++j) o[hd][j] = fmaf(pr, v[t][j], o[hd][j]);
+            for (int k = 0; k < MT; ++k) {
+                mma_bf16_k8(o[2 * cp][k], a[0], a[1], phi[k]);
+                mma_bf16_k8(o[2 * cp][k], a[0], a[1], plo[k]);
+                mma_bf16_k8(o[2 * cp + 1][k], a[2], a[3], phi[k]);
+                mma_bf16_k8(o[2 * cp + 1][k], a[2], a[3], plo[k]);
             }
         }
         __syncwarp();            // every lane is done with buffer i & 1 before it is refilled
@@ -346,9 +383,17 @@ __device__ __forceinline__ void prep_body(const DecodeParams& p, const AppendPar
         }
     }
 #pragma unroll
-    for (int i = 0; i < G; ++i)
+    for (int cm = 0; cm < 8; ++cm)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) ow[warp][i][4 * lane + j] = o[i][j];
+        for (int k = 0; k < MT; ++k)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int hd = 8 * k + 2 * tig + e;
+                if (hd < G) {
+                    ow[warp][hd][16 * cm + g] = o[cm][k][e];
+                    ow[warp][hd][16 * cm + g + 8] = o[cm][k][2 + e];
+                }
+            }
     __syncthreads();
     float* part = p.part_bf16 + ((size_t)b * p.hkv + h) * G * (2 + kD);
     const int col = c & (kD - 1);
