@@ -489,6 +489,7 @@ def run_ours(args, cfg, rank, world, dist):
         dv = d_in[nq + nk:].view(vs[0].dtype).view(vs[0].shape)
         e_bytes = 0
         enqueue = 0.0
+        enq_steps, wall_steps = [], []       # per timed step: host enqueue, and enqueue to synchronised
         lens_e = [cache.length(b) for b in range(B)]
         # the fused step takes the host buffers itself (oscar_decode_step_host: copies in, step, copy out)
         qd_e = K.DTYPE_BF16 if qs[0].dtype == torch.bfloat16 else K.DTYPE_F32
@@ -511,8 +512,10 @@ def run_ours(args, cfg, rank, world, dist):
                 host_out.copy_(out, non_blocking=True)
             if s >= args.warmup:
                 enqueue += time.perf_counter() - h0
+                enq_steps.append(time.perf_counter() - h0)
             stream.synchronize()
             if s >= args.warmup:
+                wall_steps.append(time.perf_counter() - h0)
                 e_bytes += decode_bytes([lens_e[b] + s + 1 for b in range(B)], hkv, hq)
         w1 = time.perf_counter()
         welapsed = w1 - w0
@@ -525,7 +528,11 @@ def run_ours(args, cfg, rank, world, dist):
                "value": e_bytes * world / welapsed / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": host_out.numel() * host_out.element_size(),
                "ms_per_step": welapsed / args.steps * 1e3,
-               "host_enqueue_ms_per_step": enqueue / args.steps * 1e3}
+               "host_enqueue_ms_per_step": enqueue / args.steps * 1e3,
+               # spread of the per-step host times, so that a stall of the host shows as such
+               "step_ms_median": 1e3 * sorted(wall_steps)[len(wall_steps) // 2] if wall_steps else None,
+               "step_ms_max": 1e3 * max(wall_steps) if wall_steps else None,
+               "host_enqueue_ms_max": 1e3 * max(enq_steps) if enq_steps else None}
 
     if rank != 0:
         return
