@@ -214,7 +214,8 @@ __device__ __forceinline__ void prep_body(const DecodeParams& p, const AppendPar
                 for (int j = kD / 2; j < kD; ++j) k2 = __fmaf_rn(xk[j], __ldg(R + (size_t)j * kD), k2);
                 part2[G * kD + col] = k2;
             }
-            // every read of the partial sums is done before any warp writes its output partial here
+            // the partial sums are read before this barrier and the key's value right after it, ahead of
+            // store_token's barriers: all before any warp writes its output partial into this space
             __syncthreads();
             if (evict) acck = part2[G * kD + (c & (kD - 1))];
         } else {
