@@ -359,3 +359,44 @@ def test_value_rotation_built_on_gpu_and_a_layer_stored_through_it():
             plain, _ = op.attend(q[b, h * g:(h + 1) * g].cpu().numpy())
             err_rot, err_plain = rel_l2(absorbed, exact), rel_l2(plain @ wo[h], exact)
             assert err_rot < 2.0 * err_plain + 0.01, (err_rot, err_plain)
+
+
+@pytest.mark.parametrize("base", ["qwen3_4b", "qwen3_32b"])
+def test_stale_nan_bf16_slots(base, decode_path):
+    # The BF16 region starts as NaN bits, as a caller's uninitialised buffer may.  Slots the requests
+    # have not reached (the rest of a partly filled sink or window tile) must not reach the attention:
+    # the warp-MMA path runs P.V on the tensor cores, where a zero probability times NaN is still NaN.
+    # Requests of 5 and 63 tokens end inside the sink, 70 and 300 inside the window; G = 4 and 8.
+    lens = [5, 63, 70, 300]
+    cfg = synth.scaled(synth.config(base), lens, batch=len(lens))
+    rk = oracle_rk(cfg.seed, cfg.num_kv_heads, 1024)
+    rk_dev = torch.tensor(rk, device="cuda")
+    cache = make_cache(cfg, max(lens) + 2)
+    cache.bf16.fill_(float("nan"))
+    append_initial(cache, cfg, lens, rk_dev)
+    pairs = [(b, h) for b in range(cfg.batch) for h in range(cfg.num_kv_heads)]
+    ocs = oracle_caches(cfg, pairs, lens, rk)
+    q = decode_query(cfg, 0)
+    out = _attend(cache, q, rk_dev)
+    assert np.isfinite(out).all()
+    _check_attention(out, q, ocs, cfg)
+    if decode_path == "mma":
+        # chunked prefill over the same cache: the last n_q tokens of each request as the chunk
+        n_q = [min(x, 4) for x in lens]
+        g = cfg.group
+        qg = torch.Generator(device="cpu").manual_seed(cfg.seed + 7)
+        qp = (torch.randn(sum(n_q), cfg.num_q_heads, 128, generator=qg) * 0.7).cuda()
+        po = torch.full_like(qp, float("nan"))
+        ws = cache.prefill(qp, n_q, rk_dev, po)
+        K.oscar_decode_status(cache.handle, ws)
+        torch.cuda.synchronize()
+        got, qh = po.cpu().numpy(), qp.cpu().numpy()
+        assert np.isfinite(got).all()
+        r0 = 0
+        for b in range(cfg.batch):
+            for h in range(cfg.num_kv_heads):
+                for i in range(n_q[b]):
+                    ref, _ = ocs[(b, h)].attend_upto(qh[r0 + i, h * g:(h + 1) * g], lens[b] - n_q[b] + i)
+                    o = got[r0 + i, h * g:(h + 1) * g]
+                    assert rel_l2(o, ref) <= REL_L2 and np.abs(o - ref).max() <= MAX_ABS, (b, h, i)
+            r0 += n_q[b]
