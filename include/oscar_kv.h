@@ -126,7 +126,9 @@ size_t oscar_seq_lens_bytes(const oscar_cache_desc *d);
  * above).  The handle keeps the pointers but never frees them.  All requests start
  * empty and the free list hands out physical pages 0, 1, 2, ... until
  * kv_page_table_init() sets another order.  Nothing is enqueued; the first sync
- * clears the device page table and lengths.
+ * clears the device page table and lengths.  pool and bf16 need no initial contents:
+ * whatever bits sit in slots and pages a request has not reached (NaN included) never
+ * reach a result.
  * Errors: OSCAR_EINVAL (bad descriptor or NULL), OSCAR_EALIGN. */
 int oscar_cache_create(const oscar_cache_desc *d, void *pool, void *bf16, int32_t *page_table,
                        int32_t *seq_lens, oscar_cache **out);
